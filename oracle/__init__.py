@@ -1,0 +1,264 @@
+"""Plain fp64 CPU oracle for one batched DDTree draft-tree round.
+
+TEST INFRASTRUCTURE. Only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package. The
+product path (the CUDA library and its binding) never imports it, and the two
+share no code; only the seeded input generators feed both.
+
+The arithmetic lives in ``oracle.c`` (plain C, IEEE double). This module only
+marshals numpy arrays into it. bf16 tensors travel as their raw 16-bit
+patterns (``numpy.uint16``) and are widened exactly inside the C code.
+
+Pages cited (by title and section):
+  "SparklingTree: 30-40% faster speculative decoding over DSpark",
+      "How is the tree actually created?", Steps 1-4.
+  "DDTree Explained: From Block Diffusion to Optimal Diffusion Draft Trees
+      for Speculative Decoding", sections 3-5 (Prop. 1, Prop. 2, Lemma 1,
+      Algorithm 1, implementation highlights).
+  "Robot2050/TreeSpark", item 4 and the batched engine description.
+
+Parity status: every function here is pinned by a ``-m "not gpu"`` test
+against something other than itself (closed forms, brute force, library
+routines for special cases, the pages' printed numbers).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+NAN_SEEN = 1
+BAD_ARG = 2
+BAD_PAGE = 4
+
+_lib = None
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+        L.orc_topk_logprobs.argtypes = [p, i32, i64, i64, i32, p, p, p]
+        L.orc_topk_logprobs.restype = i32
+        L.orc_build_tree.argtypes = [p, p, i32, i32, i32, i32, p, p, p, p, p, p]
+        L.orc_build_tree.restype = i32
+        L.orc_build_tree_bruteforce.argtypes = [p, p, i32, i32, i32, i64, p, p, p, p, p, p]
+        L.orc_build_tree_bruteforce.restype = i64
+        L.orc_build_mask.argtypes = [p, p, i32, i32, p]
+        L.orc_build_mask.restype = None
+        L.orc_tree_attention_rows.argtypes = [p, p, p, p, p, p, i32, i64, p, p, i32, i32,
+                                              i32, i32, i32, i32, dbl, p, i64, p]
+        L.orc_tree_attention_rows.restype = i32
+        L.orc_argmax.argtypes = [p, i32, i64, i64, p]
+        L.orc_argmax.restype = i32
+        L.orc_walk.argtypes = [p, p, p, p, i32, i32, i32, p, p, p, p]
+        L.orc_walk.restype = None
+        L.orc_compact.argtypes = [p, p, p, i32, i64, p, p, p, p, p, i32, i32, i32, i32, i32, i32]
+        L.orc_compact.restype = i32
+        L.orc_num_threads.argtypes = []
+        L.orc_num_threads.restype = i32
+        _lib = L
+    return _lib
+
+
+def num_threads() -> int:
+    return int(lib().orc_num_threads())
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logit_dtype(a):
+    if a.dtype == np.float32:
+        return 0
+    if a.dtype == np.uint16:
+        return 1
+    if a.dtype == np.float64:
+        return 2
+    raise TypeError("logits must be float32, float64 or bf16 bits (uint16), got %s" % a.dtype)
+
+
+def topk_logprobs(z, K):
+    """Per row of z [..., V]: (lp [..., K] fp64, ids [..., K] int32, logZ [...], flags).
+
+    lp = z - logsumexp(z); ids are the K largest logits, value descending,
+    equal values by lower id.
+    """
+    z = np.ascontiguousarray(z)
+    V = z.shape[-1]
+    rows = int(np.prod(z.shape[:-1]))
+    lp = np.empty(z.shape[:-1] + (K,), np.float64)
+    ids = np.empty(z.shape[:-1] + (K,), np.int32)
+    logz = np.empty(z.shape[:-1], np.float64)
+    flags = lib().orc_topk_logprobs(_ptr(z), _logit_dtype(z), rows, V, K, _ptr(lp), _ptr(ids), _ptr(logz))
+    if flags & BAD_ARG:
+        raise ValueError("bad arguments to topk_logprobs")
+    return lp, ids, logz, flags
+
+
+class Tree:
+    """Per-request tree arrays (R leading)."""
+
+    def __init__(self, R, L, B):
+        P = B + 1
+        self.tokens = np.empty((R, B), np.int32)
+        self.parents = np.empty((R, P), np.int32)
+        self.depths = np.empty((R, P), np.int32)
+        self.S = np.empty((R, P), np.float64)
+        self.ranks = np.empty((R, P, L), np.int32)
+        self.n_nodes = np.empty((R,), np.int32)
+
+
+def build_tree(lp, ids, B):
+    """Algorithm 1 (heap) on lp/ids [R, L, K] (lp widened to fp64)."""
+    lp = np.ascontiguousarray(lp, dtype=np.float64)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    R, L, K = lp.shape
+    t = Tree(R, L, B)
+    rc = lib().orc_build_tree(_ptr(lp), _ptr(ids), R, L, K, B, _ptr(t.tokens), _ptr(t.parents),
+                              _ptr(t.depths), _ptr(t.S), _ptr(t.ranks), _ptr(t.n_nodes))
+    if rc:
+        raise ValueError("bad arguments to build_tree")
+    return t
+
+
+def build_tree_bruteforce(lp, ids, B, max_prefixes=5_000_000):
+    """Sort-every-prefix construction for one request: lp/ids [L, K]."""
+    lp = np.ascontiguousarray(lp, dtype=np.float64)
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    L, K = lp.shape
+    t = Tree(1, L, B)
+    n = lib().orc_build_tree_bruteforce(_ptr(lp), _ptr(ids), L, K, B, max_prefixes, _ptr(t.tokens),
+                                        _ptr(t.parents), _ptr(t.depths), _ptr(t.S), _ptr(t.ranks),
+                                        _ptr(t.n_nodes))
+    if n < 0:
+        raise ValueError("prefix space too large for brute force")
+    return t
+
+
+def build_mask(parents, n_nodes):
+    """Ancestor bitmask [R, P, ceil(P/32)] uint32 from parents [R, P]."""
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    n_nodes = np.ascontiguousarray(n_nodes, dtype=np.int32)
+    R, P = parents.shape
+    W = (P + 31) // 32
+    mask = np.empty((R, P, W), np.uint32)
+    lib().orc_build_mask(_ptr(parents), _ptr(n_nodes), R, P, _ptr(mask))
+    return mask
+
+
+def tree_attention_rows(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, mask, sel,
+                        scale=None):
+    """fp64 tree attention for the query rows sel [n, 3] = (r, i, h).
+
+    q [R,P,Hq,d], k_tree/v_tree [R,P,Hkv,d], k_cache/v_cache [pages,page,Hkv,d]
+    (all bf16 bit patterns, uint16); block_table [R, max_pages] int32;
+    ctx_lens [R] int32; mask [R, P, W] uint32. Returns [n, d] fp64.
+    """
+    arrs = [np.ascontiguousarray(x) for x in (q, k_tree, v_tree, k_cache, v_cache)]
+    for a in arrs:
+        if a.dtype != np.uint16:
+            raise TypeError("attention tensors are bf16 bit patterns (uint16)")
+    q, k_tree, v_tree, k_cache, v_cache = arrs
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    ctx_lens = np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    mask = np.ascontiguousarray(mask, dtype=np.uint32)
+    sel = np.ascontiguousarray(sel, dtype=np.int32).reshape(-1, 3)
+    R, P, Hq, d = q.shape
+    Hkv = k_tree.shape[2]
+    pages, page = k_cache.shape[0], k_cache.shape[1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    out = np.empty((sel.shape[0], d), np.float64)
+    flags = lib().orc_tree_attention_rows(
+        _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], pages, _ptr(ctx_lens), _ptr(mask), R, P, Hq, Hkv, d, page,
+        float(scale), _ptr(sel), sel.shape[0], _ptr(out))
+    if flags & BAD_ARG:
+        raise ValueError("bad arguments to tree_attention_rows")
+    return out, flags
+
+
+def tree_attention(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, mask, scale=None):
+    """All query rows: returns [R, P, Hq, d] fp64."""
+    R, P, Hq, d = q.shape
+    rr, ii, hh = np.meshgrid(np.arange(R), np.arange(P), np.arange(Hq), indexing="ij")
+    sel = np.stack([rr.ravel(), ii.ravel(), hh.ravel()], axis=1)
+    out, flags = tree_attention_rows(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens,
+                                     mask, sel, scale)
+    return out.reshape(R, P, Hq, d), flags
+
+
+def argmax(t):
+    """First index of the row maximum over the last axis."""
+    t = np.ascontiguousarray(t)
+    V = t.shape[-1]
+    rows = int(np.prod(t.shape[:-1]))
+    out = np.empty(t.shape[:-1], np.int32)
+    flags = lib().orc_argmax(_ptr(t), _logit_dtype(t), rows, V, _ptr(out))
+    return out, flags
+
+
+def walk(a, tree_tokens, parents, n_nodes, L):
+    """Greedy verifier walk. Returns (acc_len, acc_nodes, acc_tokens, bonus)."""
+    a = np.ascontiguousarray(a, dtype=np.int32)
+    tree_tokens = np.ascontiguousarray(tree_tokens, dtype=np.int32)
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    n_nodes = np.ascontiguousarray(n_nodes, dtype=np.int32)
+    R, B = tree_tokens.shape
+    acc_len = np.empty((R,), np.int32)
+    acc_nodes = np.empty((R, L), np.int32)
+    acc_tokens = np.empty((R, L + 1), np.int32)
+    bonus = np.empty((R,), np.int32)
+    lib().orc_walk(_ptr(a), _ptr(tree_tokens), _ptr(parents), _ptr(n_nodes), R, B, L,
+                   _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tokens), _ptr(bonus))
+    return acc_len, acc_nodes, acc_tokens, bonus
+
+
+def compact(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree, acc_nodes, acc_len):
+    """KV compaction in place on k_cache / v_cache / ctx_lens (numpy arrays)."""
+    for a in (k_cache, v_cache, ctx_lens):
+        if not a.flags.c_contiguous:
+            raise ValueError("in-place arrays must be contiguous")
+    k_tree = np.ascontiguousarray(k_tree)
+    v_tree = np.ascontiguousarray(v_tree)
+    block_table = np.ascontiguousarray(block_table, dtype=np.int32)
+    acc_nodes = np.ascontiguousarray(acc_nodes, dtype=np.int32)
+    acc_len = np.ascontiguousarray(acc_len, dtype=np.int32)
+    R, P, Hkv, d = k_tree.shape
+    L = acc_nodes.shape[1]
+    pages, page = k_cache.shape[0], k_cache.shape[1]
+    return lib().orc_compact(_ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+                             pages, _ptr(ctx_lens), _ptr(k_tree), _ptr(v_tree), _ptr(acc_nodes),
+                             _ptr(acc_len), R, P, L, Hkv, d, page)
+
+
+def round_(inputs, target_logits_fn=None, target_logits=None, B=None, K=None):
+    """One whole round a1..a7 on host arrays (used for the CPU baseline).
+
+    inputs: dict with draft_logits, q, k_tree, v_tree, k_cache, v_cache,
+    block_table, ctx_lens (copied before compaction). Returns a dict.
+    """
+    z = inputs["draft_logits"]
+    lp, ids, _, f1 = topk_logprobs(z, K)
+    tree = build_tree(lp, ids, B)
+    mask = build_mask(tree.parents, tree.n_nodes)
+    attn, f2 = tree_attention(inputs["q"], inputs["k_tree"], inputs["v_tree"], inputs["k_cache"],
+                              inputs["v_cache"], inputs["block_table"], inputs["ctx_lens"], mask)
+    if target_logits is None:
+        target_logits = target_logits_fn(tree)
+    a, f3 = argmax(target_logits)
+    L = z.shape[1]
+    acc_len, acc_nodes, acc_tokens, bonus = walk(a, tree.tokens, tree.parents, tree.n_nodes, L)
+    ctx = inputs["ctx_lens"].copy()
+    f4 = compact(inputs["k_cache"], inputs["v_cache"], inputs["block_table"], ctx, inputs["k_tree"],
+                 inputs["v_tree"], acc_nodes, acc_len)
+    return dict(lp=lp, ids=ids, tree=tree, mask=mask, attn=attn, a=a, acc_len=acc_len,
+                acc_nodes=acc_nodes, acc_tokens=acc_tokens, bonus=bonus, ctx_lens=ctx,
+                flags=f1 | f2 | f3 | f4)

@@ -1,0 +1,644 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for one batched DDTree round.
+ *
+ * TEST INFRASTRUCTURE. Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg load this library. The CUDA library never
+ * calls it, and the two share no source, header, table or helper.
+ *
+ * Every floating-point step runs in IEEE double. Inputs arrive as fp32 or as
+ * raw bf16 bit patterns and are widened exactly. Each function states the
+ * passage it follows; pages are named by title and section:
+ *
+ *   [SPARK]  "SparklingTree: 30-40% faster speculative decoding over DSpark",
+ *            section "How is the tree actually created?", Steps 1-4.
+ *   [DDTX]   "DDTree Explained: From Block Diffusion to Optimal Diffusion
+ *            Draft Trees for Speculative Decoding", sections 2-5.
+ *   [TSPK]   "Robot2050/TreeSpark", item 4 (exactness by construction) and
+ *            the continuous-batching engine description.
+ *
+ * Readings where the pages are silent are listed beside the function.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_LMAX 32 /* deepest draft block the oracle accepts */
+
+/* status bits returned by the oracle (0 = clean) */
+#define ORC_NAN_SEEN 1
+#define ORC_BAD_ARG 2
+#define ORC_BAD_PAGE 4
+
+/* exact widening: dtype 0 = fp32, 1 = bf16 bit pattern, 2 = fp64 */
+static double widen(const void *base, int dtype, int64_t i)
+{
+    if (dtype == 0)
+        return (double)((const float *)base)[i];
+    if (dtype == 2)
+        return ((const double *)base)[i];
+    uint32_t u = ((uint32_t)((const uint16_t *)base)[i]) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double bf16_to_double(uint16_t b)
+{
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 1 of the round [SPARK, Step 1; DDTX section 3, Lemma 1].
+ * For every row (request r, depth d) of the drafter's marginals:
+ *   logZ = log sum_v exp(z_v)           (max-shifted, fp64)
+ *   the K largest logits, ordered by value descending, equal values by
+ *   lower token id first (reading: the pages' top-k leaves ties open),
+ *   lp_k = z_{id_k} - logZ.
+ * Rows are independent; OpenMP spreads them over host threads.
+ * ---------------------------------------------------------------------- */
+int orc_topk_logprobs(const void *z, int dtype, int64_t rows, int64_t V, int K,
+                      double *lp, int32_t *ids, double *logz_out)
+{
+    if (K < 1 || (int64_t)K > V)
+        return ORC_BAD_ARG;
+    int flags = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+    for (int64_t row = 0; row < rows; ++row) {
+        const int64_t off = row * V;
+        double m = -INFINITY;
+        for (int64_t v = 0; v < V; ++v) {
+            double x = widen(z, dtype, off + v);
+            if (isnan(x))
+                flags |= ORC_NAN_SEEN;
+            if (x > m)
+                m = x;
+        }
+        double s = 0.0;
+        for (int64_t v = 0; v < V; ++v)
+            s += exp(widen(z, dtype, off + v) - m);
+        const double logZ = m + log(s);
+
+        /* running top-K by insertion; ids arrive in increasing order, so an
+         * equal value never displaces an earlier (lower) id */
+        double *tv = (double *)malloc(sizeof(double) * (size_t)K);
+        int32_t *ti = (int32_t *)malloc(sizeof(int32_t) * (size_t)K);
+        int n = 0;
+        for (int64_t v = 0; v < V; ++v) {
+            double x = widen(z, dtype, off + v);
+            if (n == K && !(x > tv[K - 1]))
+                continue;
+            int pos = (n < K) ? n : K - 1;
+            while (pos > 0 && tv[pos - 1] < x) {
+                tv[pos] = tv[pos - 1];
+                ti[pos] = ti[pos - 1];
+                --pos;
+            }
+            tv[pos] = x;
+            ti[pos] = (int32_t)v;
+            if (n < K)
+                ++n;
+        }
+        for (int k = 0; k < K; ++k) {
+            lp[row * K + k] = tv[k] - logZ;
+            ids[row * K + k] = ti[k];
+        }
+        if (logz_out)
+            logz_out[row] = logZ;
+        free(tv);
+        free(ti);
+    }
+    return flags;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 2: best-first selection of the B most probable prefixes
+ * [SPARK, Step 3; DDTX section 4, Algorithm 1; DDTX section 3, Prop. 2].
+ *
+ * A prefix is a rank tuple rho = (rho_1..rho_d): position i takes the
+ * rho_i-th most probable token of row i. Its score is
+ *   S(rho) = lp[0][rho_1] + lp[1][rho_2] + ... + lp[d-1][rho_d],
+ * accumulated left to right in fp64. The heap pops the entry with the
+ * largest S; equal S falls to the lexicographically smaller rank tuple,
+ * a tuple before its own extensions (this is how the pages' heap compares
+ * its (-score, ranks, ...) records). Each pop becomes node n = pops so far,
+ * then pushes the sibling (.., rho_d + 1) when rho_d + 1 < K and the child
+ * (.., rho_d, 0) when d < L. The heap starts from the single entry (0,).
+ *
+ * Reading: the pages update a sibling's score incrementally
+ * (score - lp[rank] + lp[rank+1]); here every entry carries its parent's S
+ * and scores as parent_S + lp, which is the same number in exact
+ * arithmetic and rounds identically on every machine.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double S;
+    double parent_S;
+    int32_t ranks[ORC_LMAX];
+    int32_t len; /* depth of the prefix */
+    int32_t parent;
+} heap_ent;
+
+/* does a pop before b? */
+static int ent_before(const heap_ent *a, const heap_ent *b)
+{
+    if (a->S != b->S)
+        return a->S > b->S;
+    int n = a->len < b->len ? a->len : b->len;
+    for (int i = 0; i < n; ++i)
+        if (a->ranks[i] != b->ranks[i])
+            return a->ranks[i] < b->ranks[i];
+    return a->len < b->len;
+}
+
+static void heap_push(heap_ent *h, int *size, const heap_ent *e)
+{
+    int i = (*size)++;
+    h[i] = *e;
+    while (i > 0) {
+        int p = (i - 1) / 2;
+        if (!ent_before(&h[i], &h[p]))
+            break;
+        heap_ent t = h[i];
+        h[i] = h[p];
+        h[p] = t;
+        i = p;
+    }
+}
+
+static heap_ent heap_pop(heap_ent *h, int *size)
+{
+    heap_ent top = h[0];
+    h[0] = h[--(*size)];
+    int i = 0;
+    for (;;) {
+        int l = 2 * i + 1, r = l + 1, best = i;
+        if (l < *size && ent_before(&h[l], &h[best]))
+            best = l;
+        if (r < *size && ent_before(&h[r], &h[best]))
+            best = r;
+        if (best == i)
+            break;
+        heap_ent t = h[i];
+        h[i] = h[best];
+        h[best] = t;
+        i = best;
+    }
+    return top;
+}
+
+/*
+ * lp, ids: [R, L, K]. Outputs per request (P = B + 1 positions):
+ *   tree_tokens [R, B]   token of node n at slot n-1, -1 when unused
+ *   parents     [R, P]   parents[0] = -1 (root = the bonus token)
+ *   depths      [R, P]   depths[0] = 0, nodes are 1-based in depth
+ *   node_S      [R, P]   prefix score of each node, node_S[0] = 0
+ *   node_ranks  [R, P, L] rank tuple of each node, -1 padded
+ *   n_nodes     [R]      number of non-root nodes (< B only when the
+ *                        whole prefix space is smaller than B)
+ */
+int orc_build_tree(const double *lp, const int32_t *ids, int R, int L, int K, int B,
+                   int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                   double *node_S, int32_t *node_ranks, int32_t *n_nodes)
+{
+    if (L < 1 || L > ORC_LMAX || K < 1 || B < 1)
+        return ORC_BAD_ARG;
+    const int P = B + 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        const double *lpr = lp + (int64_t)r * L * K;
+        const int32_t *idr = ids + (int64_t)r * L * K;
+        int32_t *tok = tree_tokens + (int64_t)r * B;
+        int32_t *par = parents + (int64_t)r * P;
+        int32_t *dep = depths + (int64_t)r * P;
+        double *ns = node_S + (int64_t)r * P;
+        int32_t *nr = node_ranks + (int64_t)r * P * L;
+        for (int j = 0; j < B; ++j)
+            tok[j] = -1;
+        for (int j = 0; j < P; ++j) {
+            par[j] = -1;
+            dep[j] = -1;
+            ns[j] = 0.0;
+            for (int i = 0; i < L; ++i)
+                nr[j * L + i] = -1;
+        }
+        dep[0] = 0;
+
+        heap_ent *heap = (heap_ent *)malloc(sizeof(heap_ent) * (size_t)(2 * B + 4));
+        int size = 0;
+        heap_ent first;
+        memset(&first, 0, sizeof first);
+        first.parent_S = 0.0;
+        first.S = 0.0 + lpr[0];
+        first.ranks[0] = 0;
+        first.len = 1;
+        first.parent = 0;
+        heap_push(heap, &size, &first);
+
+        int count = 0;
+        while (size > 0 && count < B) {
+            heap_ent e = heap_pop(heap, &size);
+            const int depth = e.len;
+            const int rank = e.ranks[depth - 1];
+            const int node = count + 1;
+            tok[count] = idr[(depth - 1) * K + rank];
+            par[node] = e.parent;
+            dep[node] = depth;
+            ns[node] = e.S;
+            for (int i = 0; i < depth; ++i)
+                nr[node * L + i] = e.ranks[i];
+            ++count;
+            if (rank + 1 < K) {
+                heap_ent sib = e;
+                sib.ranks[depth - 1] = rank + 1;
+                sib.S = e.parent_S + lpr[(depth - 1) * K + rank + 1];
+                heap_push(heap, &size, &sib);
+            }
+            if (depth < L) {
+                heap_ent ch = e;
+                ch.ranks[depth] = 0;
+                ch.len = depth + 1;
+                ch.parent = node;
+                ch.parent_S = e.S;
+                ch.S = e.S + lpr[depth * K + 0];
+                heap_push(heap, &size, &ch);
+            }
+        }
+        n_nodes[r] = count;
+        free(heap);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Second, independent construction of the same tree for small inputs: list
+ * every prefix of depth 1..L over ranks 0..K-1, score each left to right,
+ * sort the whole list by (S descending, rank tuple ascending) with qsort,
+ * keep the first B. [DDTX section 3, Prop. 2: the B best prefixes form a
+ * prefix-closed tree.] Node n is the n-th prefix of the sorted list; its
+ * parent is the node whose tuple drops the last rank. Returns the number of
+ * enumerated prefixes, or -1 when that exceeds max_prefixes.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double S;
+    int32_t ranks[ORC_LMAX];
+    int32_t len;
+} pref_ent;
+
+static int pref_cmp(const void *pa, const void *pb)
+{
+    const pref_ent *a = (const pref_ent *)pa, *b = (const pref_ent *)pb;
+    if (a->S != b->S)
+        return a->S > b->S ? -1 : 1;
+    int n = a->len < b->len ? a->len : b->len;
+    for (int i = 0; i < n; ++i)
+        if (a->ranks[i] != b->ranks[i])
+            return a->ranks[i] < b->ranks[i] ? -1 : 1;
+    return (a->len > b->len) - (a->len < b->len);
+}
+
+int64_t orc_build_tree_bruteforce(const double *lp, const int32_t *ids, int L, int K, int B,
+                                  int64_t max_prefixes, int32_t *tree_tokens, int32_t *parents,
+                                  int32_t *depths, double *node_S, int32_t *node_ranks,
+                                  int32_t *n_nodes)
+{
+    if (L < 1 || L > ORC_LMAX || K < 1 || B < 1)
+        return -1;
+    int64_t total = 0, layer = 1;
+    for (int d = 1; d <= L; ++d) {
+        layer *= K;
+        total += layer;
+        if (total > max_prefixes)
+            return -1;
+    }
+    pref_ent *all = (pref_ent *)calloc((size_t)total, sizeof(pref_ent));
+    int64_t n = 0;
+    int32_t digits[ORC_LMAX];
+    for (int d = 1; d <= L; ++d) {
+        for (int i = 0; i < d; ++i)
+            digits[i] = 0;
+        for (;;) {
+            pref_ent *p = &all[n++];
+            p->len = d;
+            double S = 0.0;
+            for (int i = 0; i < d; ++i) {
+                p->ranks[i] = digits[i];
+                S = S + lp[i * K + digits[i]];
+            }
+            p->S = S;
+            int i = d - 1;
+            while (i >= 0 && ++digits[i] == K) {
+                digits[i] = 0;
+                --i;
+            }
+            if (i < 0)
+                break;
+        }
+    }
+    qsort(all, (size_t)n, sizeof(pref_ent), pref_cmp);
+    const int P = B + 1;
+    const int take = (int)(n < B ? n : B);
+    for (int j = 0; j < B; ++j)
+        tree_tokens[j] = -1;
+    for (int j = 0; j < P; ++j) {
+        parents[j] = -1;
+        depths[j] = -1;
+        node_S[j] = 0.0;
+        for (int i = 0; i < L; ++i)
+            node_ranks[j * L + i] = -1;
+    }
+    depths[0] = 0;
+    for (int j = 0; j < take; ++j) {
+        const pref_ent *p = &all[j];
+        const int node = j + 1;
+        tree_tokens[j] = ids[(p->len - 1) * K + p->ranks[p->len - 1]];
+        depths[node] = p->len;
+        node_S[node] = p->S;
+        for (int i = 0; i < p->len; ++i)
+            node_ranks[node * L + i] = p->ranks[i];
+        /* parent: the selected prefix equal to this one minus its last rank */
+        int parent = -1;
+        if (p->len == 1) {
+            parent = 0;
+        } else {
+            for (int q = 0; q < j; ++q) {
+                const pref_ent *c = &all[q];
+                if (c->len != p->len - 1)
+                    continue;
+                int same = 1;
+                for (int i = 0; i < c->len; ++i)
+                    if (c->ranks[i] != p->ranks[i]) {
+                        same = 0;
+                        break;
+                    }
+                if (same) {
+                    parent = q + 1;
+                    break;
+                }
+            }
+        }
+        parents[node] = parent; /* -1 here would mean the set is not prefix-closed */
+    }
+    *n_nodes = take;
+    free(all);
+    return n;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 3: ancestor visibility [SPARK, Step 4; DDTX section 5, "ancestor-only
+ * tree attention mask"]. Row 0 sees only itself; row i copies its parent's
+ * row over columns < i and sets its own column. Rows of unused positions
+ * (i > n_nodes) stay empty (reading). Packed as little-endian 32-bit words:
+ * bit j of word w is column 32*w + j.
+ * ---------------------------------------------------------------------- */
+void orc_build_mask(const int32_t *parents, const int32_t *n_nodes, int R, int P, uint32_t *mask)
+{
+    const int W = (P + 31) / 32;
+    unsigned char *vis = (unsigned char *)malloc((size_t)P * (size_t)P);
+    for (int r = 0; r < R; ++r) {
+        memset(vis, 0, (size_t)P * (size_t)P);
+        const int32_t *par = parents + (int64_t)r * P;
+        vis[0] = 1;
+        for (int i = 1; i <= n_nodes[r] && i < P; ++i) {
+            const int p = par[i];
+            for (int j = 0; j < i; ++j)
+                vis[i * P + j] = vis[p * P + j];
+            vis[i * P + i] = 1;
+        }
+        for (int i = 0; i < P; ++i)
+            for (int w = 0; w < W; ++w) {
+                uint32_t word = 0;
+                for (int b = 0; b < 32; ++b) {
+                    const int j = 32 * w + b;
+                    if (j < P && vis[i * P + j])
+                        word |= (uint32_t)1 << b;
+                }
+                mask[((int64_t)r * P + i) * W + w] = word;
+            }
+    }
+    free(vis);
+}
+
+/* ------------------------------------------------------------------------
+ * Step 4: tree attention for one query row [SPARK, Step 4 and "the weird
+ * matmul"; DDTX sections 5 and 8 (custom attention mask, Qwen GQA)].
+ * Query (r, i, h) attends to every cached token t < ctx_lens[r] of its KV
+ * head g = h / (Hq / Hkv), reached through the page table, and to every
+ * tree position j whose bit is set in mask row (r, i). Scores are
+ * q . k * scale; softmax and the weighted sum of values run in fp64.
+ * Layouts (bf16 bit patterns):
+ *   q, out  [R, P, Hq, d]          k_tree, v_tree [R, P, Hkv, d]
+ *   k_cache, v_cache [pages, page, Hkv, d], block_table [R, max_pages]
+ * sel lists n query rows as (r, i, h) triples; out is [n, d] doubles.
+ * ---------------------------------------------------------------------- */
+int orc_tree_attention_rows(const uint16_t *q, const uint16_t *k_tree, const uint16_t *v_tree,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *block_table, int max_pages, int64_t num_pages,
+                            const int32_t *ctx_lens, const uint32_t *mask, int R, int P, int Hq,
+                            int Hkv, int d, int page, double scale, const int32_t *sel, int64_t n,
+                            double *out)
+{
+    if (Hkv < 1 || Hq % Hkv != 0 || d < 1 || page < 1)
+        return ORC_BAD_ARG;
+    (void)R; /* rows are named by (r, i, h) in sel */
+    const int W = (P + 31) / 32;
+    const int group = Hq / Hkv;
+    int flags = 0;
+#pragma omp parallel for schedule(dynamic, 4) reduction(| : flags)
+    for (int64_t s = 0; s < n; ++s) {
+        const int r = sel[3 * s], i = sel[3 * s + 1], h = sel[3 * s + 2];
+        const int g = h / group;
+        const int ctx = ctx_lens[r];
+        const uint16_t *qrow = q + (((int64_t)r * P + i) * Hq + h) * d;
+        const uint32_t *mrow = mask + ((int64_t)r * P + i) * W;
+        const int ntree = P;
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(ctx + ntree));
+        const uint16_t **vrows = (const uint16_t **)malloc(sizeof(void *) * (size_t)(ctx + ntree));
+        int cnt = 0;
+        double mx = -INFINITY;
+        for (int t = 0; t < ctx; ++t) {
+            const int32_t pg = block_table[(int64_t)r * max_pages + t / page];
+            if (pg < 0 || pg >= num_pages) {
+                flags |= ORC_BAD_PAGE;
+                continue;
+            }
+            const int64_t row = ((int64_t)pg * page + t % page) * Hkv + g;
+            const uint16_t *krow = k_cache + row * d;
+            double dot = 0.0;
+            for (int x = 0; x < d; ++x)
+                dot += bf16_to_double(qrow[x]) * bf16_to_double(krow[x]);
+            scores[cnt] = dot * scale;
+            vrows[cnt] = v_cache + row * d;
+            if (scores[cnt] > mx)
+                mx = scores[cnt];
+            ++cnt;
+        }
+        for (int j = 0; j < ntree; ++j) {
+            if (!((mrow[j / 32] >> (j % 32)) & 1u))
+                continue;
+            const int64_t row = ((int64_t)r * P + j) * Hkv + g;
+            const uint16_t *krow = k_tree + row * d;
+            double dot = 0.0;
+            for (int x = 0; x < d; ++x)
+                dot += bf16_to_double(qrow[x]) * bf16_to_double(krow[x]);
+            scores[cnt] = dot * scale;
+            vrows[cnt] = v_tree + row * d;
+            if (scores[cnt] > mx)
+                mx = scores[cnt];
+            ++cnt;
+        }
+        double *o = out + s * d;
+        for (int x = 0; x < d; ++x)
+            o[x] = 0.0;
+        double den = 0.0;
+        for (int c = 0; c < cnt; ++c) {
+            const double p = exp(scores[c] - mx);
+            den += p;
+            for (int x = 0; x < d; ++x)
+                o[x] += p * bf16_to_double(vrows[c][x]);
+        }
+        for (int x = 0; x < d; ++x)
+            o[x] = cnt ? o[x] / den : 0.0;
+        free(scores);
+        free(vrows);
+    }
+    return flags;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 5a: target argmax per tree position [DDTX section 5, verifier walk
+ * under the greedy decoding rule; TSPK, vectorised acceptance retrieval].
+ * The first index holding the largest value wins; -0 equals +0. A NaN is
+ * reported through the status bits (the pages assume finite logits).
+ * ---------------------------------------------------------------------- */
+int orc_argmax(const void *t, int dtype, int64_t rows, int64_t V, int32_t *out)
+{
+    int flags = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : flags)
+    for (int64_t row = 0; row < rows; ++row) {
+        double best = 0.0;
+        int32_t arg = -1;
+        for (int64_t v = 0; v < V; ++v) {
+            const double x = widen(t, dtype, row * V + v);
+            if (isnan(x)) {
+                flags |= ORC_NAN_SEEN;
+                continue;
+            }
+            if (arg < 0 || x > best) {
+                best = x;
+                arg = (int32_t)v;
+            }
+        }
+        if (arg < 0)
+            arg = 0;
+        out[row] = arg;
+    }
+    return flags;
+}
+
+/* ------------------------------------------------------------------------
+ * Step 5b: greedy verifier walk [DDTX section 5, "Verifier walk"; TSPK
+ * item 4]. Start at the root (the bonus token). At node cur, the target's
+ * greedy token is a[cur]; if a child of cur carries that token the child is
+ * accepted and the walk moves to it, otherwise a[cur] becomes the new bonus
+ * token and the walk ends. Outputs per request:
+ *   acc_len    accepted drafts + 1 (the bonus is counted, as the pages'
+ *              acceptance length is)
+ *   acc_nodes  [R, L] accepted node indices in path order, -1 padded
+ *   acc_tokens [R, L+1] accepted tokens then the bonus, -1 padded
+ *   bonus      [R]
+ * ---------------------------------------------------------------------- */
+void orc_walk(const int32_t *a, const int32_t *tree_tokens, const int32_t *parents,
+              const int32_t *n_nodes, int R, int B, int L, int32_t *acc_len, int32_t *acc_nodes,
+              int32_t *acc_tokens, int32_t *bonus)
+{
+    const int P = B + 1;
+    for (int r = 0; r < R; ++r) {
+        const int32_t *ar = a + (int64_t)r * P;
+        const int32_t *tok = tree_tokens + (int64_t)r * B;
+        const int32_t *par = parents + (int64_t)r * P;
+        int32_t *an = acc_nodes + (int64_t)r * L;
+        int32_t *at = acc_tokens + (int64_t)r * (L + 1);
+        for (int j = 0; j < L; ++j)
+            an[j] = -1;
+        for (int j = 0; j <= L; ++j)
+            at[j] = -1;
+        int cur = 0, n = 0;
+        for (;;) {
+            const int32_t want = ar[cur];
+            int found = -1;
+            for (int c = 1; c <= n_nodes[r]; ++c)
+                if (par[c] == cur && tok[c - 1] == want) {
+                    found = c;
+                    break;
+                }
+            if (found < 0 || n >= L) {
+                bonus[r] = want;
+                break;
+            }
+            an[n] = found;
+            at[n] = want;
+            ++n;
+            cur = found;
+        }
+        at[n] = bonus[r];
+        acc_len[r] = n + 1;
+    }
+}
+
+/* ------------------------------------------------------------------------
+ * Step 5c: KV compaction to the accepted path [DDTX section 5,
+ * "compact_cache keeps only the accepted path's cache"; SPARK, conclusion
+ * (the C++ KV compaction kernel)].
+ * Reading: this round's tree keys and values are inputs k_tree, v_tree
+ * [R, P, Hkv, d]. The root goes to sequence slot ctx, the accepted node at
+ * path depth j to slot ctx + j; slot s lives in page block_table[r][s/page]
+ * at row s % page. Afterwards ctx_lens[r] grows by acc_len[r].
+ * ---------------------------------------------------------------------- */
+int orc_compact(uint16_t *k_cache, uint16_t *v_cache, const int32_t *block_table, int max_pages,
+                int64_t num_pages, int32_t *ctx_lens, const uint16_t *k_tree,
+                const uint16_t *v_tree, const int32_t *acc_nodes, const int32_t *acc_len, int R,
+                int P, int L, int Hkv, int d, int page)
+{
+    int flags = 0;
+    const int64_t rowlen = (int64_t)Hkv * d;
+    for (int r = 0; r < R; ++r) {
+        const int ctx = ctx_lens[r];
+        const int n_acc = acc_len[r] - 1;
+        for (int j = 0; j <= n_acc; ++j) {
+            const int node = (j == 0) ? 0 : acc_nodes[(int64_t)r * L + j - 1];
+            const int slot = ctx + j;
+            const int pidx = slot / page;
+            if (pidx >= max_pages) {
+                flags |= ORC_BAD_PAGE;
+                continue;
+            }
+            const int32_t pg = block_table[(int64_t)r * max_pages + pidx];
+            if (pg < 0 || pg >= num_pages) {
+                flags |= ORC_BAD_PAGE;
+                continue;
+            }
+            const int64_t dst = ((int64_t)pg * page + slot % page) * rowlen;
+            const int64_t src = ((int64_t)r * P + node) * rowlen;
+            memcpy(k_cache + dst, k_tree + src, sizeof(uint16_t) * (size_t)rowlen);
+            memcpy(v_cache + dst, v_tree + src, sizeof(uint16_t) * (size_t)rowlen);
+        }
+        ctx_lens[r] = ctx + 1 + n_acc;
+    }
+    return flags;
+}
+
+/* number of threads OpenMP will use (1 when built without OpenMP) */
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
