@@ -1,0 +1,445 @@
+"""Benchmark: batched DDTree draft-tree rounds per second on GB300.
+
+Workload (default): 64 in-flight requests, 15 draft depths, vocabulary
+151,936, budget 32 (K = 32, P = 33 tree positions), Qwen3-8B attention
+shapes (32 query heads, 8 KV heads, head dim 128), bf16 paged KV cache
+with 16-token pages, contexts uniform in [512, 16384] -- seeded synthetic
+inputs (synth.py), larger than L2 per round (about 3.2 GB), so no flush is
+needed between rounds.
+
+A step is one full round (ddt_round: top-K, tree, mask, attention, target
+argmax, walk, compaction). Every step restores ctx_lens first (a 256-byte
+device copy) so each step does the same work. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle (the only other implementation
+of the round) on the host cores over a bounded sample of the same workload.
+Under torchrun each rank runs its own replica of the round (requests shard
+across ranks with no exchange); rank 0 prints the aggregate.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree rounds/s at R=64,L=15,V=152K,B=32; achieved HBM GB/s vs GB300 peak"
+UNIT = "rounds/s"
+WORKLOAD = "batch64"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _workload_desc(cfg):
+    return ("%s: R=%d,L=%d,V=%d,B=%d,K=%d,P=%d,Hq=%d,Hkv=%d,d=%d,page=%d,ctx~U[%d,%d],bf16"
+            % (cfg.name, cfg.R, cfg.L, cfg.V, cfg.B, cfg.K, cfg.P, cfg.Hq, cfg.Hkv, cfg.d, cfg.page,
+               cfg.ctx_args[0], cfg.ctx_args[1]))
+
+
+def round_bytes(cfg, ctx_lens, acc_len=None):
+    """Algorithmic HBM bytes of one round, by stage (each tensor once)."""
+    R, L, V, K, P = cfg.R, cfg.L, cfg.V, cfg.K, cfg.P
+    W = cfg.W
+    kv_row = cfg.Hkv * cfg.d * 2  # bytes of one token's K (or V) for all KV heads
+    ctx_tot = int(np.sum(ctx_lens))
+    b = {}
+    b["topk"] = R * L * V * 2 + R * L * K * 8
+    b["tree"] = R * L * K * 8 + R * (cfg.B + 3 * P) * 4 + R * P * W * 4
+    b["attention"] = (2 * ctx_tot * kv_row          # paged K and V
+                      + 2 * R * P * cfg.Hq * cfg.d * 2  # Q in, O out
+                      + 2 * R * P * kv_row          # tree K and V
+                      + R * P * W * 4 + R * 4)      # mask, ctx_lens
+    nacc = int(np.sum(acc_len)) if acc_len is not None else R
+    b["accept"] = (R * P * V * 2                    # target logits
+                   + R * (P + cfg.B + 2 * L + 4) * 4
+                   + 2 * 2 * nacc * kv_row)         # compaction: read + write K and V rows
+    b["total"] = sum(b.values())
+    return b
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _traffic_for(kernel_file, kernel_key):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current source of the kernel (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel_key]
+        src = open(os.path.join(ROOT, "speculative_decoding_draft_depth_gb300", "csrc",
+                                kernel_file), "rb").read()
+        if rec.get("source_sha1") != hashlib.sha1(src).hexdigest():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_round(cfg, inp, reqs):
+    """The oracle's round on a subset of requests (host arrays); seconds."""
+    import oracle
+    sub = {}
+    for k in ("draft_logits", "q", "k_tree", "v_tree", "block_table", "ctx_lens"):
+        sub[k] = np.ascontiguousarray(inp[k][reqs])
+    t0 = time.perf_counter()
+    lp, ids, _, _ = oracle.topk_logprobs(sub["draft_logits"], cfg.K)
+    tree = oracle.build_tree(lp, ids, cfg.B)
+    mask = oracle.build_mask(tree.parents, tree.n_nodes)
+    oracle.tree_attention(sub["q"], sub["k_tree"], sub["v_tree"], inp["k_cache"], inp["v_cache"],
+                          sub["block_table"], sub["ctx_lens"], mask)
+    a, _ = oracle.argmax(inp["target_logits"][reqs])
+    acc_len, acc_nodes, _, _ = oracle.walk(a, tree.tokens, tree.parents, tree.n_nodes, cfg.L)
+    # compaction writes into scratch copies of only the touched pages' pool
+    kc = inp["k_cache"].copy() if inp.get("copy_cache") else inp["k_cache"]
+    vc = inp["v_cache"].copy() if inp.get("copy_cache") else inp["v_cache"]
+    ctx = sub["ctx_lens"].copy()
+    oracle.compact(kc, vc, sub["block_table"], ctx, sub["k_tree"], sub["v_tree"], acc_nodes,
+                   acc_len)
+    return time.perf_counter() - t0
+
+
+def cpu_sample(cfg, inp, n_req):
+    import oracle
+    rng = np.random.default_rng(12345)
+    reqs = np.sort(rng.choice(cfg.R, size=n_req, replace=False))
+    secs = cpu_oracle_round(cfg, inp, reqs)
+    per_round = secs * cfg.R / n_req
+    return {"value": 1.0 / per_round, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d requests of the same round (all stages), %.2f s, scaled to the "
+                      "full batch" % (n_req, cfg.R, secs)}
+
+
+# ----------------------------------------------------------------- inputs
+def make_inputs(cfg):
+    from speculative_decoding_draft_depth_gb300 import synth
+    inp = synth.draw_round_inputs(cfg)
+    return inp
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from speculative_decoding_draft_depth_gb300 import synth
+    cfg = synth.config(WORKLOAD, seed=synth.config(WORKLOAD).seed + rank)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(cfg, args)
+        return
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    from speculative_decoding_draft_depth_gb300 import ddt
+    ddt.load()
+
+    inp = make_inputs(cfg)
+    dev = torch.device("cuda", local_rank)
+
+    def td(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    c = ddt.make_config(R_max=cfg.R, L=cfg.L, V=cfg.V, B=cfg.B, K=cfg.K, Hq=cfg.Hq, Hkv=cfg.Hkv,
+                        d=cfg.d, page_size=cfg.page,
+                        max_pages_per_req=inp["block_table"].shape[1],
+                        num_pages=inp["k_cache"].shape[0])
+    ctx = ddt.Context(c)
+    bufs = ctx.alloc_outputs(cfg.R, device=dev)
+    d = {k: td(inp[k]) for k in ("draft_logits", "q", "k_tree", "v_tree", "k_cache", "v_cache",
+                                 "block_table", "ctx_lens")}
+    ctx0 = d["ctx_lens"].clone()
+    # target logits follow this round's tree (set-up round, untimed)
+    bufs.update(d)
+    bufs["target_logits"] = torch.zeros((cfg.R, cfg.P, cfg.V), dtype=torch.int16, device=dev)
+    ctx.ddt_round(cfg.R, bufs)
+    torch.cuda.synchronize()
+    target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+    tl = target.logits_for_tree(bufs["tree_tokens"].cpu().numpy(), bufs["parents"].cpu().numpy(),
+                                bufs["n_nodes"].cpu().numpy())
+    inp["target_logits"] = tl
+    bufs["target_logits"] = td(tl)
+    d["ctx_lens"].copy_(ctx0)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        ctx.ddt_round(cfg.R, bufs, stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set during warm-up")
+    acc_len = bufs["acc_len"].cpu().numpy()
+
+    # ---------------- timed region: K full rounds
+    clocks = Clocks(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+    value = world * args.steps / (ms_total / 1e3)
+
+    # ---------------- per-stage durations (same stream, CUDA events)
+    stage_ms = time_stages(ctx, cfg, bufs, d, ctx0, stream, reps=max(20, args.steps // 10))
+
+    peak, peak_kind = _peaks()
+    nb = round_bytes(cfg, inp["ctx_lens"], acc_len)
+    att_gbs = nb["attention"] / (stage_ms["attention"] / 1e3) / 1e9
+    traffic = _traffic_for("attention.cu", "att_kernel")
+    roofline = {"bound": "hbm", "achieved": round(att_gbs, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(att_gbs / peak, 4), "traffic": traffic,
+                "kernel": "ddt_tree_attention (paged GQA tree attention)",
+                "peak_kind": peak_kind}
+    round_gbs = nb["total"] * value / world / 1e9
+    stages = {k: {"ms": round(v, 4),
+                  "GBps": round(nb[k] / (v / 1e3) / 1e9, 1) if k in nb else None}
+              for k, v in stage_ms.items()}
+
+    out = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded numpy generators)",
+           "config": {"workload": _workload_desc(cfg),
+                      "l2": "inputs larger than L2 (%.2f GB algorithmic per round), no flush"
+                            % (nb["total"] / 1e9),
+                      "parallelism": "replicas (requests shard by rank, no collective)"},
+           "round_hbm": {"bytes_per_round": nb["total"], "achieved_GBps": round(round_gbs, 1),
+                         "peak": peak, "frac": round(round_gbs / peak, 4), "peak_kind": peak_kind},
+           "stages": stages,
+           "roofline": roofline,
+           "gpu_launches": 6 * args.steps,
+           "clocks": clk,
+           "acceptance": {"mean_acc_len": float(np.mean(acc_len))}}
+
+    if not args.no_e2e:
+        out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
+                              steps=max(10, min(args.steps, 50)))
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_sample(cfg, inp, n_req=16)
+    if rank == 0:
+        print(json.dumps(out))
+    if dist:
+        dist.destroy_process_group()
+
+
+def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps):
+    import torch
+    R = cfg.R
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    res = {}
+
+    def run(name, fn):
+        fn()
+        torch.cuda.synchronize()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / reps
+
+    run("topk", lambda: ctx.ddt_topk_logprobs(bufs["draft_logits"], R, bufs["top_lp"],
+                                              bufs["top_ids"], stream))
+    run("tree", lambda: ctx.ddt_build_tree(bufs["top_lp"], bufs["top_ids"], R, bufs["tree_tokens"],
+                                           bufs["parents"], bufs["depths"], bufs["n_nodes"],
+                                           bufs["mask"], stream))
+    d["ctx_lens"].copy_(ctx0)
+    run("attention", lambda: ctx.ddt_tree_attention(bufs["q"], bufs["k_tree"], bufs["v_tree"],
+                                                    bufs["k_cache"], bufs["v_cache"],
+                                                    bufs["block_table"], bufs["ctx_lens"],
+                                                    bufs["mask"], R, bufs["attn_out"], stream))
+
+    def accept():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        ctx.ddt_accept(bufs["target_logits"], bufs["tree_tokens"], bufs["parents"],
+                       bufs["n_nodes"], R, bufs["target_argmax"], bufs["acc_len"],
+                       bufs["acc_nodes"], bufs["acc_tokens"], bufs["bonus"], bufs["k_cache"],
+                       bufs["v_cache"], bufs["block_table"], bufs["k_tree"], bufs["v_tree"],
+                       bufs["ctx_lens"], stream)
+
+    run("accept", accept)
+    d["ctx_lens"].copy_(ctx0)
+    torch.cuda.synchronize()
+    return res
+
+
+def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps):
+    """Same metric through the C ABI with the step's inputs in pinned host
+    memory: H2D of the per-round inputs, the round, D2H of the results."""
+    import torch
+    names = ("draft_logits", "target_logits", "q", "k_tree", "v_tree")
+    host = {}
+    for k in names:
+        a = np.ascontiguousarray(inp[k])
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        host[k] = torch.from_numpy(a).pin_memory()
+    host_ctx = ctx0.cpu().pin_memory()
+    outs = {k: torch.empty(bufs[k].shape, dtype=bufs[k].dtype).pin_memory()
+            for k in ("acc_len", "acc_tokens", "bonus")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_ctx.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def step():
+        for k in names:
+            bufs[k].copy_(host[k], non_blocking=True)
+        d["ctx_lens"].copy_(host_ctx, non_blocking=True)
+        ctx.ddt_round(cfg.R, bufs, stream)
+        for k, t in outs.items():
+            t.copy_(bufs[k], non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    d["ctx_lens"].copy_(ctx0)
+    return {"value": round(world * steps / (ms / 1e3), 2), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def run_reference(cfg, args):
+    """The fp64 CPU oracle as the reference arm, on the host cores."""
+    import oracle
+    from speculative_decoding_draft_depth_gb300 import synth
+    inp = make_inputs(cfg)
+    lp, ids, _, _ = oracle.topk_logprobs(inp["draft_logits"], cfg.K)
+    tree = oracle.build_tree(lp, ids, cfg.B)
+    target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+    inp["target_logits"] = target.logits_for_tree(tree.tokens, tree.parents, tree.n_nodes)
+    n_req = 1
+    rng = np.random.default_rng(777)
+    times = []
+    for s in range(args.warmup + args.steps):
+        reqs = np.sort(rng.choice(cfg.R, size=n_req, replace=False))
+        secs = cpu_oracle_round(cfg, inp, reqs)
+        if s >= args.warmup:
+            times.append(secs * cfg.R / n_req)
+    per_round = float(np.mean(times))
+    value = 1.0 / per_round
+    out = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_round * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded numpy generators)", "impl": "reference",
+           "config": {"workload": _workload_desc(cfg)},
+           "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": oracle.num_threads(),
+                            "kind": "oracle",
+                            "sample": "each step: %d random requests of the round, all stages, "
+                                      "time scaled to %d requests" % (n_req, cfg.R)},
+           "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,234 @@
+/*
+ * ddt.h -- C ABI of the GB300 (sm_103a) batched draft-tree round.
+ *
+ * One round, for R in-flight requests that each hold a block drafter's
+ * per-depth marginals, runs
+ *   a1 ddt_topk_logprobs   per-depth log-softmax + top-K over the vocabulary
+ *   a2 ddt_build_tree      best-first selection of the B most probable prefixes
+ *   a3 ddt_build_mask      ancestor bitmask of every tree position
+ *   a4 ddt_tree_attention  paged GQA attention of the tree queries
+ *   a5 ddt_target_argmax   greedy target token at every tree position
+ *   a6 ddt_walk            greedy acceptance walk down the tree
+ *   a7 ddt_compact         KV of the accepted path written into the cache
+ * and ddt_round chains a1..a7 (ddt_accept chains a5..a7) on one stream
+ * with no host synchronisation.
+ *
+ * Pages the operations follow (title and section):
+ *   "SparklingTree: 30-40% faster speculative decoding over DSpark",
+ *       "How is the tree actually created?", Steps 1-4.
+ *   "DDTree Explained: From Block Diffusion to Optimal Diffusion Draft Trees
+ *       for Speculative Decoding", sections 3 (Prop. 1, Prop. 2, Lemma 1),
+ *       4 (Algorithm 1) and 5 (implementation highlights).
+ *   "Robot2050/TreeSpark", item 4 and the continuous-batching engine
+ *       (device-side masks, vectorised acceptance, ragged-batch KV).
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers unless stated. The caller owns every
+ *     input and output buffer; a context owns only its workspace.
+ *   - bf16 tensors are passed as uint16_t* holding raw bf16 bit patterns.
+ *   - Logit tensors (draft, target) are bf16 or fp32 as the context's
+ *     config says; their pointers are const void*.
+ *   - All tensors are dense row-major with the shapes given below; no
+ *     strides are accepted. Vectorised paths need 16-byte-aligned base
+ *     pointers; unaligned ones are rejected with DDT_EINVAL.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
+ *     call only enqueues work on it and returns; none synchronises the host
+ *     except ddt_device_status. One context must not be used by two streams
+ *     at once (its workspace is shared by its calls).
+ *   - Shape and argument errors return DDT_EINVAL (or DDT_EUNSUPPORTED)
+ *     synchronously and enqueue nothing. Launch failures return DDT_ECUDA.
+ *     Data errors found on the device (NaN logits, page ids out of range,
+ *     malformed parents) never trap: they set bits of a device status word
+ *     read with ddt_device_status, and the kernels skip the bad access.
+ *
+ * Notation: R requests (R <= R_max), L draft depths, V vocabulary, B budget
+ * of non-root tree nodes, K = min(B, V) kept per depth (the config may ask
+ * for another K <= V), P = B + 1 tree positions (position 0 is the root, the
+ * round's bonus token), W = ceil(P / 32) mask words, Hq query heads, Hkv KV
+ * heads (Hq % Hkv == 0), d head dimension, page_size tokens per KV page.
+ */
+#ifndef DDT_H
+#define DDT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ddt_status {
+    DDT_OK = 0,
+    DDT_EINVAL = 1,       /* bad shape, dtype, pointer or alignment; nothing enqueued */
+    DDT_EUNSUPPORTED = 2, /* valid request outside what this build implements */
+    DDT_ECUDA = 3,        /* a CUDA runtime call failed (see ddt_last_cuda_error) */
+    DDT_ENOMEM = 4        /* workspace allocation failed in ddt_create */
+} ddt_status;
+
+typedef enum ddt_dtype { DDT_BF16 = 0, DDT_F32 = 1 } ddt_dtype;
+
+/* bits of the device status word (ddt_device_status) */
+#define DDT_DEV_NAN_LOGITS 0x1 /* a NaN reached top-K or argmax */
+#define DDT_DEV_BAD_PAGE 0x2   /* a block-table entry was outside [0, num_pages) */
+#define DDT_DEV_BAD_TREE 0x4   /* parents/n_nodes/acc arrays out of range */
+
+typedef struct ddt_config {
+    int32_t R_max;             /* most requests a call may carry */
+    int32_t L;                 /* draft depths per request (1..18) */
+    int32_t V;                 /* vocabulary size */
+    int32_t B;                 /* non-root tree nodes (1..127) */
+    int32_t K;                 /* per-depth top-K; 0 selects min(B, V) */
+    int32_t Hq, Hkv, d;        /* attention heads and head dim (d = 128 or 64) */
+    int32_t page_size;         /* tokens per KV page (multiple of 16 for a4) */
+    int32_t max_pages_per_req; /* row length of block_table */
+    int64_t num_pages;         /* pages in the KV pool (bounds checks) */
+    int32_t draft_dtype;       /* ddt_dtype of draft logits */
+    int32_t target_dtype;      /* ddt_dtype of target logits */
+} ddt_config;
+
+typedef struct ddt_ctx ddt_ctx; /* opaque */
+
+/* Validate cfg, pick the current CUDA device, allocate the workspace
+ * (ddt_workspace_bytes) and return a context in *out. DDT_EINVAL for a bad
+ * config, DDT_ENOMEM if the workspace cannot be allocated. */
+ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out);
+
+/* Free the workspace and the context (waits for nothing: the caller makes
+ * sure no enqueued call still runs). NULL is ignored. */
+void ddt_destroy(ddt_ctx *ctx);
+
+/* Device bytes a context with this config allocates (0 for a bad config). */
+size_t ddt_workspace_bytes(const ddt_config *cfg);
+
+/* a1 -- "SparklingTree ...", Step 1; "DDTree Explained ...", Lemma 1.
+ * draft_logits [R, L, V] (draft_dtype). For each (request, depth) row:
+ * logZ = log sum_v exp(z_v); the K largest logits in order value
+ * descending, equal values by lower token id; top_lp = z - logZ (fp32),
+ * top_ids their token ids. Outputs top_lp [R, L, K] f32, top_ids [R, L, K]
+ * i32. NaN logits set DDT_DEV_NAN_LOGITS. */
+ddt_status ddt_topk_logprobs(ddt_ctx *ctx, const void *draft_logits, int32_t R, float *top_lp,
+                             int32_t *top_ids, void *stream);
+
+/* a2 -- "DDTree Explained ...", section 4, Algorithm 1; "SparklingTree ...",
+ * Step 3. From top_lp/top_ids [R, L, K], pops the B prefixes with the
+ * largest S (the fp64 sum of their per-depth log-probs, parent score plus
+ * own log-prob); equal S goes to the lexicographically smaller rank tuple.
+ * Node n (1..B) is the n-th pop. Outputs:
+ *   tree_tokens [R, B]  token of node n at index n-1 (-1 if unused)
+ *   parents     [R, P]  parent node of node n; parents[0] = -1
+ *   depths      [R, P]  depth of node n (1..L); depths[0] = 0; -1 if unused
+ *   n_nodes     [R]     nodes built (B unless the prefix space is smaller)
+ * mask (may be NULL): when given, the a3 ancestor mask is written as well
+ * ([R, P, W] u32, same contents as ddt_build_mask). */
+ddt_status ddt_build_tree(ddt_ctx *ctx, const float *top_lp, const int32_t *top_ids, int32_t R,
+                          int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                          int32_t *n_nodes, uint32_t *mask, void *stream);
+
+/* a3 -- "SparklingTree ...", Step 4; "DDTree Explained ...", section 5.
+ * mask [R, P, W] u32: bit j of word w of row (r, i) is set iff position
+ * 32w + j is the root, an ancestor of i, or i itself. Rows past n_nodes are
+ * zero. Bad parents set DDT_DEV_BAD_TREE. */
+ddt_status ddt_build_mask(ddt_ctx *ctx, const int32_t *parents, const int32_t *n_nodes,
+                          int32_t R, uint32_t *mask, void *stream);
+
+/* a4 -- "SparklingTree ...", Step 4 and the verification discussion;
+ * "DDTree Explained ...", sections 5 and 8 (ancestor-only mask, GQA).
+ * Query row (r, i, h) attends, with scale 1/sqrt(d), to the ctx_lens[r]
+ * cached tokens of KV head h / (Hq / Hkv) and to the tree positions set in
+ * mask row (r, i); softmax in fp32, bf16 inputs, fp32 accumulation.
+ *   q, out          [R, P, Hq, d] bf16
+ *   k_tree, v_tree  [R, P, Hkv, d] bf16 (this round's tree keys/values)
+ *   k_cache,v_cache [num_pages, page_size, Hkv, d] bf16
+ *   block_table     [R, max_pages_per_req] i32: page of token t is
+ *                   block_table[r][t / page_size], row t % page_size
+ *   ctx_lens        [R] i32, mask [R, P, W] u32
+ * Page ids out of range set DDT_DEV_BAD_PAGE and are read as zeros. */
+ddt_status ddt_tree_attention(ddt_ctx *ctx, const uint16_t *q, const uint16_t *k_tree,
+                              const uint16_t *v_tree, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *block_table,
+                              const int32_t *ctx_lens, const uint32_t *mask, int32_t R,
+                              uint16_t *out, void *stream);
+
+/* a5 -- "DDTree Explained ...", section 5 (verifier walk under greedy
+ * decoding); "Robot2050/TreeSpark" (vectorised acceptance).
+ * target_logits [R, P, V] (target_dtype) -> argmax_out [R, P] i32, the first
+ * index of each row's maximum (-0 equals +0). NaN sets DDT_DEV_NAN_LOGITS. */
+ddt_status ddt_target_argmax(ddt_ctx *ctx, const void *target_logits, int32_t R,
+                             int32_t *argmax_out, void *stream);
+
+/* a6 -- "DDTree Explained ...", section 5, verifier walk; "Robot2050/
+ * TreeSpark" item 4. From the root, while a child of the current node
+ * carries the target's token argmax[r][cur], accept it and move there;
+ * the first unmatched argmax is the new bonus token. Outputs
+ *   acc_len    [R]       accepted drafts + 1 (the bonus counts)
+ *   acc_nodes  [R, L]    accepted node indices, -1 padded
+ *   acc_tokens [R, L+1]  accepted tokens then the bonus, -1 padded
+ *   bonus      [R] */
+ddt_status ddt_walk(ddt_ctx *ctx, const int32_t *argmax, const int32_t *tree_tokens,
+                    const int32_t *parents, const int32_t *n_nodes, int32_t R, int32_t *acc_len,
+                    int32_t *acc_nodes, int32_t *acc_tokens, int32_t *bonus, void *stream);
+
+/* a7 -- "DDTree Explained ...", section 5 (compact_cache keeps only the
+ * accepted path). Writes the root's tree K/V to sequence slot ctx_lens[r]
+ * and the accepted node at path depth j to slot ctx_lens[r] + j, through
+ * block_table, then adds acc_len[r] to ctx_lens[r] (in place). The page
+ * table must already cover the new slots; entries out of range set
+ * DDT_DEV_BAD_PAGE and the row is skipped. */
+ddt_status ddt_compact(ddt_ctx *ctx, uint16_t *k_cache, uint16_t *v_cache,
+                       const int32_t *block_table, int32_t *ctx_lens, const uint16_t *k_tree,
+                       const uint16_t *v_tree, const int32_t *acc_nodes, const int32_t *acc_len,
+                       int32_t R, void *stream);
+
+/* a5..a7 in one call. argmax_out may be NULL. */
+ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tree_tokens,
+                      const int32_t *parents, const int32_t *n_nodes, int32_t R,
+                      int32_t *argmax_out, int32_t *acc_len, int32_t *acc_nodes,
+                      int32_t *acc_tokens, int32_t *bonus, uint16_t *k_cache, uint16_t *v_cache,
+                      const int32_t *block_table, const uint16_t *k_tree, const uint16_t *v_tree,
+                      int32_t *ctx_lens, void *stream);
+
+/* Everything one round reads and writes (shapes as above). */
+typedef struct ddt_round_args {
+    int32_t R;
+    const void *draft_logits;  /* [R, L, V] */
+    const void *target_logits; /* [R, P, V] */
+    const uint16_t *q;         /* [R, P, Hq, d] */
+    const uint16_t *k_tree;    /* [R, P, Hkv, d] */
+    const uint16_t *v_tree;    /* [R, P, Hkv, d] */
+    uint16_t *k_cache;         /* [num_pages, page_size, Hkv, d], compacted in place */
+    uint16_t *v_cache;
+    const int32_t *block_table; /* [R, max_pages_per_req] */
+    int32_t *ctx_lens;          /* [R], grows by acc_len */
+    float *top_lp;              /* [R, L, K] */
+    int32_t *top_ids;           /* [R, L, K] */
+    int32_t *tree_tokens;       /* [R, B] */
+    int32_t *parents;           /* [R, P] */
+    int32_t *depths;            /* [R, P] */
+    int32_t *n_nodes;           /* [R] */
+    uint32_t *mask;             /* [R, P, W] */
+    uint16_t *attn_out;         /* [R, P, Hq, d] */
+    int32_t *target_argmax;     /* [R, P], may be NULL */
+    int32_t *acc_len;           /* [R] */
+    int32_t *acc_nodes;         /* [R, L] */
+    int32_t *acc_tokens;        /* [R, L+1] */
+    int32_t *bonus;             /* [R] */
+} ddt_round_args;
+
+/* a1..a7 chained on one stream with no host synchronisation. */
+ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *args, void *stream);
+
+/* Wait for the context's device to finish all enqueued work, copy the
+ * device status word to *host_out (DDT_DEV_* bits) and clear it. */
+ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);
+
+/* Static text for a status code. */
+const char *ddt_strerror(ddt_status status);
+
+/* The CUDA error code behind the most recent DDT_ECUDA of this thread. */
+int32_t ddt_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DDT_H */

@@ -1,0 +1,489 @@
+// api.cu -- the extern "C" boundary of libddt.so: argument validation,
+// workspace layout and the launch sequence of a round. Every check that can
+// be made on the host is made here, before anything is enqueued.
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "ddt_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+ddt_status cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error = (int)e;
+    return DDT_ECUDA;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// resolve K and check every field; fills *out with the resolved config
+ddt_status check_config(const ddt_config *in, ddt_config *out)
+{
+    if (in == nullptr)
+        return DDT_EINVAL;
+    ddt_config c = *in;
+    if (c.K == 0)
+        c.K = c.B < c.V ? c.B : c.V;
+    if (c.R_max < 1 || c.L < 1 || c.V < 1 || c.B < 1 || c.K < 1 || c.K > c.V)
+        return DDT_EINVAL;
+    if (c.Hq < 1 || c.Hkv < 1 || c.Hq % c.Hkv != 0 || c.page_size < 1 ||
+        c.max_pages_per_req < 1 || c.num_pages < 1)
+        return DDT_EINVAL;
+    if ((c.draft_dtype != DDT_BF16 && c.draft_dtype != DDT_F32) ||
+        (c.target_dtype != DDT_BF16 && c.target_dtype != DDT_F32))
+        return DDT_EINVAL;
+    if (c.L > DDT_MAX_L || c.K > DDT_MAX_K || c.B > DDT_MAX_B)
+        return DDT_EUNSUPPORTED;
+    if (c.d != 64 && c.d != 128)
+        return DDT_EUNSUPPORTED;
+    if (c.Hkv > 255)
+        return DDT_EUNSUPPORTED;
+    const int nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
+    if ((int64_t)nch * c.K > TOPK_CAND_CAP)
+        return DDT_EUNSUPPORTED;
+    const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
+    if (max_ctx > (int64_t)64 * ATT_CHUNK || c.R_max > 2048)
+        return DDT_EUNSUPPORTED;
+    *out = c;
+    return DDT_OK;
+}
+
+struct Layout {
+    size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
+        att_rg_base, att_part_o, att_part_ml, total;
+    int tk_nch, am_nch, rowgroups, max_items;
+};
+
+Layout layout_for(const ddt_config &c)
+{
+    Layout L;
+    const int P = c.B + 1, G = c.Hq / c.Hkv;
+    L.tk_nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
+    L.am_nch = (c.V + amax_chunk_elems(c.target_dtype) - 1) / amax_chunk_elems(c.target_dtype);
+    L.rowgroups = (P * G + ATT_ROWS - 1) / ATT_ROWS;
+    const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
+    const int ns_max = (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK) > 0
+                           ? (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK)
+                           : 1;
+    L.max_items = c.R_max * c.Hkv * L.rowgroups * ns_max;
+    const size_t rows_d = (size_t)c.R_max * c.L, rows_t = (size_t)c.R_max * P;
+    const size_t rg = (size_t)c.R_max * c.Hkv * L.rowgroups;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align_up(off + bytes, 256);
+        return at;
+    };
+    L.status = take(sizeof(int32_t));
+    L.tk_val = take(rows_d * L.tk_nch * c.K * sizeof(float));
+    L.tk_idx = take(rows_d * L.tk_nch * c.K * sizeof(int32_t));
+    L.tk_ms = take(rows_d * L.tk_nch * sizeof(float2));
+    L.tk_cnt = take(rows_d * sizeof(unsigned));
+    L.am_val = take(rows_t * L.am_nch * sizeof(float));
+    L.am_idx = take(rows_t * L.am_nch * sizeof(int32_t));
+    L.att_items = take((size_t)L.max_items * sizeof(int4));
+    L.att_meta = take(4 * sizeof(int32_t));
+    L.att_rg_cnt = take(rg * sizeof(unsigned));
+    L.att_rg_base = take(rg * sizeof(int32_t));
+    L.att_part_o = take((size_t)L.max_items * ATT_ROWS * c.d * sizeof(float));
+    L.att_part_ml = take((size_t)L.max_items * ATT_ROWS * sizeof(float2));
+    L.total = off;
+    return L;
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+
+ddt_status check_R(const ddt_ctx *ctx, int32_t R)
+{
+    if (ctx == nullptr || R < 0 || R > ctx->cfg.R_max)
+        return DDT_EINVAL;
+    return DDT_OK;
+}
+
+ddt_status set_device(const ddt_ctx *ctx)
+{
+    int cur = -1;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    if (cur != ctx->device) {
+        e = cudaSetDevice(ctx->device);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return DDT_OK;
+}
+
+#define DDT_TRY(expr)                                                                              \
+    do {                                                                                           \
+        cudaError_t _e = (expr);                                                                   \
+        if (_e != cudaSuccess)                                                                     \
+            return cuda_fail(_e);                                                                  \
+    } while (0)
+
+#define DDT_CHECK(cond)                                                                            \
+    do {                                                                                           \
+        if (!(cond))                                                                               \
+            return DDT_EINVAL;                                                                     \
+    } while (0)
+
+ddt_status chk_topk(const ddt_ctx *c, const void *z, const float *lp, const int32_t *ids)
+{
+    DDT_CHECK(z && lp && ids && aligned16(z) && aligned4(lp) && aligned4(ids));
+    (void)c;
+    return DDT_OK;
+}
+
+ddt_status chk_tree(const float *lp, const int32_t *ids, const int32_t *tok, const int32_t *par,
+                    const int32_t *dep, const int32_t *nn)
+{
+    DDT_CHECK(lp && ids && tok && par && dep && nn);
+    DDT_CHECK(aligned4(lp) && aligned4(ids) && aligned4(tok) && aligned4(par) && aligned4(dep) &&
+              aligned4(nn));
+    return DDT_OK;
+}
+
+ddt_status chk_attn(const uint16_t *q, const uint16_t *kt, const uint16_t *vt, const uint16_t *kc,
+                    const uint16_t *vc, const int32_t *bt, const int32_t *cl, const uint32_t *mask,
+                    const uint16_t *out)
+{
+    DDT_CHECK(q && kt && vt && kc && vc && bt && cl && mask && out);
+    DDT_CHECK(aligned16(q) && aligned16(kt) && aligned16(vt) && aligned16(kc) && aligned16(vc) &&
+              aligned16(out) && aligned4(bt) && aligned4(cl) && aligned4(mask));
+    return DDT_OK;
+}
+
+ddt_status chk_walk(const int32_t *tok, const int32_t *par, const int32_t *nn, const int32_t *al,
+                    const int32_t *an, const int32_t *at, const int32_t *bo)
+{
+    DDT_CHECK(tok && par && nn && al && an && at && bo);
+    return DDT_OK;
+}
+
+ddt_status chk_compact(const uint16_t *kc, const uint16_t *vc, const int32_t *bt,
+                       const int32_t *cl, const uint16_t *kt, const uint16_t *vt)
+{
+    DDT_CHECK(kc && vc && bt && cl && kt && vt);
+    DDT_CHECK(aligned16(kc) && aligned16(vc) && aligned16(kt) && aligned16(vt));
+    return DDT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ddt_workspace_bytes(const ddt_config *cfg)
+{
+    ddt_config c;
+    if (check_config(cfg, &c) != DDT_OK)
+        return 0;
+    return layout_for(c).total;
+}
+
+ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
+{
+    if (out == nullptr)
+        return DDT_EINVAL;
+    *out = nullptr;
+    ddt_config c;
+    const ddt_status st = check_config(cfg, &c);
+    if (st != DDT_OK)
+        return st;
+    ddt_ctx *ctx = (ddt_ctx *)calloc(1, sizeof(ddt_ctx));
+    if (ctx == nullptr)
+        return DDT_ENOMEM;
+    ctx->cfg = c;
+    cudaError_t e = cudaGetDevice(&ctx->device);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+    if (e != cudaSuccess) {
+        free(ctx);
+        return cuda_fail(e);
+    }
+    const Layout L = layout_for(c);
+    e = cudaMalloc((void **)&ctx->ws, L.total);
+    if (e != cudaSuccess) {
+        free(ctx);
+        g_last_cuda_error = (int)e;
+        return DDT_ENOMEM;
+    }
+    e = cudaMemset(ctx->ws, 0, L.total);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(ctx->ws);
+        free(ctx);
+        return cuda_fail(e);
+    }
+    ctx->ws_bytes = L.total;
+    char *w = ctx->ws;
+    ctx->status = (int32_t *)(w + L.status);
+    ctx->tk_nch = L.tk_nch;
+    ctx->tk_val = (float *)(w + L.tk_val);
+    ctx->tk_idx = (int32_t *)(w + L.tk_idx);
+    ctx->tk_ms = (float2 *)(w + L.tk_ms);
+    ctx->tk_cnt = (unsigned *)(w + L.tk_cnt);
+    ctx->am_nch = L.am_nch;
+    ctx->am_val = (float *)(w + L.am_val);
+    ctx->am_idx = (int32_t *)(w + L.am_idx);
+    ctx->att_rowgroups = L.rowgroups;
+    ctx->att_max_items = L.max_items;
+    ctx->att_items = (int4 *)(w + L.att_items);
+    ctx->att_meta = (int32_t *)(w + L.att_meta);
+    ctx->att_rg_cnt = (unsigned *)(w + L.att_rg_cnt);
+    ctx->att_rg_base = (int32_t *)(w + L.att_rg_base);
+    ctx->att_part_o = (float *)(w + L.att_part_o);
+    ctx->att_part_ml = (float2 *)(w + L.att_part_ml);
+    ctx->att_grid = ctx->num_sms;
+    *out = ctx;
+    return DDT_OK;
+}
+
+void ddt_destroy(ddt_ctx *ctx)
+{
+    if (ctx == nullptr)
+        return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    cudaSetDevice(ctx->device);
+    cudaFree(ctx->ws);
+    if (cur >= 0)
+        cudaSetDevice(cur);
+    free(ctx);
+}
+
+ddt_status ddt_topk_logprobs(ddt_ctx *ctx, const void *draft_logits, int32_t R, float *top_lp,
+                             int32_t *top_ids, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if ((st = chk_topk(ctx, draft_logits, top_lp, top_ids)) != DDT_OK)
+        return st;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_topk(ctx, draft_logits, R, top_lp, top_ids, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_build_tree(ddt_ctx *ctx, const float *top_lp, const int32_t *top_ids, int32_t R,
+                          int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                          int32_t *n_nodes, uint32_t *mask, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if ((st = chk_tree(top_lp, top_ids, tree_tokens, parents, depths, n_nodes)) != DDT_OK)
+        return st;
+    if (mask != nullptr && !aligned4(mask))
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_build_tree(ctx, top_lp, top_ids, R, tree_tokens, parents, depths, n_nodes, mask,
+                              (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_build_mask(ddt_ctx *ctx, const int32_t *parents, const int32_t *n_nodes, int32_t R,
+                          uint32_t *mask, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!parents || !n_nodes || !mask || !aligned4(parents) || !aligned4(n_nodes) || !aligned4(mask))
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_build_mask(ctx, parents, n_nodes, R, mask, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_tree_attention(ddt_ctx *ctx, const uint16_t *q, const uint16_t *k_tree,
+                              const uint16_t *v_tree, const uint16_t *k_cache,
+                              const uint16_t *v_cache, const int32_t *block_table,
+                              const int32_t *ctx_lens, const uint32_t *mask, int32_t R,
+                              uint16_t *out, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if ((st = chk_attn(q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, mask, out)) !=
+        DDT_OK)
+        return st;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_attention(ctx, q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, mask,
+                             R, out, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_target_argmax(ddt_ctx *ctx, const void *target_logits, int32_t R,
+                             int32_t *argmax_out, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!target_logits || !argmax_out || !aligned16(target_logits) || !aligned4(argmax_out))
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_argmax_partials(ctx, target_logits, R, (cudaStream_t)stream));
+    DDT_TRY(launch_argmax_finish(ctx, R, argmax_out, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_walk(ddt_ctx *ctx, const int32_t *argmax, const int32_t *tree_tokens,
+                    const int32_t *parents, const int32_t *n_nodes, int32_t R, int32_t *acc_len,
+                    int32_t *acc_nodes, int32_t *acc_tokens, int32_t *bonus, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!argmax || (st = chk_walk(tree_tokens, parents, n_nodes, acc_len, acc_nodes, acc_tokens,
+                                  bonus)) != DDT_OK)
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_walk_compact(ctx, argmax, false, nullptr, tree_tokens, parents, n_nodes, R,
+                                acc_len, acc_nodes, acc_tokens, bonus, true, false, nullptr,
+                                nullptr, nullptr, nullptr, nullptr, nullptr, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_compact(ddt_ctx *ctx, uint16_t *k_cache, uint16_t *v_cache,
+                       const int32_t *block_table, int32_t *ctx_lens, const uint16_t *k_tree,
+                       const uint16_t *v_tree, const int32_t *acc_nodes, const int32_t *acc_len,
+                       int32_t R, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!acc_nodes || !acc_len ||
+        (st = chk_compact(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree)) != DDT_OK)
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_walk_compact(ctx, nullptr, false, nullptr, nullptr, nullptr, nullptr, R,
+                                const_cast<int32_t *>(acc_len), const_cast<int32_t *>(acc_nodes),
+                                nullptr, nullptr, false, true, k_cache, v_cache, block_table,
+                                ctx_lens, k_tree, v_tree, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tree_tokens,
+                      const int32_t *parents, const int32_t *n_nodes, int32_t R,
+                      int32_t *argmax_out, int32_t *acc_len, int32_t *acc_nodes,
+                      int32_t *acc_tokens, int32_t *bonus, uint16_t *k_cache, uint16_t *v_cache,
+                      const int32_t *block_table, const uint16_t *k_tree, const uint16_t *v_tree,
+                      int32_t *ctx_lens, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!target_logits || !aligned16(target_logits))
+        return DDT_EINVAL;
+    if ((st = chk_walk(tree_tokens, parents, n_nodes, acc_len, acc_nodes, acc_tokens, bonus)) !=
+            DDT_OK ||
+        (st = chk_compact(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree)) != DDT_OK)
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    DDT_TRY(launch_argmax_partials(ctx, target_logits, R, s));
+    DDT_TRY(launch_walk_compact(ctx, nullptr, true, argmax_out, tree_tokens, parents, n_nodes, R,
+                                acc_len, acc_nodes, acc_tokens, bonus, true, true, k_cache, v_cache,
+                                block_table, ctx_lens, k_tree, v_tree, s));
+    return DDT_OK;
+}
+
+ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *a, void *stream)
+{
+    if (a == nullptr)
+        return DDT_EINVAL;
+    const int32_t R = a->R;
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if ((st = chk_topk(ctx, a->draft_logits, a->top_lp, a->top_ids)) != DDT_OK ||
+        (st = chk_tree(a->top_lp, a->top_ids, a->tree_tokens, a->parents, a->depths,
+                       a->n_nodes)) != DDT_OK ||
+        (st = chk_attn(a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache, a->block_table,
+                       a->ctx_lens, a->mask, a->attn_out)) != DDT_OK ||
+        (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
+                       a->acc_tokens, a->bonus)) != DDT_OK)
+        return st;
+    if (!a->target_logits || !aligned16(a->target_logits))
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    DDT_TRY(launch_topk(ctx, a->draft_logits, R, a->top_lp, a->top_ids, s));
+    DDT_TRY(launch_build_tree(ctx, a->top_lp, a->top_ids, R, a->tree_tokens, a->parents,
+                              a->depths, a->n_nodes, a->mask, s));
+    DDT_TRY(launch_attention(ctx, a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache,
+                             a->block_table, a->ctx_lens, a->mask, R, a->attn_out, s));
+    DDT_TRY(launch_argmax_partials(ctx, a->target_logits, R, s));
+    DDT_TRY(launch_walk_compact(ctx, nullptr, true, a->target_argmax, a->tree_tokens, a->parents,
+                                a->n_nodes, R, a->acc_len, a->acc_nodes, a->acc_tokens, a->bonus,
+                                true, true, a->k_cache, a->v_cache, a->block_table, a->ctx_lens,
+                                a->k_tree, a->v_tree, s));
+    return DDT_OK;
+}
+
+ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out)
+{
+    if (ctx == nullptr || host_out == nullptr)
+        return DDT_EINVAL;
+    ddt_status st = set_device(ctx);
+    if (st != DDT_OK)
+        return st;
+    DDT_TRY(cudaDeviceSynchronize());
+    DDT_TRY(cudaMemcpy(host_out, ctx->status, sizeof(int32_t), cudaMemcpyDeviceToHost));
+    DDT_TRY(cudaMemset(ctx->status, 0, sizeof(int32_t)));
+    DDT_TRY(cudaDeviceSynchronize());
+    return DDT_OK;
+}
+
+const char *ddt_strerror(ddt_status status)
+{
+    switch (status) {
+    case DDT_OK:
+        return "ok";
+    case DDT_EINVAL:
+        return "invalid argument";
+    case DDT_EUNSUPPORTED:
+        return "unsupported configuration";
+    case DDT_ECUDA:
+        return "CUDA runtime error";
+    case DDT_ENOMEM:
+        return "out of device memory";
+    }
+    return "unknown status";
+}
+
+int32_t ddt_last_cuda_error(void) { return (int32_t)g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// ddt_internal.h -- context layout and kernel launchers shared by the
+// translation units of libddt.so. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ddt.h"
+
+// ---------------------------------------------------------------- limits
+constexpr int DDT_MAX_L = 18;    // rank tuples pack 18 fields of 7 bits into 128 bits
+constexpr int DDT_MAX_K = 127;   // rank + 1 must fit a 7-bit field
+constexpr int DDT_MAX_B = 127;   // frontier of <= B entries in 4 slots per lane
+constexpr int DDT_MAX_P = 128;   // tree positions (B + 1)
+
+// a1: one CTA of TOPK_THREADS reads one chunk of a row
+constexpr int TOPK_THREADS = 256;
+constexpr int TOPK_VEC_PER_THREAD = 8;   // 16-byte vectors per thread per chunk
+constexpr int TOPK_CAND_CAP = 2048;      // candidate buffer entries
+
+// a5: same chunking as a1
+constexpr int AMAX_THREADS = 256;
+constexpr int AMAX_VEC_PER_THREAD = 8;
+
+// a4: work items of at most ATT_CHUNK cached tokens per (request, KV head)
+constexpr int ATT_CHUNK = 4096;
+constexpr int ATT_BLOCK_N = 64;          // KV tokens per pipeline stage
+constexpr int ATT_MTILES = 9;            // m16 tiles (warps) per row group
+constexpr int ATT_ROWS = ATT_MTILES * 16;  // query rows per row group (144)
+constexpr int ATT_THREADS = ATT_MTILES * 32;
+constexpr int ATT_STAGES = 3;
+
+struct ddt_ctx {
+    ddt_config cfg;  // with K resolved
+    int device;
+    int num_sms;
+    size_t ws_bytes;
+    char *ws;                // one allocation, carved below
+    int32_t *status;         // device status word
+    // a1 partials
+    int tk_nch;              // chunks per row
+    float *tk_val;           // [R_max * L, nch, K]
+    int32_t *tk_idx;         // [R_max * L, nch, K]
+    float2 *tk_ms;           // [R_max * L, nch] (max, sum of exp)
+    unsigned *tk_cnt;        // [R_max * L] arrival counters (self-resetting)
+    // a5 partials
+    int am_nch;
+    float *am_val;           // [R_max * P, nch]
+    int32_t *am_idx;         // [R_max * P, nch]
+    // a4 plan + partials
+    int att_rowgroups;       // ceil(P * G / ATT_ROWS)
+    int att_max_items;
+    int4 *att_items;         // [max_items] (r, g | rowgroup << 16, t0, t1)
+    int32_t *att_meta;       // [0] = item count, [1] = work counter, [2] = done counter
+    unsigned *att_rg_cnt;    // [R_max * Hkv * rowgroups] arrival counters
+    int32_t *att_rg_base;    // [R_max * Hkv * rowgroups] first item of each (r, g, rowgroup)
+    float *att_part_o;       // [max_items, ATT_ROWS, d]
+    float2 *att_part_ml;     // [max_items, ATT_ROWS]
+    int att_grid;            // persistent CTAs
+};
+
+// launchers (return the cudaGetLastError of the launch)
+cudaError_t launch_topk(const ddt_ctx *c, const void *z, int R, float *top_lp, int32_t *top_ids,
+                        cudaStream_t s);
+cudaError_t launch_build_tree(const ddt_ctx *c, const float *top_lp, const int32_t *top_ids, int R,
+                              int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                              int32_t *n_nodes, uint32_t *mask, cudaStream_t s);
+cudaError_t launch_build_mask(const ddt_ctx *c, const int32_t *parents, const int32_t *n_nodes,
+                              int R, uint32_t *mask, cudaStream_t s);
+cudaError_t launch_argmax_partials(const ddt_ctx *c, const void *t, int R, cudaStream_t s);
+cudaError_t launch_argmax_finish(const ddt_ctx *c, int R, int32_t *argmax_out, cudaStream_t s);
+cudaError_t launch_walk_compact(const ddt_ctx *c, const int32_t *argmax, bool argmax_from_partials,
+                                int32_t *argmax_out, const int32_t *tree_tokens,
+                                const int32_t *parents, const int32_t *n_nodes, int R,
+                                int32_t *acc_len, int32_t *acc_nodes, int32_t *acc_tokens,
+                                int32_t *bonus, bool do_walk, bool do_compact, uint16_t *k_cache,
+                                uint16_t *v_cache, const int32_t *block_table, int32_t *ctx_lens,
+                                const uint16_t *k_tree, const uint16_t *v_tree, cudaStream_t s);
+cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
+                             const uint16_t *v_tree, const uint16_t *k_cache,
+                             const uint16_t *v_cache, const int32_t *block_table,
+                             const int32_t *ctx_lens, const uint32_t *mask, int R, uint16_t *out,
+                             cudaStream_t s);
+
+// sizes used by both the workspace carve-up and the launchers
+int topk_chunk_elems(int dtype);
+int amax_chunk_elems(int dtype);

@@ -1,0 +1,429 @@
+// topk.cu -- a1: per-depth log-softmax and top-K over the vocabulary.
+//
+// "SparklingTree: 30-40% faster speculative decoding over DSpark", Step 1
+// (top-K of each depth row of the drafter's marginals and the row's
+// logsumexp; log-probs are logits minus logsumexp) and "DDTree Explained
+// ...", section 3, Lemma 1 (K = min(B, |V|) keeps the optimal tree).
+//
+// Design (HBM-bound: each logit is read once):
+//  * A row of V logits is cut into chunks of TOPK_THREADS * 8 vectors of
+//    16 bytes; one CTA per (chunk, row). Each thread keeps its 8 vectors in
+//    registers: pass 1 takes its max, pass 2 sums exp2((x - max) * log2 e)
+//    on the MUFU unit; the CTA combines (max, sum) pairs with shuffles.
+//  * Candidate filter: every lane's max is a distinct element of the chunk,
+//    so if each of the 8 warps finds its ceil(K/8)-th largest lane max, the
+//    smallest of those, T0, has at least K chunk elements >= T0 and no
+//    element of the chunk's top-K lies below it. Only threads whose max is
+//    >= T0 scan their registers; survivors go to a shared buffer.
+//  * The exact order (value desc, token id asc) is decided by counting, for
+//    each survivor, how many survivors beat it. If the filter lets through
+//    too many (flat or heavily tied rows), an exact bitwise search over the
+//    ordered 32-bit keys and the chunk-local index picks exactly K.
+//  * The CTA that finishes a row last (atomic arrival counter) merges the
+//    per-chunk sorted lists by binary search and the per-chunk (max, sum)
+//    into logZ (final combination in fp64), then writes lp = z - logZ.
+#include <stdint.h>
+
+#include "ddt_device.cuh"
+#include "ddt_internal.h"
+
+namespace {
+
+constexpr int NV = TOPK_VEC_PER_THREAD;
+constexpr int SELECT_MAX = 512;  // above this many survivors, use the exact search
+
+template <typename T> struct Elem;
+template <> struct Elem<uint16_t> {
+    static constexpr int VE = 8;
+    static constexpr uint32_t NEG_INF_FILL = 0xFF80FF80u;
+    DDT_DEVINL static float get(const uint4 &v, int e)
+    {
+        const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+        return (e & 1) ? bf16hi(w) : bf16lo(w);
+    }
+};
+template <> struct Elem<float> {
+    static constexpr int VE = 4;
+    static constexpr uint32_t NEG_INF_FILL = 0xFF800000u;
+    DDT_DEVINL static float get(const uint4 &v, int e)
+    {
+        const uint32_t w = (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+        return __uint_as_float(w);
+    }
+};
+
+// scalar gather of one vector's worth of elements (unaligned rows / tails)
+template <typename T>
+DDT_DEVINL uint4 load_scalar(const T *p, int valid)
+{
+    uint32_t w[4] = {Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL,
+                     Elem<T>::NEG_INF_FILL};
+    if constexpr (sizeof(T) == 2) {
+        for (int e = 0; e < 8; ++e)
+            if (e < valid) {
+                const uint32_t b = (uint32_t)__ldg(reinterpret_cast<const unsigned short *>(p) + e);
+                if (e & 1)
+                    w[e >> 1] = (w[e >> 1] & 0x0000FFFFu) | (b << 16);
+                else
+                    w[e >> 1] = (w[e >> 1] & 0xFFFF0000u) | b;
+            }
+    } else {
+        for (int e = 0; e < 4; ++e)
+            if (e < valid)
+                w[e] = __float_as_uint(__ldg(reinterpret_cast<const float *>(p) + e));
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// merge two (max, sum-of-exp) pairs
+DDT_DEVINL void ms_combine(float &m, float &s, float mo, float so)
+{
+    const float M = fmaxf(m, mo);
+    float r = 0.f;
+    if (m != DDT_NEG_INF)
+        r += s * ex2((m - M) * DDT_LOG2E);
+    if (mo != DDT_NEG_INF)
+        r += so * ex2((mo - M) * DDT_LOG2E);
+    m = M;
+    s = r;
+}
+
+// total ordering key of a finite float (-0 == +0); larger float -> larger key
+DDT_DEVINL uint32_t okey(float x)
+{
+    const uint32_t b = __float_as_uint(x + 0.0f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// one element as fp32 (the exact fallback's re-read)
+template <typename T>
+DDT_DEVINL float load_one(const T *p, int i)
+{
+    if constexpr (sizeof(T) == 2)
+        return bf16_to_f32(__ldg(reinterpret_cast<const unsigned short *>(p) + i));
+    else
+        return __ldg(reinterpret_cast<const float *>(p) + i);
+}
+
+DDT_DEVINL int block_sum(int v, int *s_acc)
+{
+    // s_acc must be zero on entry; returns the CTA-wide sum to every thread
+    v = __reduce_add_sync(0xFFFFFFFFu, v);
+    if ((threadIdx.x & 31) == 0)
+        atomicAdd(s_acc, v);
+    __syncthreads();
+    const int total = *s_acc;
+    __syncthreads();
+    if (threadIdx.x == 0)
+        *s_acc = 0;
+    __syncthreads();
+    return total;
+}
+
+template <typename T, bool ALIGNED>
+__global__ void __launch_bounds__(TOPK_THREADS)
+topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restrict__ part_val,
+                  int32_t *__restrict__ part_idx, float2 *__restrict__ part_ms,
+                  unsigned *__restrict__ cnt, float *__restrict__ top_lp,
+                  int32_t *__restrict__ top_ids, int32_t *__restrict__ status)
+{
+    constexpr int VE = Elem<T>::VE;
+    constexpr int CH = TOPK_THREADS * NV * VE;
+    const int chunk = blockIdx.x, row = blockIdx.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const T *zrow = z + (int64_t)row * V;
+    const int c0 = chunk * CH;
+    const int cn = min(CH, V - c0);
+
+    __shared__ float s_val[TOPK_CAND_CAP];
+    __shared__ int s_idx[TOPK_CAND_CAP];
+    __shared__ float s_wm[TOPK_THREADS / 32], s_ws[TOPK_THREADS / 32], s_wt[TOPK_THREADS / 32];
+    __shared__ int s_count, s_acc, s_last;
+    __shared__ double s_logz;
+
+    // ---- load this thread's vectors (coalesced: consecutive threads, consecutive 16 B)
+    uint4 raw[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int e0 = (j * TOPK_THREADS + tid) * VE;
+        if (ALIGNED) {
+            if (e0 < cn)
+                raw[j] = ldg_stream(zrow + c0 + e0);
+            else
+                raw[j] = make_uint4(Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL,
+                                    Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL);
+        } else {
+            raw[j] = load_scalar<T>(zrow + c0 + e0, e0 < cn ? min(VE, cn - e0) : 0);
+        }
+    }
+    if (tid == 0) {
+        s_count = 0;
+        s_acc = 0;
+    }
+
+    // ---- pass 1: thread max; pass 2: sum of exp relative to it
+    float m = DDT_NEG_INF;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int e = 0; e < VE; ++e)
+            m = fmaxf(m, Elem<T>::get(raw[j], e));
+    float s = 0.f;
+    if (m != DDT_NEG_INF) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+#pragma unroll
+            for (int e = 0; e < VE; ++e)
+                s += ex2((Elem<T>::get(raw[j], e) - m) * DDT_LOG2E);
+    }
+    const float lane_max = m;
+
+    // ---- per-warp quota threshold: ceil(K/8)-th largest lane max (bitonic sort, descending)
+    float v = lane_max;
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int jj = k >> 1; jj > 0; jj >>= 1) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
+            const bool want_max = ((lane & k) == 0) == ((lane & jj) == 0);
+            v = want_max ? fmaxf(v, o) : fminf(v, o);
+        }
+    const int quota = (K + (TOPK_THREADS / 32) - 1) / (TOPK_THREADS / 32);
+    const float warp_t = __shfl_sync(0xFFFFFFFFu, v, quota - 1);
+
+    // ---- CTA (max, sum)
+    float mm = m, ss = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float mo = __shfl_xor_sync(0xFFFFFFFFu, mm, off);
+        const float so = __shfl_xor_sync(0xFFFFFFFFu, ss, off);
+        ms_combine(mm, ss, mo, so);
+    }
+    if (lane == 0) {
+        s_wm[warp] = mm;
+        s_ws[warp] = ss;
+        s_wt[warp] = warp_t;
+    }
+    __syncthreads();
+    float cm = s_wm[0], cs = s_ws[0], T0 = s_wt[0];
+#pragma unroll
+    for (int w = 1; w < TOPK_THREADS / 32; ++w) {
+        ms_combine(cm, cs, s_wm[w], s_ws[w]);
+        T0 = fminf(T0, s_wt[w]);
+    }
+
+    // ---- survivors of the filter
+    if (lane_max >= T0) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e0 = (j * TOPK_THREADS + tid) * VE;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const float x = Elem<T>::get(raw[j], e);
+                if (x >= T0 && e0 + e < cn) {
+                    const int pos = atomicAdd(&s_count, 1);
+                    if (pos < TOPK_CAND_CAP) {
+                        s_val[pos] = x;
+                        s_idx[pos] = c0 + e0 + e;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    int n = s_count;
+
+    if (n > SELECT_MAX) {
+        // ---- exact fallback (flat or heavily tied chunks): re-read the chunk
+        // from global memory, find the K-th largest key t bit by bit, then
+        // the lowest-index ties at t
+        __syncthreads();
+        const T *cz = zrow + c0;
+        uint32_t t = 0;
+        for (int b = 31; b >= 0; --b) {
+            const uint32_t cand = t | (1u << b);
+            int c = 0;
+#pragma unroll 1
+            for (int li = tid; li < cn; li += TOPK_THREADS) {
+                const float x = load_one(cz, li);
+                c += (x == x && okey(x) >= cand) ? 1 : 0;
+            }
+            if (block_sum(c, &s_acc) >= K)
+                t = cand;
+        }
+        int gt = 0;
+#pragma unroll 1
+        for (int li = tid; li < cn; li += TOPK_THREADS) {
+            const float x = load_one(cz, li);
+            gt += (x == x && okey(x) > t) ? 1 : 0;
+        }
+        const int need = K - block_sum(gt, &s_acc);
+        int I = 0;  // largest I with #(ties at chunk-local index < I) < need
+        for (int b = 15; b >= 0; --b) {
+            const int cand = I | (1 << b);
+            int c = 0;
+#pragma unroll 1
+            for (int li = tid; li < cn && li < cand; li += TOPK_THREADS) {
+                const float x = load_one(cz, li);
+                c += (x == x && okey(x) == t) ? 1 : 0;
+            }
+            if (block_sum(c, &s_acc) < need)
+                I = cand;
+        }
+        if (tid == 0)
+            s_count = 0;
+        __syncthreads();
+#pragma unroll 1
+        for (int li = tid; li < cn; li += TOPK_THREADS) {
+            const float x = load_one(cz, li);
+            if (x == x) {
+                const uint32_t kx = okey(x);
+                if (kx > t || (kx == t && li <= I)) {
+                    const int pos = atomicAdd(&s_count, 1);
+                    s_val[pos] = x;
+                    s_idx[pos] = c0 + li;
+                }
+            }
+        }
+        __syncthreads();
+        n = s_count;
+    }
+
+    // ---- exact ranks of the survivors -> this chunk's sorted top-K
+    const bool single = (nch == 1);
+    float *pv = part_val + ((int64_t)row * nch + chunk) * K;
+    int32_t *pi = part_idx + ((int64_t)row * nch + chunk) * K;
+    if (single && tid == 0) {
+        if (cs != cs)
+            set_status(status, DDT_DEV_NAN_LOGITS);
+        s_logz = (double)cm + log((double)cs);
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += TOPK_THREADS) {
+        const float vi = s_val[i];
+        const int ii = s_idx[i];
+        int rank = 0;
+        for (int jx = 0; jx < n; ++jx)
+            rank += beats(s_val[jx], s_idx[jx], vi, ii) ? 1 : 0;
+        if (rank < K) {
+            if (single) {
+                top_lp[(int64_t)row * K + rank] = (float)((double)vi - s_logz);
+                top_ids[(int64_t)row * K + rank] = ii;
+            } else {
+                pv[rank] = vi;
+                pi[rank] = ii;
+            }
+        }
+    }
+    for (int rank = n + tid; rank < K; rank += TOPK_THREADS) {
+        if (single) {
+            top_lp[(int64_t)row * K + rank] = DDT_NEG_INF;
+            top_ids[(int64_t)row * K + rank] = -1;
+        } else {
+            pv[rank] = DDT_NEG_INF;
+            pi[rank] = 0x7FFFFFFF;
+        }
+    }
+    if (single)
+        return;
+    if (tid == 0)
+        part_ms[(int64_t)row * nch + chunk] = make_float2(cm, cs);
+
+    // ---- arrival; the last CTA of the row merges
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+        s_last = (atomicAdd(&cnt[row], 1u) == (unsigned)(nch - 1));
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+
+    const int total = nch * K;
+    const float *rv = part_val + (int64_t)row * nch * K;
+    const int32_t *ri = part_idx + (int64_t)row * nch * K;
+    for (int i = tid; i < total; i += TOPK_THREADS) {
+        s_val[i] = __ldcg(rv + i);
+        s_idx[i] = __ldcg(ri + i);
+    }
+    if (tid == 0) {
+        float M = DDT_NEG_INF;
+        for (int c = 0; c < nch; ++c)
+            M = fmaxf(M, __ldcg(&part_ms[(int64_t)row * nch + c].x));
+        float S = 0.f;
+        for (int c = 0; c < nch; ++c) {
+            const float2 ms = __ldcg(&part_ms[(int64_t)row * nch + c]);
+            if (ms.x != DDT_NEG_INF)
+                S += ms.y * ex2((ms.x - M) * DDT_LOG2E);
+        }
+        if (S != S)
+            set_status(status, DDT_DEV_NAN_LOGITS);
+        s_logz = (double)M + log((double)S);
+        cnt[row] = 0u;  // ready for the next launch
+    }
+    __syncthreads();
+    for (int i = tid; i < total; i += TOPK_THREADS) {
+        const int a = i / K, rho = i - a * K;
+        const float vi = s_val[i];
+        const int ii = s_idx[i];
+        if (ii == 0x7FFFFFFF)
+            continue;
+        int rank = rho;
+        for (int b = 0; b < nch && rank < K; ++b) {
+            if (b == a)
+                continue;
+            // entries of list b that beat (vi, ii): lists are sorted, so binary search
+            int lo = 0, hi = K;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (beats(s_val[b * K + mid], s_idx[b * K + mid], vi, ii))
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank < K) {
+            top_lp[(int64_t)row * K + rank] = (float)((double)vi - s_logz);
+            top_ids[(int64_t)row * K + rank] = ii;
+        }
+    }
+}
+
+}  // namespace
+
+int topk_chunk_elems(int dtype)
+{
+    return TOPK_THREADS * NV * (dtype == DDT_BF16 ? 8 : 4);
+}
+
+cudaError_t launch_topk(const ddt_ctx *c, const void *z, int R, float *top_lp, int32_t *top_ids,
+                        cudaStream_t s)
+{
+    const ddt_config &cfg = c->cfg;
+    const int rows = R * cfg.L;
+    dim3 grid(c->tk_nch, rows);
+    const bool bf16 = cfg.draft_dtype == DDT_BF16;
+    const int esz = bf16 ? 2 : 4;
+    const bool aligned = ((int64_t)cfg.V * esz) % 16 == 0 && ((uintptr_t)z % 16) == 0;
+    if (bf16) {
+        if (aligned)
+            topk_chunk_kernel<uint16_t, true><<<grid, TOPK_THREADS, 0, s>>>(
+                (const uint16_t *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
+                c->tk_cnt, top_lp, top_ids, c->status);
+        else
+            topk_chunk_kernel<uint16_t, false><<<grid, TOPK_THREADS, 0, s>>>(
+                (const uint16_t *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
+                c->tk_cnt, top_lp, top_ids, c->status);
+    } else {
+        if (aligned)
+            topk_chunk_kernel<float, true><<<grid, TOPK_THREADS, 0, s>>>(
+                (const float *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
+                c->tk_cnt, top_lp, top_ids, c->status);
+        else
+            topk_chunk_kernel<float, false><<<grid, TOPK_THREADS, 0, s>>>(
+                (const float *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
+                c->tk_cnt, top_lp, top_ids, c->status);
+    }
+    return cudaGetLastError();
+}

@@ -1,0 +1,227 @@
+"""Thin ctypes binding over libddt.so (include/ddt.h).
+
+Argument marshalling only: every step of the round runs in the library's
+sm_103a kernels. Tensors are torch CUDA tensors (torch supplies device
+memory and streams); bf16 tensors may be torch.bfloat16 or int16/uint16
+views of the same bits. There is no fallback: if the library is missing or
+fails to load, loading raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libddt.so")
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM = 0, 1, 2, 3, 4
+BF16, F32 = 0, 1
+DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
+
+EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
+           "ddt_build_tree", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
+           "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_device_status",
+           "ddt_strerror", "ddt_last_cuda_error")
+
+
+class DdtError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.ddt_strerror(status).decode() if _lib is not None else str(status)
+        extra = ""
+        if status == ECUDA and _lib is not None:
+            extra = " (cudaError %d)" % _lib.ddt_last_cuda_error()
+        super().__init__("%s: %s%s" % (where, msg, extra))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("R_max", ctypes.c_int32), ("L", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("B", ctypes.c_int32), ("K", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("max_pages_per_req", ctypes.c_int32), ("num_pages", ctypes.c_int64),
+                ("draft_dtype", ctypes.c_int32), ("target_dtype", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+
+
+class RoundArgs(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32)] + [(n, _P) for n in (
+        "draft_logits", "target_logits", "q", "k_tree", "v_tree", "k_cache", "v_cache",
+        "block_table", "ctx_lens", "top_lp", "top_ids", "tree_tokens", "parents", "depths",
+        "n_nodes", "mask", "attn_out", "target_argmax", "acc_len", "acc_nodes", "acc_tokens",
+        "bonus")]
+
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load libddt.so and declare its signatures; raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("libddt.so not built at %s (run __graft_entry__.build())" % path)
+    L = ctypes.CDLL(path)
+    i32, i64, sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sig = {
+        "ddt_create": ([ctypes.POINTER(Config), ctypes.POINTER(_P)], i32),
+        "ddt_destroy": ([_P], None),
+        "ddt_workspace_bytes": ([ctypes.POINTER(Config)], sz),
+        "ddt_topk_logprobs": ([_P, _P, i32, _P, _P, _P], i32),
+        "ddt_build_tree": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
+        "ddt_build_mask": ([_P, _P, _P, i32, _P, _P], i32),
+        "ddt_tree_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, i32, _P, _P], i32),
+        "ddt_target_argmax": ([_P, _P, i32, _P, _P], i32),
+        "ddt_walk": ([_P, _P, _P, _P, _P, i32, _P, _P, _P, _P, _P], i32),
+        "ddt_compact": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, i32, _P], i32),
+        "ddt_accept": ([_P, _P, _P, _P, _P, i32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+                       i32),
+        "ddt_round": ([_P, ctypes.POINTER(RoundArgs), _P], i32),
+        "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
+        "ddt_strerror": ([i32], ctypes.c_char_p),
+        "ddt_last_cuda_error": ([], i32),
+    }
+    for name, (argt, rest) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = argt
+        fn.restype = rest
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, where):
+    if status != OK:
+        raise DdtError(status, where)
+
+
+def make_config(R_max, L, V, B, Hq, Hkv, d, page_size, max_pages_per_req, num_pages, K=0,
+                draft_dtype=BF16, target_dtype=BF16):
+    return Config(R_max, L, V, B, K, Hq, Hkv, d, page_size, max_pages_per_req, num_pages,
+                  draft_dtype, target_dtype)
+
+
+def workspace_bytes(cfg):
+    return int(load().ddt_workspace_bytes(ctypes.byref(cfg)))
+
+
+class Context:
+    """One ddt_ctx (and its device workspace) on the current CUDA device."""
+
+    def __init__(self, cfg):
+        lib = load()
+        self.cfg = cfg
+        h = _P()
+        _check(lib.ddt_create(ctypes.byref(cfg), ctypes.byref(h)), "ddt_create")
+        self._h = h
+        self.K = cfg.K if cfg.K else min(cfg.B, cfg.V)
+        self.P = cfg.B + 1
+        self.W = (self.P + 31) // 32
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib.ddt_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- one call per C entry point -----------------------------------------
+    def ddt_topk_logprobs(self, draft_logits, R, top_lp, top_ids, stream=None):
+        _check(_lib.ddt_topk_logprobs(self._h, _ptr(draft_logits), R, _ptr(top_lp), _ptr(top_ids),
+                                      _stream(stream)), "ddt_topk_logprobs")
+
+    def ddt_build_tree(self, top_lp, top_ids, R, tree_tokens, parents, depths, n_nodes, mask=None,
+                       stream=None):
+        _check(_lib.ddt_build_tree(self._h, _ptr(top_lp), _ptr(top_ids), R, _ptr(tree_tokens),
+                                   _ptr(parents), _ptr(depths), _ptr(n_nodes), _ptr(mask),
+                                   _stream(stream)), "ddt_build_tree")
+
+    def ddt_build_mask(self, parents, n_nodes, R, mask, stream=None):
+        _check(_lib.ddt_build_mask(self._h, _ptr(parents), _ptr(n_nodes), R, _ptr(mask),
+                                   _stream(stream)), "ddt_build_mask")
+
+    def ddt_tree_attention(self, q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens, mask,
+                           R, out, stream=None):
+        _check(_lib.ddt_tree_attention(self._h, _ptr(q), _ptr(k_tree), _ptr(v_tree), _ptr(k_cache),
+                                       _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), _ptr(mask),
+                                       R, _ptr(out), _stream(stream)), "ddt_tree_attention")
+
+    def ddt_target_argmax(self, target_logits, R, argmax_out, stream=None):
+        _check(_lib.ddt_target_argmax(self._h, _ptr(target_logits), R, _ptr(argmax_out),
+                                      _stream(stream)), "ddt_target_argmax")
+
+    def ddt_walk(self, argmax, tree_tokens, parents, n_nodes, R, acc_len, acc_nodes, acc_tokens,
+                 bonus, stream=None):
+        _check(_lib.ddt_walk(self._h, _ptr(argmax), _ptr(tree_tokens), _ptr(parents),
+                             _ptr(n_nodes), R, _ptr(acc_len), _ptr(acc_nodes), _ptr(acc_tokens),
+                             _ptr(bonus), _stream(stream)), "ddt_walk")
+
+    def ddt_compact(self, k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree, acc_nodes,
+                    acc_len, R, stream=None):
+        _check(_lib.ddt_compact(self._h, _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+                                _ptr(ctx_lens), _ptr(k_tree), _ptr(v_tree), _ptr(acc_nodes),
+                                _ptr(acc_len), R, _stream(stream)), "ddt_compact")
+
+    def ddt_accept(self, target_logits, tree_tokens, parents, n_nodes, R, argmax_out, acc_len,
+                   acc_nodes, acc_tokens, bonus, k_cache, v_cache, block_table, k_tree, v_tree,
+                   ctx_lens, stream=None):
+        _check(_lib.ddt_accept(self._h, _ptr(target_logits), _ptr(tree_tokens), _ptr(parents),
+                               _ptr(n_nodes), R, _ptr(argmax_out), _ptr(acc_len), _ptr(acc_nodes),
+                               _ptr(acc_tokens), _ptr(bonus), _ptr(k_cache), _ptr(v_cache),
+                               _ptr(block_table), _ptr(k_tree), _ptr(v_tree), _ptr(ctx_lens),
+                               _stream(stream)), "ddt_accept")
+
+    def ddt_round(self, R, bufs, stream=None):
+        """bufs: dict of tensors named like the fields of ddt_round_args."""
+        a = RoundArgs()
+        a.R = R
+        for name, _ in RoundArgs._fields_[1:]:
+            setattr(a, name, _ptr(bufs.get(name)))
+        _check(_lib.ddt_round(self._h, ctypes.byref(a), _stream(stream)), "ddt_round")
+
+    def ddt_device_status(self):
+        out = ctypes.c_int32(0)
+        _check(_lib.ddt_device_status(self._h, ctypes.byref(out)), "ddt_device_status")
+        return out.value
+
+    # -- allocation helper (plumbing) ----------------------------------------
+    def alloc_outputs(self, R, device="cuda"):
+        """Output buffers of one round for R requests, named as in ddt_round_args."""
+        c, K, P, W = self.cfg, self.K, self.P, self.W
+        i32 = dict(dtype=torch.int32, device=device)
+        return dict(
+            top_lp=torch.empty((R, c.L, K), dtype=torch.float32, device=device),
+            top_ids=torch.empty((R, c.L, K), **i32),
+            tree_tokens=torch.empty((R, c.B), **i32),
+            parents=torch.empty((R, P), **i32),
+            depths=torch.empty((R, P), **i32),
+            n_nodes=torch.empty((R,), **i32),
+            mask=torch.empty((R, P, W), **i32),
+            attn_out=torch.empty((R, P, c.Hq, c.d), dtype=torch.bfloat16, device=device),
+            target_argmax=torch.empty((R, P), **i32),
+            acc_len=torch.empty((R,), **i32),
+            acc_nodes=torch.empty((R, c.L), **i32),
+            acc_tokens=torch.empty((R, c.L + 1), **i32),
+            bonus=torch.empty((R,), **i32),
+        )

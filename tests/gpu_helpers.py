@@ -1,0 +1,76 @@
+"""Shared plumbing for the GPU parity tests: host<->device copies and one
+full round through the C ABI, with the oracle's stage results beside it.
+
+Inputs come from the seeded generators only. The target logits are built
+from the ORACLE's tree, never from the GPU's, and every oracle call gets
+host arrays that the generators (or an earlier oracle step) produced --
+except in the stage-wise comparisons, where the oracle is deliberately fed
+the GPU's fp32 log-probs to check the next stage bit-exactly.
+"""
+import numpy as np
+import torch
+
+import oracle
+from speculative_decoding_draft_depth_gb300 import ddt, synth
+
+
+def dev(a, device="cuda"):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    if a.dtype == np.uint32:
+        a = a.view(np.int32)
+    return torch.from_numpy(a).to(device)
+
+
+def host(t, dtype=None):
+    a = t.detach().cpu()
+    if a.dtype == torch.bfloat16:
+        a = a.view(torch.int16)
+    a = a.numpy()
+    if dtype is not None:
+        a = a.view(dtype)
+    return a
+
+
+def make_ctx(cfg, inp, R_max=None):
+    c = ddt.make_config(
+        R_max=R_max or cfg.R, L=cfg.L, V=cfg.V, B=cfg.B, K=cfg.K, Hq=cfg.Hq, Hkv=cfg.Hkv, d=cfg.d,
+        page_size=cfg.page, max_pages_per_req=inp["block_table"].shape[1],
+        num_pages=inp["k_cache"].shape[0],
+        draft_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32,
+        target_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32)
+    return ddt.Context(c)
+
+
+class RoundCase:
+    """One round on the GPU (ddt_round) and the oracle's view of it."""
+
+    def __init__(self, cfg, seed=None):
+        self.cfg = cfg
+        self.inp = inp = synth.draw_round_inputs(cfg, seed)
+        # oracle: fp64 log-probs and its own tree; the target follows that tree
+        self.o_lp, self.o_ids, self.o_logz, _ = oracle.topk_logprobs(inp["draft_logits"], cfg.K)
+        self.o_tree = oracle.build_tree(self.o_lp, self.o_ids, cfg.B)
+        self.target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+        self.target_logits = self.target.logits_for_tree(self.o_tree.tokens, self.o_tree.parents,
+                                                         self.o_tree.n_nodes)
+        self.ctx = make_ctx(cfg, inp)
+        d = self.d = {k: dev(inp[k]) for k in ("draft_logits", "q", "k_tree", "v_tree", "k_cache",
+                                                 "v_cache", "block_table", "ctx_lens")}
+        d["target_logits"] = dev(self.target_logits)
+        self.out = self.ctx.alloc_outputs(cfg.R)
+        bufs = dict(self.out)
+        bufs.update(d)
+        self.ctx.ddt_round(cfg.R, bufs)
+        torch.cuda.synchronize()
+        self.status = self.ctx.ddt_device_status()
+        self.g = {k: host(v) for k, v in self.out.items()}
+        self.g_k_cache = host(d["k_cache"], np.uint16)
+        self.g_v_cache = host(d["v_cache"], np.uint16)
+        self.g_ctx_lens = host(d["ctx_lens"])
+
+    # stage-wise oracle results (fed the GPU's own upstream outputs)
+    def oracle_tree_from_gpu_lp(self):
+        return oracle.build_tree(self.g["top_lp"].astype(np.float64), self.g["top_ids"],
+                                 self.cfg.B)
