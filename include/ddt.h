@@ -221,6 +221,40 @@ ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *args, void *stream);
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);
 
+/* a1 without a context, for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point.
+ *
+ * Who needs it: code that must not call cudaMalloc -- for example a hook or
+ * plugin inside a serving engine that owns all device memory and hands its
+ * extensions no workspace, or a latency-critical loop that may not risk the
+ * device-wide synchronisation an allocation can cause. ddt_create allocates
+ * a workspace, so such callers cannot use ddt_topk_logprobs.
+ *
+ * Same operation, layouts and kernel as ddt_topk_logprobs, for `rows`
+ * independent rows of V logits (draft_logits [rows, V], draft_dtype BF16 or
+ * F32; top_lp, top_ids [rows, K]). Its scratch (per-chunk partial lists,
+ * arrival counters, a status word) is one fixed array in the library's
+ * device memory, about 8.5 MB, which every GPU that loads libddt.so keeps
+ * until the process exits. No call allocates or frees device memory.
+ *
+ * Limits (DDT_EUNSUPPORTED beyond them, nothing enqueued), with
+ * chunks = ceil(V / 16384) for bf16 and ceil(V / 8192) for fp32:
+ *   rows <= DDT_NOALLOC_MAX_ROWS, rows * chunks <= DDT_NOALLOC_MAX_ROW_CHUNKS,
+ *   rows * chunks * K <= DDT_NOALLOC_MAX_ENTRIES, chunks * K <= 2048,
+ *   1 <= K <= min(127, V). Bad pointers or dtype: DDT_EINVAL.
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream
+ * capture. Every call clears the counters it needs on `stream` first, but
+ * all calls share the one array: calls that can overlap on the GPU (other
+ * streams, other threads) race and corrupt each other's results. NaN logits
+ * are not reported by this entry point. */
+#define DDT_NOALLOC_MAX_ROWS 4096
+#define DDT_NOALLOC_MAX_ROW_CHUNKS 65536
+#define DDT_NOALLOC_MAX_ENTRIES 1048576
+ddt_status ddt_topk_logprobs_noalloc(const void *draft_logits, int32_t draft_dtype, int32_t rows,
+                                     int32_t V, int32_t K, float *top_lp, int32_t *top_ids,
+                                     void *stream);
+
 /* Static text for a status code. */
 const char *ddt_strerror(ddt_status status);
 

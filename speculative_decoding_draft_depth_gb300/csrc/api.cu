@@ -487,3 +487,5 @@ const char *ddt_strerror(ddt_status status)
 int32_t ddt_last_cuda_error(void) { return (int32_t)g_last_cuda_error; }
 
 }  // extern "C"
+
+void ddt_note_cuda_error(int e) { g_last_cuda_error = e; }

@@ -82,6 +82,15 @@ cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t
                              const int32_t *ctx_lens, const uint32_t *mask, int R, uint16_t *out,
                              cudaStream_t s);
 
+// a1 with caller-supplied scratch (used by the allocation-free entry point)
+cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,
+                                float *part_val, int32_t *part_idx, float2 *part_ms,
+                                unsigned *cnt, float *top_lp, int32_t *top_ids, int32_t *status,
+                                cudaStream_t s);
+
+// records the CUDA error reported by ddt_last_cuda_error (this thread)
+void ddt_note_cuda_error(int e);
+
 // sizes used by both the workspace carve-up and the launchers
 int topk_chunk_elems(int dtype);
 int amax_chunk_elems(int dtype);

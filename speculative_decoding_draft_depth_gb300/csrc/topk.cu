@@ -427,3 +427,34 @@ cudaError_t launch_topk(const ddt_ctx *c, const void *z, int R, float *top_lp, i
     }
     return cudaGetLastError();
 }
+
+cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,
+                                float *part_val, int32_t *part_idx, float2 *part_ms,
+                                unsigned *cnt, float *top_lp, int32_t *top_ids, int32_t *status,
+                                cudaStream_t s)
+{
+    dim3 grid(nch, rows);
+    const bool bf16 = dtype == DDT_BF16;
+    const int esz = bf16 ? 2 : 4;
+    const bool aligned = ((int64_t)V * esz) % 16 == 0 && ((uintptr_t)z % 16) == 0;
+    if (bf16) {
+        if (aligned)
+            topk_chunk_kernel<uint16_t, true><<<grid, TOPK_THREADS, 0, s>>>(
+                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                status);
+        else
+            topk_chunk_kernel<uint16_t, false><<<grid, TOPK_THREADS, 0, s>>>(
+                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                status);
+    } else {
+        if (aligned)
+            topk_chunk_kernel<float, true><<<grid, TOPK_THREADS, 0, s>>>(
+                (const float *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                status);
+        else
+            topk_chunk_kernel<float, false><<<grid, TOPK_THREADS, 0, s>>>(
+                (const float *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                status);
+    }
+    return cudaGetLastError();
+}
