@@ -187,6 +187,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--stage", default="round",
+                    choices=["round", "topk", "tree", "attention", "accept"],
+                    help="time one stage alone (small profiling cases)")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="requests per round (default: the workload's 64)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -195,6 +200,8 @@ def main():
 
     from speculative_decoding_draft_depth_gb300 import synth
     cfg = synth.config(WORKLOAD, seed=synth.config(WORKLOAD).seed + rank)
+    if args.requests:
+        cfg = synth.config(WORKLOAD, R=args.requests, seed=cfg.seed)
 
     if args.impl == "reference":
         if rank != 0:
@@ -251,6 +258,11 @@ def main():
     torch.cuda.synchronize()
     if ctx.ddt_device_status() != 0:
         raise RuntimeError("device status flags set during warm-up")
+    if args.stage != "round":
+        ms = time_stages(ctx, cfg, bufs, d, ctx0, stream, reps=args.steps, only=args.stage)
+        print(json.dumps({"stage": args.stage, "requests": cfg.R, "ms": ms[args.stage],
+                          "workload": _workload_desc(cfg)}))
+        return
     acc_len = bufs["acc_len"].cpu().numpy()
 
     # ---------------- timed region: K full rounds
@@ -320,13 +332,15 @@ def main():
         dist.destroy_process_group()
 
 
-def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps):
+def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):
     import torch
     R = cfg.R
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     res = {}
 
     def run(name, fn):
+        if only is not None and name != only:
+            return
         fn()
         torch.cuda.synchronize()
         a, b = ev(), ev()
