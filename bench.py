@@ -62,7 +62,7 @@ def round_bytes(cfg, ctx_lens, acc_len=None):
     b["topk"] = R * L * V * 2 + R * L * K * 8
     b["tree"] = R * L * K * 8 + R * (cfg.B + 3 * P) * 4 + R * P * W * 4
     b["attention"] = (2 * ctx_tot * kv_row          # paged K and V
-                      + 2 * R * P * cfg.Hq * cfg.d * 2  # Q in, O out
+                      + R * P * cfg.Hq * cfg.d * (2 + 4)  # Q in (bf16), O out (f32)
                       + 2 * R * P * kv_row          # tree K and V
                       + R * P * W * 4 + R * 4)      # mask, ctx_lens
     nacc = int(np.sum(acc_len)) if acc_len is not None else R

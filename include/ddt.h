@@ -71,6 +71,7 @@ typedef enum ddt_dtype { DDT_BF16 = 0, DDT_F32 = 1 } ddt_dtype;
 #define DDT_DEV_NAN_LOGITS 0x1 /* a NaN reached top-K or argmax */
 #define DDT_DEV_BAD_PAGE 0x2   /* a block-table entry was outside [0, num_pages) */
 #define DDT_DEV_BAD_TREE 0x4   /* parents/n_nodes/acc arrays out of range */
+#define DDT_DEV_TIMEOUT 0x8    /* a bounded on-device wait gave up (the kernel wound down) */
 
 typedef struct ddt_config {
     int32_t R_max;             /* most requests a call may carry */
@@ -135,8 +136,9 @@ ddt_status ddt_build_mask(ddt_ctx *ctx, const int32_t *parents, const int32_t *n
  * "DDTree Explained ...", sections 5 and 8 (ancestor-only mask, GQA).
  * Query row (r, i, h) attends, with scale 1/sqrt(d), to the ctx_lens[r]
  * cached tokens of KV head h / (Hq / Hkv) and to the tree positions set in
- * mask row (r, i); softmax in fp32, bf16 inputs, fp32 accumulation.
- *   q, out          [R, P, Hq, d] bf16
+ * mask row (r, i); softmax in fp32, bf16 inputs, fp32 accumulation, fp32
+ * output (a bf16 output alone would round values in [2, 4) by up to 0.0078).
+ *   q               [R, P, Hq, d] bf16;  out [R, P, Hq, d] f32
  *   k_tree, v_tree  [R, P, Hkv, d] bf16 (this round's tree keys/values)
  *   k_cache,v_cache [num_pages, page_size, Hkv, d] bf16
  *   block_table     [R, max_pages_per_req] i32: page of token t is
@@ -147,7 +149,7 @@ ddt_status ddt_tree_attention(ddt_ctx *ctx, const uint16_t *q, const uint16_t *k
                               const uint16_t *v_tree, const uint16_t *k_cache,
                               const uint16_t *v_cache, const int32_t *block_table,
                               const int32_t *ctx_lens, const uint32_t *mask, int32_t R,
-                              uint16_t *out, void *stream);
+                              float *out, void *stream);
 
 /* a5 -- "DDTree Explained ...", section 5 (verifier walk under greedy
  * decoding); "Robot2050/TreeSpark" (vectorised acceptance).
@@ -206,7 +208,7 @@ typedef struct ddt_round_args {
     int32_t *depths;            /* [R, P] */
     int32_t *n_nodes;           /* [R] */
     uint32_t *mask;             /* [R, P, W] */
-    uint16_t *attn_out;         /* [R, P, Hq, d] */
+    float *attn_out;            /* [R, P, Hq, d] f32 */
     int32_t *target_argmax;     /* [R, P], may be NULL */
     int32_t *acc_len;           /* [R] */
     int32_t *acc_nodes;         /* [R, L] */

@@ -65,6 +65,12 @@ Layout layout_for(const ddt_config &c)
     L.tk_nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
     L.am_nch = (c.V + amax_chunk_elems(c.target_dtype) - 1) / amax_chunk_elems(c.target_dtype);
     L.rowgroups = (P * G + ATT_ROWS - 1) / ATT_ROWS;
+    if (c.d == 128) {  // the tensor-core kernel groups rows by 128 plus a short tail
+        int nm, tail, rg_tc;
+        attention_tc_rows(c, &nm, &tail, &rg_tc);
+        if (rg_tc > L.rowgroups)
+            L.rowgroups = rg_tc;
+    }
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
     const int ns_max = (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK) > 0
                            ? (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK)
@@ -150,7 +156,7 @@ ddt_status chk_tree(const float *lp, const int32_t *ids, const int32_t *tok, con
 
 ddt_status chk_attn(const uint16_t *q, const uint16_t *kt, const uint16_t *vt, const uint16_t *kc,
                     const uint16_t *vc, const int32_t *bt, const int32_t *cl, const uint32_t *mask,
-                    const uint16_t *out)
+                    const float *out)
 {
     DDT_CHECK(q && kt && vt && kc && vc && bt && cl && mask && out);
     DDT_CHECK(aligned16(q) && aligned16(kt) && aligned16(vt) && aligned16(kc) && aligned16(vc) &&
@@ -240,6 +246,7 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->att_part_o = (float *)(w + L.att_part_o);
     ctx->att_part_ml = (float2 *)(w + L.att_part_ml);
     ctx->att_grid = ctx->num_sms;
+    ctx->att_use_tc = attention_tc_supported(c);
     *out = ctx;
     return DDT_OK;
 }
@@ -313,7 +320,7 @@ ddt_status ddt_tree_attention(ddt_ctx *ctx, const uint16_t *q, const uint16_t *k
                               const uint16_t *v_tree, const uint16_t *k_cache,
                               const uint16_t *v_cache, const int32_t *block_table,
                               const int32_t *ctx_lens, const uint32_t *mask, int32_t R,
-                              uint16_t *out, void *stream)
+                              float *out, void *stream)
 {
     ddt_status st = check_R(ctx, R);
     if (st != DDT_OK)

@@ -112,7 +112,7 @@ __global__ void att_plan_kernel(const int32_t *__restrict__ ctx_lens, int R, int
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
         const int ns = s_ns[r], ctx = s_ctx[r], base = s_off[r];
-        const int len = (ctx + ns - 1) / ns;
+        const int len = ((ctx + ns - 1) / ns + 127) / 128 * 128;  // chunks start on 128-token tiles
         for (int s = 0; s < ns; ++s) {
             const int t0 = min(ctx, s * len), t1 = min(ctx, (s + 1) * len);
             for (int g = 0; g < Hkv; ++g)
@@ -143,7 +143,7 @@ struct AttArgs {
     const uint16_t *q, *k_tree, *v_tree, *k_cache, *v_cache;
     const int32_t *block_table, *ctx_lens;
     const uint32_t *mask;
-    uint16_t *out;
+    float *out;
     const int4 *items;
     const int32_t *rg_base;
     int32_t *meta;
@@ -387,12 +387,12 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) att_mma_kernel(AttArgs a)
             for (int dn = 0; dn < DTILES; ++dn) {
                 const int col = dn * 8 + (lane & 3) * 2;
                 if (gr0 < rowsPerHead) {
-                    uint16_t *dst = a.out + (((int64_t)r * a.P + i0) * a.Hq + g * a.G + gr0 % a.G) * D + col;
-                    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[dn][0] * inv0, o[dn][1] * inv0);
+                    float *dst = a.out + (((int64_t)r * a.P + i0) * a.Hq + g * a.G + gr0 % a.G) * D + col;
+                    *reinterpret_cast<float2 *>(dst) = make_float2(o[dn][0] * inv0, o[dn][1] * inv0);
                 }
                 if (gr1 < rowsPerHead) {
-                    uint16_t *dst = a.out + (((int64_t)r * a.P + i1) * a.Hq + g * a.G + gr1 % a.G) * D + col;
-                    *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[dn][2] * inv1, o[dn][3] * inv1);
+                    float *dst = a.out + (((int64_t)r * a.P + i1) * a.Hq + g * a.G + gr1 % a.G) * D + col;
+                    *reinterpret_cast<float2 *>(dst) = make_float2(o[dn][2] * inv1, o[dn][3] * inv1);
                 }
             }
             __syncthreads();  // smem reuse by the next item
@@ -454,8 +454,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) att_mma_kernel(AttArgs a)
                 x1 += v.y * f;
             }
             const int i = gr / a.G, hl = gr % a.G;
-            uint16_t *dst = a.out + (((int64_t)r * a.P + i) * a.Hq + g * a.G + hl) * D + col;
-            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(x0, x1);
+            float *dst = a.out + (((int64_t)r * a.P + i) * a.Hq + g * a.G + hl) * D + col;
+            *reinterpret_cast<float2 *>(dst) = make_float2(x0, x1);
         }
         if (tid == 0)
             a.rg_cnt[rg_slot] = 0u;
@@ -465,19 +465,29 @@ __global__ void __launch_bounds__(ATT_THREADS, 1) att_mma_kernel(AttArgs a)
 
 }  // namespace
 
+cudaError_t launch_att_plan(const ddt_ctx *c, const int32_t *ctx_lens, int R, int RG, int max_ctx,
+                            cudaStream_t s)
+{
+    att_plan_kernel<<<1, 256, 4 * R * sizeof(int), s>>>(ctx_lens, R, c->cfg.Hkv, RG, max_ctx,
+                                                        c->att_items, c->att_rg_base, c->att_meta,
+                                                        c->status);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                              const uint16_t *v_tree, const uint16_t *k_cache,
                              const uint16_t *v_cache, const int32_t *block_table,
-                             const int32_t *ctx_lens, const uint32_t *mask, int R, uint16_t *out,
+                             const int32_t *ctx_lens, const uint32_t *mask, int R, float *out,
                              cudaStream_t s)
 {
     const ddt_config &cfg = c->cfg;
+    if (c->att_use_tc)
+        return launch_attention_tc(c, q, k_tree, v_tree, k_cache, v_cache, block_table, ctx_lens,
+                                   mask, R, out, s);
     const int P = cfg.B + 1, G = cfg.Hq / cfg.Hkv;
     const int max_ctx = cfg.max_pages_per_req * cfg.page_size;
-    att_plan_kernel<<<1, 256, 4 * R * sizeof(int), s>>>(ctx_lens, R, cfg.Hkv, c->att_rowgroups,
-                                                        max_ctx, c->att_items, c->att_rg_base,
-                                                        c->att_meta, c->status);
-    cudaError_t e = cudaGetLastError();
+    const int RG = (P * G + ATT_ROWS - 1) / ATT_ROWS;
+    cudaError_t e = launch_att_plan(c, ctx_lens, R, RG, max_ctx, s);
     if (e != cudaSuccess)
         return e;
     AttArgs a;
@@ -505,7 +515,7 @@ cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t
     a.W = (P + 31) / 32;
     a.page = cfg.page_size;
     a.max_pages = cfg.max_pages_per_req;
-    a.RG = c->att_rowgroups;
+    a.RG = RG;
     a.num_pages = cfg.num_pages;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)cfg.d);
     if (cfg.d == 128) {

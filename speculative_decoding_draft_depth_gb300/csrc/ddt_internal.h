@@ -57,6 +57,7 @@ struct ddt_ctx {
     float *att_part_o;       // [max_items, ATT_ROWS, d]
     float2 *att_part_ml;     // [max_items, ATT_ROWS]
     int att_grid;            // persistent CTAs
+    bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };
 
 // launchers (return the cudaGetLastError of the launch)
@@ -79,8 +80,19 @@ cudaError_t launch_walk_compact(const ddt_ctx *c, const int32_t *argmax, bool ar
 cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                              const uint16_t *v_tree, const uint16_t *k_cache,
                              const uint16_t *v_cache, const int32_t *block_table,
-                             const int32_t *ctx_lens, const uint32_t *mask, int R, uint16_t *out,
+                             const int32_t *ctx_lens, const uint32_t *mask, int R, float *out,
                              cudaStream_t s);
+
+// a4 on tcgen05 (attention_tc.cu) and the shared work-list plan
+bool attention_tc_supported(const ddt_config &cfg);
+void attention_tc_rows(const ddt_config &cfg, int *n_main, int *tail_rows, int *rowgroups);
+cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
+                                const uint16_t *v_tree, const uint16_t *k_cache,
+                                const uint16_t *v_cache, const int32_t *block_table,
+                                const int32_t *ctx_lens, const uint32_t *mask, int R,
+                                float *out, cudaStream_t s);
+cudaError_t launch_att_plan(const ddt_ctx *c, const int32_t *ctx_lens, int R, int RG, int max_ctx,
+                            cudaStream_t s);
 
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,

@@ -218,7 +218,7 @@ class Context:
             depths=torch.empty((R, P), **i32),
             n_nodes=torch.empty((R,), **i32),
             mask=torch.empty((R, P, W), **i32),
-            attn_out=torch.empty((R, P, c.Hq, c.d), dtype=torch.bfloat16, device=device),
+            attn_out=torch.empty((R, P, c.Hq, c.d), dtype=torch.float32, device=device),
             target_argmax=torch.empty((R, P), **i32),
             acc_len=torch.empty((R,), **i32),
             acc_nodes=torch.empty((R, c.L), **i32),
