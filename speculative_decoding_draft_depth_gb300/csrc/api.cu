@@ -76,6 +76,8 @@ Layout layout_for(const ddt_config &c)
                            ? (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK)
                            : 1;
     L.max_items = c.R_max * c.Hkv * L.rowgroups * ns_max;
+    if (c.d == 128 && L.max_items < 512)  // room for splitting a small batch across the SMs
+        L.max_items = 512;
     const size_t rows_d = (size_t)c.R_max * c.L, rows_t = (size_t)c.R_max * P;
     const size_t rg = (size_t)c.R_max * c.Hkv * L.rowgroups;
     size_t off = 0;
