@@ -9,10 +9,10 @@
 // the accepted path's KV).
 //
 // a5 is HBM-bound: one CTA per (chunk, row) of the [R, P, V] target logits,
-// 8 x 16-byte vectors per thread; the per-vector max is a packed bf16x2
-// max that propagates NaN, so only vectors that can move the running best
-// (or hold a NaN) are looked at element by element. Per-chunk (max, first
-// index) pairs are reduced per row by the walk kernel (or the finish kernel).
+// 8 x 16-byte vectors per thread; the chunk's max comes from packed bf16x2
+// maxima and warp reductions, and only the threads holding it look at single
+// elements. Per-chunk (max, first index) pairs are reduced per row by the
+// walk kernel (or the finish kernel).
 #include <stdint.h>
 
 #include "ddt_device.cuh"
@@ -30,15 +30,6 @@ DDT_DEVINL uint32_t bmax2_nan(uint32_t a, uint32_t b)
     return d;
 }
 
-// take (x, i) if it beats (best, bi): larger value, or equal value with no index yet
-DDT_DEVINL void amax_take(float x, int i, float &best, int &bi)
-{
-    if (x > best || (x == best && bi == IDX_NONE)) {
-        best = x;
-        bi = i;
-    }
-}
-
 // combine two partial (max, first index) results
 DDT_DEVINL void amax_merge(float &best, int &bi, float ob, int oi)
 {
@@ -50,14 +41,38 @@ DDT_DEVINL void amax_merge(float &best, int &bi, float ob, int oi)
     }
 }
 
+DDT_DEVINL uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// order-preserving map of a float to uint32 (-0 == +0; NaN must be excluded first)
+DDT_DEVINL uint32_t fkey(float x)
+{
+    const uint32_t b = __float_as_uint(x + 0.0f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+DDT_DEVINL float fkey_inv(uint32_t k)
+{
+    return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
+}
+
+// One CTA per (chunk, row). The chunk's max is found without looking at single
+// elements (packed bf16x2 max per thread, one warp reduction, one CTA step);
+// only the threads that hold it scan their own elements, in index order, for
+// its first occurrence. NaN elements are skipped (and flagged).
 template <bool BF16, bool ALIGNED>
-__global__ void __launch_bounds__(AMAX_THREADS)
+__global__ void __launch_bounds__(AMAX_THREADS, 5)
 argmax_chunk_kernel(const void *__restrict__ t, int V, int nch, float *__restrict__ am_val,
                     int32_t *__restrict__ am_idx, int32_t *__restrict__ status)
 {
     constexpr int VE = BF16 ? 8 : 4;
     constexpr int CH = AMAX_THREADS * NV * VE;
+    constexpr uint32_t FILL = BF16 ? 0xFF80FF80u : 0xFF800000u;  // -inf
     const int chunk = blockIdx.x, row = blockIdx.y, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     const int c0 = chunk * CH;
     const int cn = min(CH, V - c0);
     const char *rowp = (const char *)t + (int64_t)row * V * (BF16 ? 2 : 4);
@@ -66,73 +81,91 @@ argmax_chunk_kernel(const void *__restrict__ t, int V, int nch, float *__restric
 #pragma unroll
     for (int j = 0; j < NV; ++j) {
         const int e0 = (j * AMAX_THREADS + tid) * VE;
-        if (ALIGNED && e0 < cn)
+        if (ALIGNED && e0 < cn) {
             raw[j] = ldg_stream(rowp + (int64_t)(c0 + e0) * (BF16 ? 2 : 4));
-        else
-            raw[j] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+            uint32_t w[4] = {FILL, FILL, FILL, FILL};
+            if (!ALIGNED)
+                for (int e = 0; e < VE; ++e)
+                    if (e0 + e < cn) {
+                        if (BF16) {
+                            const uint32_t h = __ldg((const unsigned short *)rowp + c0 + e0 + e);
+                            w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0xFFFFu) | (h << 16))
+                                                : ((w[e >> 1] & 0xFFFF0000u) | h);
+                        } else {
+                            w[e] = __float_as_uint(__ldg((const float *)rowp + c0 + e0 + e));
+                        }
+                    }
+            raw[j] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 
-    float best = DDT_NEG_INF;
-    int bi = IDX_NONE;
-    bool nan = false;
+    // ---- this thread's max (NaN ignored) and whether it holds a NaN
+    float m;
+    bool nan;
+    if (BF16) {
+        uint32_t mx = FILL, mn = FILL;
 #pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int e0 = (j * AMAX_THREADS + tid) * VE;
-        if (e0 >= cn)
-            continue;
-        if (ALIGNED && BF16) {
-            const uint32_t m2 = bmax2_nan(bmax2_nan(raw[j].x, raw[j].y), bmax2_nan(raw[j].z, raw[j].w));
-            const uint32_t m1 = bmax2_nan(m2, __byte_perm(m2, 0, 0x1032));
-            const float vm = bf16lo(m1);
-            if (vm > best || (vm == best && bi == IDX_NONE) || vm != vm) {
-                const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+        for (int j = 0; j < NV; ++j) {
+            mx = bmax2(mx, bmax2(bmax2(raw[j].x, raw[j].y), bmax2(raw[j].z, raw[j].w)));
+            mn = bmax2_nan(mn, bmax2_nan(bmax2_nan(raw[j].x, raw[j].y), bmax2_nan(raw[j].z, raw[j].w)));
+        }
+        m = fmaxf(bf16lo(mx), bf16hi(mx));
+        nan = (bf16lo(mn) != bf16lo(mn)) || (bf16hi(mn) != bf16hi(mn));
+    } else {
+        m = DDT_NEG_INF;
+        nan = false;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float x = (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
-                    if (x != x)
-                        nan = true;
-                    else
-                        amax_take(x, c0 + e0 + e, best, bi);
-                }
-            }
-        } else {
-            for (int e = 0; e < VE && e0 + e < cn; ++e) {
-                float x;
-                if (ALIGNED) {
-                    const uint32_t w = (e == 0) ? raw[j].x : (e == 1) ? raw[j].y : (e == 2) ? raw[j].z : raw[j].w;
-                    x = __uint_as_float(w);
-                } else if (BF16) {
-                    x = bf16_to_f32(__ldg((const unsigned short *)rowp + c0 + e0 + e));
-                } else {
-                    x = __ldg((const float *)rowp + c0 + e0 + e);
-                }
-                if (x != x)
-                    nan = true;
-                else
-                    amax_take(x, c0 + e0 + e, best, bi);
+        for (int j = 0; j < NV; ++j) {
+            const float x0 = __uint_as_float(raw[j].x), x1 = __uint_as_float(raw[j].y);
+            const float x2 = __uint_as_float(raw[j].z), x3 = __uint_as_float(raw[j].w);
+            m = fmaxf(m, fmaxf(fmaxf(x0, x1), fmaxf(x2, x3)));
+            nan |= (x0 != x0) | (x1 != x1) | (x2 != x2) | (x3 != x3);
+        }
+    }
+    if (m != m)
+        m = DDT_NEG_INF;  // every element NaN
+
+    // ---- the chunk's max
+    __shared__ uint32_t s_k[AMAX_THREADS / 32];
+    __shared__ int s_i[AMAX_THREADS / 32];
+    const uint32_t key = fkey(m);
+    const uint32_t wk = __reduce_max_sync(0xFFFFFFFFu, key);
+    if (lane == 0)
+        s_k[warp] = wk;
+    const int any_nan = __syncthreads_or(nan ? 1 : 0);
+    uint32_t bk = s_k[0];
+#pragma unroll
+    for (int w = 1; w < AMAX_THREADS / 32; ++w)
+        bk = max(bk, s_k[w]);
+    const float M = fkey_inv(bk);
+
+    // ---- its first occurrence: only threads whose max equals it look
+    int fi = IDX_NONE;
+    if (key == bk) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            const int e0 = (j * AMAX_THREADS + tid) * VE;
+            const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                const float x = BF16 ? ((e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]))
+                                     : __uint_as_float(w[e]);
+                if (fi == IDX_NONE && x == M && e0 + e < cn)
+                    fi = c0 + e0 + e;
             }
         }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-        amax_merge(best, bi, ob, oi);
-    }
-    __shared__ float s_b[AMAX_THREADS / 32];
-    __shared__ int s_i[AMAX_THREADS / 32];
-    const int lane = tid & 31, warp = tid >> 5;
-    if (lane == 0) {
-        s_b[warp] = best;
-        s_i[warp] = bi;
-    }
-    const int any_nan = __syncthreads_or(nan ? 1 : 0);
+    fi = __reduce_min_sync(0xFFFFFFFFu, fi);
+    if (lane == 0)
+        s_i[warp] = fi;
+    __syncthreads();
     if (tid == 0) {
-        float b = s_b[0];
         int i = s_i[0];
+#pragma unroll
         for (int w = 1; w < AMAX_THREADS / 32; ++w)
-            amax_merge(b, i, s_b[w], s_i[w]);
-        am_val[(int64_t)row * nch + chunk] = b;
+            i = min(i, s_i[w]);
+        am_val[(int64_t)row * nch + chunk] = M;
         am_idx[(int64_t)row * nch + chunk] = i;
         if (any_nan)
             set_status(status, DDT_DEV_NAN_LOGITS);

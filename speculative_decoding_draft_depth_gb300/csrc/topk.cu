@@ -52,6 +52,25 @@ template <> struct Elem<float> {
     }
 };
 
+// max of one vector's elements (NaN ignored unless all are NaN)
+DDT_DEVINL uint32_t bf16x2_max(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+template <typename T>
+DDT_DEVINL float vec_max(const uint4 &v)
+{
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t w = bf16x2_max(bf16x2_max(v.x, v.y), bf16x2_max(v.z, v.w));
+        return fmaxf(bf16lo(w), bf16hi(w));
+    } else {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+}
+
 // scalar gather of one vector's worth of elements (unaligned rows / tails)
 template <typename T>
 DDT_DEVINL uint4 load_scalar(const T *p, int valid)
@@ -121,7 +140,7 @@ DDT_DEVINL int block_sum(int v, int *s_acc)
 }
 
 template <typename T, bool ALIGNED>
-__global__ void __launch_bounds__(TOPK_THREADS)
+__global__ void __launch_bounds__(TOPK_THREADS, 4)
 topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restrict__ part_val,
                   int32_t *__restrict__ part_idx, float2 *__restrict__ part_ms,
                   unsigned *__restrict__ cnt, float *__restrict__ top_lp,
@@ -165,9 +184,7 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     float m = DDT_NEG_INF;
 #pragma unroll
     for (int j = 0; j < NV; ++j)
-#pragma unroll
-        for (int e = 0; e < VE; ++e)
-            m = fmaxf(m, Elem<T>::get(raw[j], e));
+        m = fmaxf(m, vec_max<T>(raw[j]));
     float s = 0.f;
     if (m != DDT_NEG_INF) {
 #pragma unroll
@@ -178,27 +195,28 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     }
     const float lane_max = m;
 
-    // ---- per-warp quota threshold: ceil(K/8)-th largest lane max (bitonic sort, descending)
-    float v = lane_max;
-#pragma unroll
-    for (int k = 2; k <= 32; k <<= 1)
-#pragma unroll
-        for (int jj = k >> 1; jj > 0; jj >>= 1) {
-            const float o = __shfl_xor_sync(0xFFFFFFFFu, v, jj);
-            const bool want_max = ((lane & k) == 0) == ((lane & jj) == 0);
-            v = want_max ? fmaxf(v, o) : fminf(v, o);
-        }
+    // ---- per-warp quota threshold: the ceil(K/8)-th largest lane max, found by
+    // removing the warp's largest lane max (one lane at a time) quota - 1 times
     const int quota = (K + (TOPK_THREADS / 32) - 1) / (TOPK_THREADS / 32);
-    const float warp_t = __shfl_sync(0xFFFFFFFFu, v, quota - 1);
-
-    // ---- CTA (max, sum)
-    float mm = m, ss = s;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float mo = __shfl_xor_sync(0xFFFFFFFFu, mm, off);
-        const float so = __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-        ms_combine(mm, ss, mo, so);
+    uint32_t key = okey(lane_max == lane_max ? lane_max : DDT_NEG_INF);
+    uint32_t top = __reduce_max_sync(0xFFFFFFFFu, key);
+    for (int q = 1; q < quota; ++q) {
+        const uint32_t holders = __ballot_sync(0xFFFFFFFFu, key == top);
+        if (lane == __ffs(holders) - 1)
+            key = 0u;
+        top = __reduce_max_sync(0xFFFFFFFFu, key);
     }
+    const float warp_t = (top & 0x80000000u) ? __uint_as_float(top & 0x7FFFFFFFu)
+                                             : __uint_as_float(~top);
+
+    // ---- CTA (max, sum): warp max by one reduction, sums rescaled to it
+    const uint32_t wkey = __reduce_max_sync(0xFFFFFFFFu, okey(m == m ? m : DDT_NEG_INF));
+    const float mm = (wkey & 0x80000000u) ? __uint_as_float(wkey & 0x7FFFFFFFu)
+                                          : __uint_as_float(~wkey);
+    float ss = (m != DDT_NEG_INF && m == m) ? s * ex2((m - mm) * DDT_LOG2E) : (s != s ? s : 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
     if (lane == 0) {
         s_wm[warp] = mm;
         s_ws[warp] = ss;
@@ -217,6 +235,8 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
             const int e0 = (j * TOPK_THREADS + tid) * VE;
+            if (!(vec_max<T>(raw[j]) >= T0))
+                continue;
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
                 const float x = Elem<T>::get(raw[j], e);
@@ -299,13 +319,19 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         s_logz = (double)cm + log((double)cs);
     }
     __syncthreads();
-    for (int i = tid; i < n; i += TOPK_THREADS) {
-        const float vi = s_val[i];
-        const int ii = s_idx[i];
+    // four threads per survivor, each counting a quarter of the survivors that beat it
+    for (int i0 = 0; i0 < n; i0 += TOPK_THREADS / 4) {
+        const int i = i0 + (tid >> 2);
+        const bool have = i < n;
+        const float vi = have ? s_val[i] : 0.f;
+        const int ii = have ? s_idx[i] : 0;
         int rank = 0;
-        for (int jx = 0; jx < n; ++jx)
-            rank += beats(s_val[jx], s_idx[jx], vi, ii) ? 1 : 0;
-        if (rank < K) {
+        if (have)
+            for (int jx = tid & 3; jx < n; jx += 4)
+                rank += beats(s_val[jx], s_idx[jx], vi, ii) ? 1 : 0;
+        rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
+        rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
+        if (have && (tid & 3) == 0 && rank < K) {
             if (single) {
                 top_lp[(int64_t)row * K + rank] = (float)((double)vi - s_logz);
                 top_ids[(int64_t)row * K + rank] = ii;
