@@ -1052,7 +1052,11 @@ __global__ void att_tc_plan_kernel(const int32_t *__restrict__ ctx_lens, int R, 
         s_ctx[r] = c;
         mine += (long long)((c + TILE - 1) / TILE + 1) * per_req;
     }
-    atomicAdd((unsigned long long *)&s_total, (unsigned long long)mine);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mine += __shfl_xor_sync(0xFFFFFFFFu, mine, o);
+    if ((tid & 31) == 0 && mine != 0)
+        atomicAdd((unsigned long long *)&s_total, (unsigned long long)mine);
     __syncthreads();
     const long long T = s_total;
     const long long npairs = (long long)R * per_req;
@@ -1080,40 +1084,66 @@ __global__ void att_tc_plan_kernel(const int32_t *__restrict__ ctx_lens, int R, 
     __syncthreads();
     const int n_items = block_excl_scan(s_off, R, s_wsum, &s_count);
     // sizes -> histogram (largest first)
-    for (int i = tid; i < n_items; i += nth) {
-        int lo = 0, hi = R - 1;  // last r with s_off[r] <= i
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_off[mid] <= i)
-                lo = mid;
-            else
-                hi = mid - 1;
+    for (int i0 = 0; i0 < n_items; i0 += nth) {
+        const int i = i0 + tid;
+        int bin = -1;
+        if (i < n_items) {
+            int lo = 0, hi = R - 1;  // last r with s_off[r] <= i
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= i)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            const int r = lo, rem = i - s_off[r], s = rem / per_req;
+            const int ctx = s_ctx[r], len = s_len[r] * TILE;
+            const int t0 = min(ctx, s * len), t1 = min(ctx, (s + 1) * len);
+            const int size = (t1 - t0 + TILE - 1) / TILE + (s == s_ns[r] - 1 ? 1 : 0);
+            bin = PLAN_BINS - 1 - min(size, PLAN_BINS - 1);
         }
-        const int r = lo, rem = i - s_off[r], s = rem / per_req;
-        const int ctx = s_ctx[r], len = s_len[r] * TILE;
-        const int t0 = min(ctx, s * len), t1 = min(ctx, (s + 1) * len);
-        const int size = (t1 - t0 + TILE - 1) / TILE + (s == s_ns[r] - 1 ? 1 : 0);
-        atomicAdd(&s_hist[PLAN_BINS - 1 - min(size, PLAN_BINS - 1)], 1);
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, bin);
+        if (bin >= 0 && (tid & 31) == __ffs(same) - 1)
+            atomicAdd(&s_hist[bin], __popc(same));
     }
     __syncthreads();
     block_excl_scan(s_hist, PLAN_BINS, s_wsum, &s_count);
-    for (int i = tid; i < n_items; i += nth) {
-        int lo = 0, hi = R - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_off[mid] <= i)
-                lo = mid;
-            else
-                hi = mid - 1;
+    for (int i0 = 0; i0 < n_items; i0 += nth) {
+        const int i = i0 + tid;
+        int bin = -1, r = 0, s = 0, g = 0, rg = 0, ns = 0, t0 = 0, t1 = 0;
+        if (i < n_items) {
+            int lo = 0, hi = R - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= i)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            r = lo;
+            const int rem = i - s_off[r];
+            s = rem / per_req;
+            g = (rem / RG) % Hkv;
+            rg = rem % RG;
+            const int ctx = s_ctx[r], len = s_len[r] * TILE;
+            ns = s_ns[r];
+            t0 = min(ctx, s * len);
+            t1 = min(ctx, (s + 1) * len);
+            const int size = (t1 - t0 + TILE - 1) / TILE + (s == ns - 1 ? 1 : 0);
+            bin = PLAN_BINS - 1 - min(size, PLAN_BINS - 1);
         }
-        const int r = lo, rem = i - s_off[r], s = rem / per_req, g = (rem / RG) % Hkv, rg = rem % RG;
-        const int ctx = s_ctx[r], len = s_len[r] * TILE, ns = s_ns[r];
-        const int t0 = min(ctx, s * len), t1 = min(ctx, (s + 1) * len);
-        const int size = (t1 - t0 + TILE - 1) / TILE + (s == ns - 1 ? 1 : 0);
-        const int at = atomicAdd(&s_hist[PLAN_BINS - 1 - min(size, PLAN_BINS - 1)], 1);
-        items[at] = make_int4(r | (ns << 12), g | (rg << 8) | (s << 16), t0, t1);
-        if (s == 0)
-            rg_base[((int64_t)r * Hkv + g) * RG + rg] = s_off[r] + g * RG + rg;
+        const unsigned same = __match_any_sync(0xFFFFFFFFu, bin);
+        const int leader = __ffs(same) - 1;
+        int base = 0;
+        if (bin >= 0 && (tid & 31) == leader)
+            base = atomicAdd(&s_hist[bin], __popc(same));
+        base = __shfl_sync(0xFFFFFFFFu, base, leader);
+        if (bin >= 0) {
+            const int at = base + __popc(same & ((1u << (tid & 31)) - 1u));
+            items[at] = make_int4(r | (ns << 12), g | (rg << 8) | (s << 16), t0, t1);
+            if (s == 0)
+                rg_base[((int64_t)r * Hkv + g) * RG + rg] = s_off[r] + g * RG + rg;
+        }
     }
     if (tid == 0) {
         meta[0] = n_items;

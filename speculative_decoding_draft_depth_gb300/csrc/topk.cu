@@ -31,6 +31,39 @@ namespace {
 
 constexpr int NV = TOPK_VEC_PER_THREAD;
 constexpr int SELECT_MAX = 512;  // above this many survivors, use the exact search
+constexpr int VEC_CAP = 512;     // staged candidate vectors (more: the exact search)
+
+// packed fp32 pairs (two lanes of one 64-bit register)
+DDT_DEVINL uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+DDT_DEVINL void f2unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+DDT_DEVINL uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+DDT_DEVINL uint64_t f2add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// 2^(x * log2 e - m * log2 e) for the two bf16 values of w (c2 = {log2 e, log2 e},
+// b2 = {-m log2 e, -m log2 e}), as a packed pair
+DDT_DEVINL uint64_t exp_pair(uint32_t w, uint64_t c2, uint64_t b2)
+{
+    float t0, t1;
+    f2unpack(f2fma(f2pack(bf16lo(w), bf16hi(w)), c2, b2), t0, t1);
+    return f2pack(ex2(t0), ex2(t1));
+}
 
 template <typename T> struct Elem;
 template <> struct Elem<uint16_t> {
@@ -157,7 +190,9 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     __shared__ float s_val[TOPK_CAND_CAP];
     __shared__ int s_idx[TOPK_CAND_CAP];
     __shared__ float s_wm[TOPK_THREADS / 32], s_ws[TOPK_THREADS / 32], s_wt[TOPK_THREADS / 32];
-    __shared__ int s_count, s_acc, s_last;
+    __shared__ uint4 s_vec[VEC_CAP];
+    __shared__ int s_vbase[VEC_CAP];
+    __shared__ int s_count, s_acc, s_last, s_nvec;
     __shared__ double s_logz;
 
     // ---- load this thread's vectors (coalesced: consecutive threads, consecutive 16 B)
@@ -178,6 +213,7 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     if (tid == 0) {
         s_count = 0;
         s_acc = 0;
+        s_nvec = 0;
     }
 
     // ---- pass 1: thread max; pass 2: sum of exp relative to it
@@ -187,11 +223,28 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         m = fmaxf(m, vec_max<T>(raw[j]));
     float s = 0.f;
     if (m != DDT_NEG_INF) {
+        const float nb = -m * DDT_LOG2E;
+        if constexpr (sizeof(T) == 2) {
+            const uint64_t c2 = f2pack(DDT_LOG2E, DDT_LOG2E), b2 = f2pack(nb, nb);
+            uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int j = 0; j < NV; ++j)
+            for (int j = 0; j < NV; ++j) {
+                acc0 = f2add(acc0, exp_pair(raw[j].x, c2, b2));
+                acc1 = f2add(acc1, exp_pair(raw[j].y, c2, b2));
+                acc0 = f2add(acc0, exp_pair(raw[j].z, c2, b2));
+                acc1 = f2add(acc1, exp_pair(raw[j].w, c2, b2));
+            }
+            float a0, a1, a2, a3;
+            f2unpack(acc0, a0, a1);
+            f2unpack(acc1, a2, a3);
+            s = (a0 + a1) + (a2 + a3);
+        } else {
 #pragma unroll
-            for (int e = 0; e < VE; ++e)
-                s += ex2((Elem<T>::get(raw[j], e) - m) * DDT_LOG2E);
+            for (int j = 0; j < NV; ++j)
+#pragma unroll
+                for (int e = 0; e < VE; ++e)
+                    s += ex2(fmaf(Elem<T>::get(raw[j], e), DDT_LOG2E, nb));
+        }
     }
     const float lane_max = m;
 
@@ -223,23 +276,41 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         s_wt[warp] = warp_t;
     }
     __syncthreads();
-    float cm = s_wm[0], cs = s_ws[0], T0 = s_wt[0];
+    float T0 = s_wt[0];
 #pragma unroll
-    for (int w = 1; w < TOPK_THREADS / 32; ++w) {
-        ms_combine(cm, cs, s_wm[w], s_ws[w]);
+    for (int w = 1; w < TOPK_THREADS / 32; ++w)
         T0 = fminf(T0, s_wt[w]);
+    float cm = DDT_NEG_INF, cs = 0.f;  // the chunk's (max, sum): thread 0 only
+    if (tid == 0) {
+        cm = s_wm[0];
+        cs = s_ws[0];
+        for (int w = 1; w < TOPK_THREADS / 32; ++w)
+            ms_combine(cm, cs, s_wm[w], s_ws[w]);
     }
 
-    // ---- survivors of the filter
+    // ---- survivors of the filter: vectors holding a value >= T0 are staged in
+    // shared memory, then expanded element by element by the whole CTA
     if (lane_max >= T0) {
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            const int e0 = (j * TOPK_THREADS + tid) * VE;
-            if (!(vec_max<T>(raw[j]) >= T0))
-                continue;
+            if (vec_max<T>(raw[j]) >= T0) {
+                const int pos = atomicAdd(&s_nvec, 1);
+                if (pos < VEC_CAP) {
+                    s_vec[pos] = raw[j];
+                    s_vbase[pos] = (j * TOPK_THREADS + tid) * VE;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    const int nvec = s_nvec;
+    if (nvec <= VEC_CAP) {
+        for (int v = tid; v < nvec; v += TOPK_THREADS) {
+            const uint4 r = s_vec[v];
+            const int e0 = s_vbase[v];
 #pragma unroll
             for (int e = 0; e < VE; ++e) {
-                const float x = Elem<T>::get(raw[j], e);
+                const float x = Elem<T>::get(r, e);
                 if (x >= T0 && e0 + e < cn) {
                     const int pos = atomicAdd(&s_count, 1);
                     if (pos < TOPK_CAND_CAP) {
@@ -251,7 +322,7 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         }
     }
     __syncthreads();
-    int n = s_count;
+    int n = (nvec <= VEC_CAP) ? s_count : SELECT_MAX + 1;
 
     if (n > SELECT_MAX) {
         // ---- exact fallback (flat or heavily tied chunks): re-read the chunk
@@ -356,10 +427,11 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         part_ms[(int64_t)row * nch + chunk] = make_float2(cm, cs);
 
     // ---- arrival; the last CTA of the row merges
-    __threadfence();
     __syncthreads();
-    if (tid == 0)
+    if (tid == 0) {
+        __threadfence();
         s_last = (atomicAdd(&cnt[row], 1u) == (unsigned)(nch - 1));
+    }
     __syncthreads();
     if (!s_last)
         return;
@@ -372,20 +444,29 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
         s_val[i] = __ldcg(rv + i);
         s_idx[i] = __ldcg(ri + i);
     }
-    if (tid == 0) {
-        float M = DDT_NEG_INF;
-        for (int c = 0; c < nch; ++c)
-            M = fmaxf(M, __ldcg(&part_ms[(int64_t)row * nch + c].x));
-        float S = 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const float2 ms = __ldcg(&part_ms[(int64_t)row * nch + c]);
-            if (ms.x != DDT_NEG_INF)
-                S += ms.y * ex2((ms.x - M) * DDT_LOG2E);
+    if (warp == 0) {  // the row's (max, sum) from the chunks', one warp
+        float M = DDT_NEG_INF, S = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + lane;
+            float2 ms = make_float2(DDT_NEG_INF, 0.f);
+            if (c < nch)
+                ms = __ldcg(&part_ms[(int64_t)row * nch + c]);
+            float wm = ms.x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+            float t = (ms.x != DDT_NEG_INF) ? ms.y * ex2((ms.x - wm) * DDT_LOG2E) : (ms.y != ms.y ? ms.y : 0.f);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+            ms_combine(M, S, wm, t);
         }
-        if (S != S)
-            set_status(status, DDT_DEV_NAN_LOGITS);
-        s_logz = (double)M + log((double)S);
-        cnt[row] = 0u;  // ready for the next launch
+        if (lane == 0) {
+            if (S != S)
+                set_status(status, DDT_DEV_NAN_LOGITS);
+            s_logz = (double)M + log((double)S);
+            cnt[row] = 0u;  // ready for the next launch
+        }
     }
     __syncthreads();
     for (int i = tid; i < total; i += TOPK_THREADS) {
