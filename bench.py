@@ -317,7 +317,7 @@ def main():
                          "peak": peak, "frac": round(round_gbs / peak, 4), "peak_kind": peak_kind},
            "stages": stages,
            "roofline": roofline,
-           "gpu_launches": 6 * args.steps,
+           "gpu_launches": launches_per_round(cfg) * args.steps,
            "clocks": clk,
            "acceptance": {"mean_acc_len": float(np.mean(acc_len))}}
 
@@ -330,6 +330,13 @@ def main():
         print(json.dumps(out))
     if dist:
         dist.destroy_process_group()
+
+
+def launches_per_round(cfg):
+    """Kernels ddt_round launches: top-K chunks (+ row merge when a row spans
+    several chunks), tree, attention plan + attention, argmax chunks, walk."""
+    chunk = 256 * 8 * (8 if cfg.logit_dtype == "bf16" else 4)
+    return 6 + (1 if cfg.V > chunk else 0)
 
 
 def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):

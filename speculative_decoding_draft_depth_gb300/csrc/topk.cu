@@ -19,9 +19,10 @@
 //    each survivor, how many survivors beat it. If the filter lets through
 //    too many (flat or heavily tied rows), an exact bitwise search over the
 //    ordered 32-bit keys and the chunk-local index picks exactly K.
-//  * The CTA that finishes a row last (atomic arrival counter) merges the
-//    per-chunk sorted lists by binary search and the per-chunk (max, sum)
-//    into logZ (final combination in fp64), then writes lp = z - logZ.
+//  * A merge kernel (one warp per row) combines the per-chunk sorted lists
+//    (bitonic merges for K <= 32, binary-search ranks above) and the
+//    per-chunk (max, sum) pairs into logZ (final step in fp64), then writes
+//    lp = z - logZ. A row that fits one chunk is finished by its chunk CTA.
 #include <stdint.h>
 
 #include "ddt_device.cuh"
@@ -32,6 +33,7 @@ namespace {
 constexpr int NV = TOPK_VEC_PER_THREAD;
 constexpr int SELECT_MAX = 512;  // above this many survivors, use the exact search
 constexpr int VEC_CAP = 512;     // staged candidate vectors (more: the exact search)
+constexpr int IDX_PAD = 0x7FFFFFFF;  // id of a padding entry in a chunk list
 
 // packed fp32 pairs (two lanes of one 64-bit register)
 DDT_DEVINL uint64_t f2pack(float lo, float hi)
@@ -147,6 +149,32 @@ DDT_DEVINL uint32_t okey(float x)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// candidate key: ordered value in the high word, complemented token id in the
+// low word (a lower id wins a tie); a larger key beats a smaller one
+DDT_DEVINL uint64_t make_key(float v, int idx)
+{
+    return ((uint64_t)okey(v) << 32) | (uint32_t)~(uint32_t)idx;
+}
+DDT_DEVINL float key_val(uint64_t k)
+{
+    const uint32_t h = (uint32_t)(k >> 32);
+    return (h & 0x80000000u) ? __uint_as_float(h & 0x7FFFFFFFu) : __uint_as_float(~h);
+}
+DDT_DEVINL int key_idx(uint64_t k) { return (int)~(uint32_t)k; }
+
+// exclusive prefix sum over the lanes of a warp
+DDT_DEVINL int warp_excl_scan(int v, int lane)
+{
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    return x - v;
+}
+
 // one element as fp32 (the exact fallback's re-read)
 template <typename T>
 DDT_DEVINL float load_one(const T *p, int i)
@@ -176,7 +204,7 @@ template <typename T, bool ALIGNED>
 __global__ void __launch_bounds__(TOPK_THREADS, 4)
 topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restrict__ part_val,
                   int32_t *__restrict__ part_idx, float2 *__restrict__ part_ms,
-                  unsigned *__restrict__ cnt, float *__restrict__ top_lp,
+                  float *__restrict__ top_lp,
                   int32_t *__restrict__ top_ids, int32_t *__restrict__ status)
 {
     constexpr int VE = Elem<T>::VE;
@@ -187,12 +215,11 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     const int c0 = chunk * CH;
     const int cn = min(CH, V - c0);
 
-    __shared__ float s_val[TOPK_CAND_CAP];
-    __shared__ int s_idx[TOPK_CAND_CAP];
+    __shared__ uint64_t s_key[TOPK_CAND_CAP];
     __shared__ float s_wm[TOPK_THREADS / 32], s_ws[TOPK_THREADS / 32], s_wt[TOPK_THREADS / 32];
     __shared__ uint4 s_vec[VEC_CAP];
     __shared__ int s_vbase[VEC_CAP];
-    __shared__ int s_count, s_acc, s_last, s_nvec;
+    __shared__ int s_count, s_acc, s_nvec;
     __shared__ double s_logz;
 
     // ---- load this thread's vectors (coalesced: consecutive threads, consecutive 16 B)
@@ -289,15 +316,31 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     }
 
     // ---- survivors of the filter: vectors holding a value >= T0 are staged in
-    // shared memory, then expanded element by element by the whole CTA
-    if (lane_max >= T0) {
+    // shared memory (one atomic per warp), then expanded element by element by
+    // the whole CTA; survivors are kept as 64-bit keys (value order, then
+    // lower token id), so that "beats" is one unsigned compare
+    {
+        int cnt = 0;
+        if (lane_max >= T0) {
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if (vec_max<T>(raw[j]) >= T0) {
-                const int pos = atomicAdd(&s_nvec, 1);
-                if (pos < VEC_CAP) {
-                    s_vec[pos] = raw[j];
-                    s_vbase[pos] = (j * TOPK_THREADS + tid) * VE;
+            for (int j = 0; j < NV; ++j)
+                cnt += (vec_max<T>(raw[j]) >= T0) ? 1 : 0;
+        }
+        int base = warp_excl_scan(cnt, lane);
+        const int wtot = __shfl_sync(0xFFFFFFFFu, base + cnt, 31);
+        int wbase = 0;
+        if (lane == 31 && wtot > 0)
+            wbase = atomicAdd(&s_nvec, wtot);
+        base += __shfl_sync(0xFFFFFFFFu, wbase, 31);
+        if (cnt > 0) {
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (vec_max<T>(raw[j]) >= T0) {
+                    if (base < VEC_CAP) {
+                        s_vec[base] = raw[j];
+                        s_vbase[base] = (j * TOPK_THREADS + tid) * VE;
+                    }
+                    ++base;
                 }
             }
         }
@@ -305,19 +348,32 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     __syncthreads();
     const int nvec = s_nvec;
     if (nvec <= VEC_CAP) {
-        for (int v = tid; v < nvec; v += TOPK_THREADS) {
-            const uint4 r = s_vec[v];
-            const int e0 = s_vbase[v];
+        for (int v0 = 0; v0 < nvec; v0 += TOPK_THREADS) {
+            const int v = v0 + tid;
+            uint4 r = make_uint4(Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL,
+                                 Elem<T>::NEG_INF_FILL);
+            int e0 = 0;
+            if (v < nvec) {
+                r = s_vec[v];
+                e0 = s_vbase[v];
+            }
+            uint32_t hit = 0;
 #pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                const float x = Elem<T>::get(r, e);
-                if (x >= T0 && e0 + e < cn) {
-                    const int pos = atomicAdd(&s_count, 1);
-                    if (pos < TOPK_CAND_CAP) {
-                        s_val[pos] = x;
-                        s_idx[pos] = c0 + e0 + e;
-                    }
-                }
+            for (int e = 0; e < VE; ++e)
+                hit |= (Elem<T>::get(r, e) >= T0 && e0 + e < cn) ? (1u << e) : 0u;
+            const int cnt = __popc(hit);
+            int base = warp_excl_scan(cnt, lane);
+            const int wtot = __shfl_sync(0xFFFFFFFFu, base + cnt, 31);
+            int wbase = 0;
+            if (lane == 31 && wtot > 0)
+                wbase = atomicAdd(&s_count, wtot);
+            base += __shfl_sync(0xFFFFFFFFu, wbase, 31);
+            while (hit) {
+                const int e = __ffs(hit) - 1;
+                hit &= hit - 1;
+                if (base < TOPK_CAND_CAP)
+                    s_key[base] = make_key(Elem<T>::get(r, e), c0 + e0 + e);
+                ++base;
             }
         }
     }
@@ -371,8 +427,7 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
                 const uint32_t kx = okey(x);
                 if (kx > t || (kx == t && li <= I)) {
                     const int pos = atomicAdd(&s_count, 1);
-                    s_val[pos] = x;
-                    s_idx[pos] = c0 + li;
+                    s_key[pos] = make_key(x, c0 + li);
                 }
             }
         }
@@ -394,15 +449,18 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     for (int i0 = 0; i0 < n; i0 += TOPK_THREADS / 4) {
         const int i = i0 + (tid >> 2);
         const bool have = i < n;
-        const float vi = have ? s_val[i] : 0.f;
-        const int ii = have ? s_idx[i] : 0;
+        const uint64_t ki = have ? s_key[i] : 0ull;
         int rank = 0;
-        if (have)
+        if (have) {
+#pragma unroll 4
             for (int jx = tid & 3; jx < n; jx += 4)
-                rank += beats(s_val[jx], s_idx[jx], vi, ii) ? 1 : 0;
+                rank += (s_key[jx] > ki) ? 1 : 0;
+        }
         rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 1);
         rank += __shfl_xor_sync(0xFFFFFFFFu, rank, 2);
         if (have && (tid & 3) == 0 && rank < K) {
+            const float vi = key_val(ki);
+            const int ii = key_idx(ki);
             if (single) {
                 top_lp[(int64_t)row * K + rank] = (float)((double)vi - s_logz);
                 top_ids[(int64_t)row * K + rank] = ii;
@@ -418,85 +476,128 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
             top_ids[(int64_t)row * K + rank] = -1;
         } else {
             pv[rank] = DDT_NEG_INF;
-            pi[rank] = 0x7FFFFFFF;
+            pi[rank] = IDX_PAD;
         }
     }
-    if (single)
-        return;
-    if (tid == 0)
+    if (!single && tid == 0)
         part_ms[(int64_t)row * nch + chunk] = make_float2(cm, cs);
+}
 
-    // ---- arrival; the last CTA of the row merges
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        s_last = (atomicAdd(&cnt[row], 1u) == (unsigned)(nch - 1));
-    }
-    __syncthreads();
-    if (!s_last)
+// ---------------------------------------------------------------- row merge
+// One warp per row: the row's log-partition from the chunks' (max, sum) pairs
+// (final step in fp64), and its top-K from the chunks' sorted lists.
+// K <= 32: the running top-32 (one key per lane, descending) absorbs each
+// list by a bitonic merge (max against the reversed list, then five
+// half-cleaner steps). K > 32: every entry's rank by binary search in the
+// other lists.
+DDT_DEVINL uint64_t shfl_xor64(uint64_t v, int m)
+{
+    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), m);
+    return ((uint64_t)hi << 32) | lo;
+}
+
+__global__ void __launch_bounds__(256)
+topk_merge_kernel(const float *__restrict__ part_val, const int32_t *__restrict__ part_idx,
+                  const float2 *__restrict__ part_ms, int rows, int nch, int K,
+                  float *__restrict__ top_lp, int32_t *__restrict__ top_ids,
+                  int32_t *__restrict__ status)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (row >= rows)
         return;
-    __threadfence();
-
-    const int total = nch * K;
+    // ---- log-partition
+    float M = DDT_NEG_INF, S = 0.f;
+    for (int c0 = 0; c0 < nch; c0 += 32) {
+        const int c = c0 + lane;
+        float2 ms = make_float2(DDT_NEG_INF, 0.f);
+        if (c < nch)
+            ms = part_ms[(int64_t)row * nch + c];
+        float wm = ms.x;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+        float t = (ms.x != DDT_NEG_INF) ? ms.y * ex2((ms.x - wm) * DDT_LOG2E) : (ms.y != ms.y ? ms.y : 0.f);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+        ms_combine(M, S, wm, t);
+    }
+    if (lane == 0 && S != S)
+        set_status(status, DDT_DEV_NAN_LOGITS);
+    const double logz = (double)M + log((double)S);
     const float *rv = part_val + (int64_t)row * nch * K;
     const int32_t *ri = part_idx + (int64_t)row * nch * K;
-    for (int i = tid; i < total; i += TOPK_THREADS) {
-        s_val[i] = __ldcg(rv + i);
-        s_idx[i] = __ldcg(ri + i);
-    }
-    if (warp == 0) {  // the row's (max, sum) from the chunks', one warp
-        float M = DDT_NEG_INF, S = 0.f;
-        for (int c0 = 0; c0 < nch; c0 += 32) {
-            const int c = c0 + lane;
-            float2 ms = make_float2(DDT_NEG_INF, 0.f);
-            if (c < nch)
-                ms = __ldcg(&part_ms[(int64_t)row * nch + c]);
-            float wm = ms.x;
+    float *olp = top_lp + (int64_t)row * K;
+    int32_t *oid = top_ids + (int64_t)row * K;
+
+    if (K <= 32) {
+        uint64_t cur = (lane < K) ? make_key(rv[lane], ri[lane]) : 0ull;
+        for (int b = 1; b < nch; ++b) {
+            const int src = 31 - lane;  // the list reversed: ascending
+            const uint64_t o = (src < K) ? make_key(rv[b * K + src], ri[b * K + src]) : 0ull;
+            cur = cur > o ? cur : o;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
-            float t = (ms.x != DDT_NEG_INF) ? ms.y * ex2((ms.x - wm) * DDT_LOG2E) : (ms.y != ms.y ? ms.y : 0.f);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-                t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
-            ms_combine(M, S, wm, t);
-        }
-        if (lane == 0) {
-            if (S != S)
-                set_status(status, DDT_DEV_NAN_LOGITS);
-            s_logz = (double)M + log((double)S);
-            cnt[row] = 0u;  // ready for the next launch
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < total; i += TOPK_THREADS) {
-        const int a = i / K, rho = i - a * K;
-        const float vi = s_val[i];
-        const int ii = s_idx[i];
-        if (ii == 0x7FFFFFFF)
-            continue;
-        int rank = rho;
-        for (int b = 0; b < nch && rank < K; ++b) {
-            if (b == a)
-                continue;
-            // entries of list b that beat (vi, ii): lists are sorted, so binary search
-            int lo = 0, hi = K;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (beats(s_val[b * K + mid], s_idx[b * K + mid], vi, ii))
-                    lo = mid + 1;
-                else
-                    hi = mid;
+            for (int j = 16; j > 0; j >>= 1) {
+                const uint64_t p = shfl_xor64(cur, j);
+                cur = (lane & j) ? (cur < p ? cur : p) : (cur > p ? cur : p);
             }
-            rank += lo;
         }
-        if (rank < K) {
-            top_lp[(int64_t)row * K + rank] = (float)((double)vi - s_logz);
-            top_ids[(int64_t)row * K + rank] = ii;
+        if (lane < K) {
+            const int id = key_idx(cur);
+            const bool pad = (cur == 0ull) || id == IDX_PAD;
+            olp[lane] = pad ? DDT_NEG_INF : (float)((double)key_val(cur) - logz);
+            oid[lane] = pad ? -1 : id;
+        }
+    } else {
+        for (int r = lane; r < K; r += 32) {  // unfilled ranks: padding
+            olp[r] = DDT_NEG_INF;
+            oid[r] = -1;
+        }
+        __syncwarp();
+        for (int i = lane; i < nch * K; i += 32) {
+            const int a = i / K, rho = i - a * K;
+            const uint64_t ki = make_key(rv[i], ri[i]);
+            if (key_idx(ki) == IDX_PAD)
+                continue;
+            int rank = rho;
+            for (int b = 0; b < nch && rank < K; ++b) {
+                if (b == a)
+                    continue;
+                int lo = 0, hi = K;  // entries of list b that beat entry i
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (make_key(rv[b * K + mid], ri[b * K + mid]) > ki)
+                        lo = mid + 1;
+                    else
+                        hi = mid;
+                }
+                rank += lo;
+            }
+            if (rank < K) {
+                olp[rank] = (float)((double)key_val(ki) - logz);
+                oid[rank] = key_idx(ki);
+            }
         }
     }
 }
 
+}  // namespace
+
+namespace {
+cudaError_t launch_merge(int rows, int V, int K, int nch, const float *part_val,
+                         const int32_t *part_idx, const float2 *part_ms, float *top_lp,
+                         int32_t *top_ids, int32_t *status, cudaStream_t s)
+{
+    (void)V;
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nch == 1 || rows == 0)
+        return e;
+    topk_merge_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_val, part_idx, part_ms, rows, nch, K,
+                                                     top_lp, top_ids, status);
+    return cudaGetLastError();
+}
 }  // namespace
 
 int topk_chunk_elems(int dtype)
@@ -517,22 +618,23 @@ cudaError_t launch_topk(const ddt_ctx *c, const void *z, int R, float *top_lp, i
         if (aligned)
             topk_chunk_kernel<uint16_t, true><<<grid, TOPK_THREADS, 0, s>>>(
                 (const uint16_t *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
-                c->tk_cnt, top_lp, top_ids, c->status);
+                top_lp, top_ids, c->status);
         else
             topk_chunk_kernel<uint16_t, false><<<grid, TOPK_THREADS, 0, s>>>(
                 (const uint16_t *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
-                c->tk_cnt, top_lp, top_ids, c->status);
+                top_lp, top_ids, c->status);
     } else {
         if (aligned)
             topk_chunk_kernel<float, true><<<grid, TOPK_THREADS, 0, s>>>(
                 (const float *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
-                c->tk_cnt, top_lp, top_ids, c->status);
+                top_lp, top_ids, c->status);
         else
             topk_chunk_kernel<float, false><<<grid, TOPK_THREADS, 0, s>>>(
                 (const float *)z, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms,
-                c->tk_cnt, top_lp, top_ids, c->status);
+                top_lp, top_ids, c->status);
     }
-    return cudaGetLastError();
+    return launch_merge(rows, cfg.V, cfg.K, c->tk_nch, c->tk_val, c->tk_idx, c->tk_ms, top_lp,
+                        top_ids, c->status, s);
 }
 
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,
@@ -547,21 +649,21 @@ cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K
     if (bf16) {
         if (aligned)
             topk_chunk_kernel<uint16_t, true><<<grid, TOPK_THREADS, 0, s>>>(
-                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, top_lp, top_ids,
                 status);
         else
             topk_chunk_kernel<uint16_t, false><<<grid, TOPK_THREADS, 0, s>>>(
-                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                (const uint16_t *)z, V, K, nch, part_val, part_idx, part_ms, top_lp, top_ids,
                 status);
     } else {
         if (aligned)
             topk_chunk_kernel<float, true><<<grid, TOPK_THREADS, 0, s>>>(
-                (const float *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                (const float *)z, V, K, nch, part_val, part_idx, part_ms, top_lp, top_ids,
                 status);
         else
             topk_chunk_kernel<float, false><<<grid, TOPK_THREADS, 0, s>>>(
-                (const float *)z, V, K, nch, part_val, part_idx, part_ms, cnt, top_lp, top_ids,
+                (const float *)z, V, K, nch, part_val, part_idx, part_ms, top_lp, top_ids,
                 status);
     }
-    return cudaGetLastError();
+    return launch_merge(rows, V, K, nch, part_val, part_idx, part_ms, top_lp, top_ids, status, s);
 }
