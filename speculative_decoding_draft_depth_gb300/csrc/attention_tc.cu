@@ -6,11 +6,15 @@
 // tree query row attends to its request's cached context through the page
 // table plus the tree positions its ancestor mask allows.
 //
-// Work items = (request r, KV head g, context chunk s, row group). A plan
-// kernel picks the chunk length from the batch's total work (long chunks when
-// there is plenty of work, so that few (r, g) pairs are split), and sorts the
-// items by size, largest first; persistent CTAs take items from a global
-// counter in that order.
+// Work split: for one KV head, every (request r, row group) pair is a run of
+// tiles (its ceil(ctx_r / 128) context tiles, then the tree tile); laid end to
+// end they form one sequence of T tiles, the same for every head. The CTAs
+// form NG groups of Hkv, CTA c = grp * Hkv + g taking head g of tiles
+// [T grp / NG, T (grp + 1) / NG): equal shares, computed by each CTA from
+// ctx_lens (no plan kernel), and the Hkv CTAs of a group read the same
+// tokens' cache rows at about the same time. A pair cut by a share boundary
+// leaves per-CTA partials (two slots per CTA: its first and its last
+// segment), combined by whichever of its CTAs finishes last.
 //
 // Inside a CTA (one per SM), for one item:
 //  * main rows: 128 query rows = 128/G positions x G heads (row = pos*G+h);
@@ -27,7 +31,7 @@
 //    issued by 8 lanes of the loader warp at once; Q is double-buffered.
 //  * warps 0-15: main-row softmax and epilogue, four warps per TMEM lane
 //    quarter, each on 32 of the 128 columns; warps 16-19: tail-row softmax;
-//    warp 20: item fetch, Q and K loads; warp 21: V loads; warp 22: TMEM
+//    warp 20: walks the CTA's share and loads Q and K; warp 21: V loads; warp 22: TMEM
 //    owner and MMA issuer, which polls its barriers and issues whichever of
 //    the next Q K^T and the next P V is ready.
 //  * softmax in the base-2 domain with a lazily updated reference max: O and
@@ -55,7 +59,7 @@ constexpr int NTAILT = 128;               // tail-row softmax threads (warps 16-
 constexpr int NSOFT = NMAIN + NTAILT;
 constexpr int W_TAIL0 = 16, W_KPROD = 20, W_VPROD = 21, W_MMA = 22;
 constexpr int NTHREADS = 23 * 32;
-constexpr int NRING = 4;                  // fetched-item ring
+constexpr int NRING = 4;                  // ring of segments handed from the walker to the other roles
 constexpr int RING_CONSUMERS = 1 + 1 + 16 + 4;  // V loader, MMA, main warps, tail warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;     // two S buffers (P overwrites their first columns)
@@ -65,7 +69,6 @@ constexpr uint32_t TM_OT = 416;  // O tail: 416..431
 constexpr float TAU = 8.0f;      // lazy-rescale threshold (log2 units)
 constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles (about 2 s)
 constexpr long long DRAIN_LIMIT = 200000000LL;   // cycles, for the wind-down waits
-constexpr int PLAN_BINS = 2048;
 
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t QSLOT = 36864;              // main 2 x 16 KB d-halves + tail 2 x 2 KB
@@ -95,7 +98,8 @@ constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16, B_KFULL = 32, B_KEMPTY = 48, B_VF
                    B_TLBAR = 360,   // tail-sum exchange (128 arrivals)
                    B_IBAR = 368,    // all softmax threads, split-item combine (640 arrivals)
                    B_TMEM = 376, B_ABORT = 380, B_LAST = 384,
-                   B_RING = 400,    // [NRING] ints: item indices
+                   B_RING = 400,    // [NRING][4] ints: segments (x = -1: end of the share)
+                   B_TOTAL = 464,   // int: T, the batch's total tiles
                    B_RED = 512,     // 2 x [4 warps][16] floats: tail column max
                    B_SUM = 1024,    // 2 x [4 warps][16] floats: tail sums
                    B_XMAX = 1536,   // 2 x [4 column quarters][128 rows] floats: row max
@@ -107,9 +111,6 @@ constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
 constexpr uint32_t IDESC_PVT = idesc_bf16(128, 16, true, false);
 
 struct TcArgs {
-    const int4 *items;
-    int32_t *meta;             // [0] item count, [1] work counter
-    const int32_t *rg_base;
     const int32_t *block_table;
     const int32_t *ctx_lens;
     const uint32_t *mask;
@@ -118,30 +119,50 @@ struct TcArgs {
     float2 *part_ml;
     unsigned *rg_cnt;
     int32_t *status;
-    int P, Hq, Hkv, G, g_shift, W, page_shift, max_pages, RG, n_main, tail_rows;
+    int R, P, Hq, Hkv, G, g_shift, W, page_shift, max_pages, RG, n_main, tail_rows, max_ctx;
     int64_t num_pages;
     float scale_log2;
 };
 
 struct Item {
-    int r, g, rg, s, ns, t0, t1, ntile_ctx, ntiles;
-    bool last, has_tail;
+    int r, g, rg, ps, t0, t1, ntile_ctx, ntiles;
+    bool last, has_tail, single;
 };
 
-DDT_DEVINL void decode_item(const TcArgs &a, int idx, Item &it)
+// a segment: x = r | g << 12 | rg << 20 | last << 24 | single << 25 (single: the
+// whole pair lies in this CTA's share), y = the pair's first tile in the
+// batch sequence, z, w = the segment's context tokens [t0, t1)
+DDT_DEVINL void decode_item(const TcArgs &a, int x, int y, int z, int w, Item &it)
 {
-    const int4 w = a.items[idx];
-    it.r = w.x & 0xFFF;
-    it.ns = w.x >> 12;
-    it.g = w.y & 0xFF;
-    it.rg = (w.y >> 8) & 0xFF;
-    it.s = w.y >> 16;
-    it.t0 = w.z;
-    it.t1 = w.w;
-    it.last = (it.s == it.ns - 1);
+    it.r = x & 0xFFF;
+    it.g = (x >> 12) & 0xFF;
+    it.rg = (x >> 20) & 0xF;
+    it.last = ((x >> 24) & 1) != 0;
+    it.single = ((x >> 25) & 1) != 0;
+    it.ps = y;
+    it.t0 = z;
+    it.t1 = w;
     it.ntile_ctx = (it.t1 > it.t0) ? (it.t1 - it.t0 + TILE - 1) / TILE : 0;
     it.ntiles = it.ntile_ctx + (it.last ? 1 : 0);
     it.has_tail = (it.rg == 0 && a.tail_rows > 0);
+}
+
+// tiles of one (request r, row group) pair of a head: context tiles, then the tree tile
+DDT_DEVINL int pair_tiles(const TcArgs &a, int r)
+{
+    const int c = min(max(__ldg(&a.ctx_lens[r]), 0), a.max_ctx);
+    return (c + TILE - 1) / TILE + 1;
+}
+// first tile of group grp's share (of NG), and the group whose share holds tile t
+DDT_DEVINL long long share_start(long long T, int grp, int NG) { return T * grp / NG; }
+DDT_DEVINL int share_of(long long t, long long T, int NG) { return (int)(((t + 1) * NG + T - 1) / T - 1); }
+// partial slot of the segment that group grp's CTA for head g holds of a pair
+// starting at tile ps: that CTA's first segment (the pair began at or before
+// its share) or its last one
+DDT_DEVINL int part_slot(long long ps, long long T, int grp, int NG, int g, int Hkv)
+{
+    const int c = grp * Hkv + g;
+    return (ps <= share_start(T, grp, NG)) ? 2 * c : 2 * c + 1;
 }
 
 // bounded mbarrier wait; false (and the abort flag raised) on timeout
@@ -186,21 +207,29 @@ DDT_DEVINL bool gsync(uint32_t bar, uint32_t parity, volatile int *abort_flag, i
     return wait_warp(bar, parity, abort_flag, status);
 }
 
-// k-th fetched item index of this CTA (-1: no more); lane 0 of a consumer
-// warp frees the ring entry once every lane has the value
-DDT_DEVINL bool ring_get(uint32_t bar, const volatile int *ring, int k, int lane, bool release,
-                         volatile int *abort_flag, int32_t *status, int &idx)
+// k-th segment of this CTA's share (false: end of the share, or abort); lane 0
+// of a consumer warp frees the ring entry once every lane has the value
+DDT_DEVINL bool ring_get(const TcArgs &a, uint32_t bar, const volatile int *ring, int k, int lane,
+                         volatile int *abort_flag, Item &it)
 {
     const int slot = k & (NRING - 1);
-    if (!wait_warp(bar + B_RFULL + 8 * slot, (k / NRING) & 1, abort_flag, status))
+    if (!wait_warp(bar + B_RFULL + 8 * slot, (k / NRING) & 1, abort_flag, a.status))
         return false;
-    int v = 0;
+    int v0 = 0, v1 = 0, v2 = 0, v3 = 0;
     if (lane == 0) {
-        v = ring[slot];
-        if (release)
-            mbar_arrive(bar + B_REMPTY + 8 * slot);
+        v0 = ring[4 * slot];
+        v1 = ring[4 * slot + 1];
+        v2 = ring[4 * slot + 2];
+        v3 = ring[4 * slot + 3];
+        mbar_arrive(bar + B_REMPTY + 8 * slot);
     }
-    idx = __shfl_sync(0xFFFFFFFFu, v, 0);
+    v0 = __shfl_sync(0xFFFFFFFFu, v0, 0);
+    if (v0 < 0)
+        return false;
+    v1 = __shfl_sync(0xFFFFFFFFu, v1, 0);
+    v2 = __shfl_sync(0xFFFFFFFFu, v2, 0);
+    v3 = __shfl_sync(0xFFFFFFFFu, v3, 0);
+    decode_item(a, v0, v1, v2, v3, it);
     return true;
 }
 
@@ -238,11 +267,12 @@ DDT_DEVINL int group_row(const TcArgs &a, const Item &it, int j, int u)
     return it.r * a.P + 16 * u;  // the tree tile: rows of k_tree / v_tree
 }
 
-// whole loader warp: the 16 boxes of one K or V tile into dst, completing on fb
-DDT_DEVINL void load_tile(const TcArgs &a, const Item &it, int j, int lane, uint32_t dst,
+// whole loader warp: the 16 boxes of one K or V tile into dst, completing on fb;
+// z = group_row(...) of this lane, looked up before the wait for the slot so
+// that the page-table load overlaps it
+DDT_DEVINL void load_tile(const Item &it, int j, int lane, int z, uint32_t dst,
                           const void *map_c, const void *map_t, uint32_t fb)
 {
-    const int z = (lane < 8) ? group_row(a, it, j, lane) : 0;
     if (lane == 0)
         mbar_arrive_expect_tx(fb, 32768u);
     __syncwarp();
@@ -274,36 +304,46 @@ DDT_DEVINL float exps32(const uint32_t *sv, float scale, float m, uint32_t *pw)
     return (r0 + r1) + (r2 + r3);
 }
 
-// a finished split item: all softmax threads publish their partials, the CTA that
-// arrives last for its (r, g, row group) combines every chunk into the output
+// a finished split segment: all softmax threads publish their partials; the CTA
+// that arrives last for its pair combines every segment's into the output
 DDT_DEVINL void split_combine(const TcArgs &a, const Item &it, unsigned char *sgen, uint32_t bar,
                               int &ib, volatile int *abort_flag, int tid, int PG)
 {
     __threadfence();
     if (!gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status))
         return;
+    const long long T = *reinterpret_cast<volatile int *>(sgen + SM_BAR + B_TOTAL);
+    const int NG = gridDim.x / a.Hkv;
+    const long long ps = it.ps, pe = ps + pair_tiles(a, it.r);
+    const int c0 = share_of(ps, T, NG), c1 = share_of(pe - 1, T, NG);
     int *s_last = reinterpret_cast<int *>(sgen + SM_BAR + B_LAST);
-    const int rg_slot = (it.r * a.Hkv + it.g) * a.RG + it.rg;
-    if (tid == 0)
-        *s_last = (atomicAdd(&a.rg_cnt[rg_slot], 1u) == (unsigned)(it.ns - 1));
+    int *slots = reinterpret_cast<int *>(sgen + SM_BAR + B_XMAX + 2048);  // [<= 512]
+    const int pair = (it.r * a.Hkv + it.g) * a.RG + it.rg;
+    if (tid == 0) {
+        int ns = 0;  // groups with a segment of this pair (shares can be empty when T < NG)
+        for (int c = c0; c <= c1; ++c)
+            if (share_start(T, c, NG) < share_start(T, c + 1, NG))
+                slots[ns++] = part_slot(ps, T, c, NG, it.g, a.Hkv);
+        s_last[1] = ns;
+        s_last[0] = (atomicAdd(&a.rg_cnt[pair], 1u) == (unsigned)(ns - 1));
+    }
     if (!gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status))
         return;
     if (*reinterpret_cast<volatile int *>(s_last) == 0)
         return;
     __threadfence();
-    const int first = a.rg_base[rg_slot];
-    const int stride = a.Hkv * a.RG;
+    const int ns = *reinterpret_cast<volatile int *>(s_last + 1);
     const int nrows = TILE + (it.has_tail ? a.tail_rows : 0);
     // pass 1: per row, the common reference and the total weight
     float2 *fac = reinterpret_cast<float2 *>(sgen + SM_BAR + B_XMAX);  // [nrows] (M, 1/L)
     if (tid < nrows) {
         float M = DDT_NEG_INF;
-        for (int s = 0; s < it.ns; ++s)
-            M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)(first + s * stride) * ATT_ROWS + tid]).x);
+        for (int s = 0; s < ns; ++s)
+            M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)slots[s] * ATT_ROWS + tid]).x);
         const float base = (M == DDT_NEG_INF) ? 0.f : M;
         float Ls = 0.f;
-        for (int s = 0; s < it.ns; ++s) {
-            const float2 ml = __ldcg(&a.part_ml[(int64_t)(first + s * stride) * ATT_ROWS + tid]);
+        for (int s = 0; s < ns; ++s) {
+            const float2 ml = __ldcg(&a.part_ml[(int64_t)slots[s] * ATT_ROWS + tid]);
             Ls += (ml.x == DDT_NEG_INF) ? 0.f : ml.y * ex2(ml.x - base);
         }
         fac[tid] = make_float2(base, Ls > 0.f ? 1.f / Ls : 0.f);
@@ -318,8 +358,8 @@ DDT_DEVINL void split_combine(const TcArgs &a, const Item &it, unsigned char *sg
             continue;
         const float2 f = fac[rho];
         float x = 0.f;
-        for (int s = 0; s < it.ns; ++s) {
-            const int64_t ir = (int64_t)(first + s * stride) * ATT_ROWS + rho;
+        for (int s = 0; s < ns; ++s) {
+            const int64_t ir = (int64_t)slots[s] * ATT_ROWS + rho;
             const float m = __ldcg(&a.part_ml[ir]).x;
             if (m != DDT_NEG_INF)
                 x += __ldcg(&a.part_o[ir * 128 + d]) * ex2(m - f.x);
@@ -328,8 +368,8 @@ DDT_DEVINL void split_combine(const TcArgs &a, const Item &it, unsigned char *sg
         a.out[(((int64_t)it.r * a.P + i2) * a.Hq + it.g * a.G + h2) * 128 + d] = x * f.y;
     }
     if (tid == 0)
-        a.rg_cnt[rg_slot] = 0u;
-    // the fac scratch is reused by the next item's row-max exchange
+        a.rg_cnt[pair] = 0u;
+    // the fac and slot scratch is reused by the next segment's row-max exchange
     gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status);
 }
 
@@ -395,35 +435,106 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int pos_per_main = TILE >> a.g_shift;
 
     if (warp == W_KPROD) {
-        // ============================================================ fetch, Q and K loads
+        // ============================================================ share walk, Q and K loads
         if (lane == 0) {
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_qt);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_kt);
         }
-        const int count = a.meta[0];
+        // ---- T, and the pair holding this CTA's first tile: each lane sums the
+        //      tiles of a contiguous run of requests, then one warp scan
+        const int PR = a.RG;  // pairs per request, for one head
+        const int NG = gridDim.x / a.Hkv, grp = blockIdx.x / a.Hkv, head = blockIdx.x % a.Hkv;
+        const int per_lane = (a.R + 31) / 32;
+        long long mine = 0;
+        for (int i = 0; i < per_lane; ++i) {
+            const int r = lane * per_lane + i;
+            if (r < a.R)
+                mine += (long long)pair_tiles(a, r) * PR;
+        }
+        long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        const long long T = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const long long lo = share_start(T, grp, NG), hi = share_start(T, grp + 1, NG);
+        const long long excl = incl - mine;
+        const unsigned holder = __ballot_sync(0xFFFFFFFFu, lo < hi && excl <= lo && lo < excl + mine);
+        int wr = 0;             // walker state (lane 0): request, its first tile, pair, tile in pair
+        long long req_off = 0;
+        if (holder != 0 && lane == __ffs(holder) - 1) {
+            long long acc = excl;
+            for (int i = 0; i < per_lane; ++i) {
+                const int r = lane * per_lane + i;
+                const long long span = (long long)pair_tiles(a, r) * PR;
+                if (lo < acc + span) {
+                    wr = r;
+                    req_off = acc;
+                    break;
+                }
+                acc += span;
+            }
+        }
+        if (holder != 0) {
+            wr = __shfl_sync(0xFFFFFFFFu, wr, __ffs(holder) - 1);
+            req_off = __shfl_sync(0xFFFFFFFFu, req_off, __ffs(holder) - 1);
+        }
+        if (lane == 0)
+            *reinterpret_cast<volatile int *>(sgen + SM_BAR + B_TOTAL) = (int)T;
+        if (blockIdx.x == 0)  // out-of-range context lengths are clamped, and reported
+            for (int r = lane; r < a.R; r += 32) {
+                const int c = __ldg(&a.ctx_lens[r]);
+                if (c < 0 || c > a.max_ctx)
+                    atomicOr(a.status, DDT_DEV_BAD_PAGE);
+            }
+        int wtp = (holder != 0) ? pair_tiles(a, wr) : 1;
+        int wctx = (holder != 0) ? min(max(__ldg(&a.ctx_lens[wr]), 0), a.max_ctx) : 0;
+        int wp = (holder != 0) ? (int)((lo - req_off) / wtp) : 0;
+        int wa = (holder != 0) ? (int)((lo - req_off) % wtp) : 0;
+        long long cur = (holder != 0) ? lo : hi;
+
         int kn = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            // fetch the next item into ring slot k
+            // the next segment of the share into ring slot k
             const int slot = k & (NRING - 1);
             if (k >= NRING &&
                 !wait_warp(bar + B_REMPTY + 8 * slot, ((k / NRING) - 1) & 1, abort_flag, a.status))
                 break;
-            int idx = 0;
+            int ix = -1, iy = 0, iz = 0, iw = 0;
+            if (cur < hi) {
+                const long long ps = req_off + (long long)wp * wtp;
+                const int b = (int)min((long long)wtp, wa + (hi - cur));
+                const bool last = (b == wtp), single = (ps >= lo && ps + wtp <= hi);
+                ix = wr | (head << 12) | (wp << 20) | ((last ? 1 : 0) << 24) | ((single ? 1 : 0) << 25);
+                iy = (int)ps;
+                iz = min(wa * TILE, wctx);
+                iw = min(b * TILE, wctx);
+                cur += b - wa;
+                wa = 0;
+                if (++wp == PR && cur < hi) {  // next request
+                    wp = 0;
+                    req_off += (long long)wtp * PR;
+                    ++wr;
+                    wtp = pair_tiles(a, wr);
+                    wctx = min(max(__ldg(&a.ctx_lens[wr]), 0), a.max_ctx);
+                }
+            }
             if (lane == 0) {
-                idx = atomicAdd(&a.meta[1], 1);
-                if (idx >= count)
-                    idx = -1;
-                ring[slot] = idx;
+                ring[4 * slot] = ix;
+                ring[4 * slot + 1] = iy;
+                ring[4 * slot + 2] = iz;
+                ring[4 * slot + 3] = iw;
                 mbar_arrive(bar + B_RFULL + 8 * slot);
             }
-            idx = __shfl_sync(0xFFFFFFFFu, idx, 0);
-            if (idx < 0)
+            if (ix < 0)
                 break;
             Item it;
-            decode_item(a, idx, it);
+            decode_item(a, ix, iy, iz, iw, it);
             // Q of item k into slot k & 1
             const int qs = k & 1;
             if (k >= 2 && !wait_warp(bar + B_QEMPTY + 8 * qs, ((k >> 1) - 1) & 1, abort_flag, a.status))
@@ -442,12 +553,13 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             for (int j = 0; j < it.ntiles; ++j, ++kn) {
                 const int sl = kn & 1;
+                const int z = (lane < 8) ? group_row(a, it, j, lane) : 0;
                 if (kn >= 2 &&
                     !wait_warp(bar + B_KEMPTY + 8 * sl, ((kn - 2) >> 1) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
-                load_tile(a, it, j, lane, sb + SM_K + sl * 32768u, &tm_k, &tm_kt, bar + B_KFULL + 8 * sl);
+                load_tile(it, j, lane, z, sb + SM_K + sl * 32768u, &tm_k, &tm_kt, bar + B_KFULL + 8 * sl);
             }
         }
         // wind down: the last K tiles this warp issued have landed
@@ -463,19 +575,18 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int vn = 0;
         bool ok = true;
         for (int k = 0; ok; ++k) {
-            int idx;
-            if (!ring_get(bar, ring, k, lane, true, abort_flag, a.status, idx) || idx < 0)
-                break;
             Item it;
-            decode_item(a, idx, it);
+            if (!ring_get(a, bar, ring, k, lane, abort_flag, it))
+                break;
             for (int j = 0; j < it.ntiles; ++j, ++vn) {
                 const int sl = vn & 1;
+                const int z = (lane < 8) ? group_row(a, it, j, lane) : 0;
                 if (vn >= 2 &&
                     !wait_warp(bar + B_VEMPTY + 8 * sl, ((vn - 2) >> 1) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
-                load_tile(a, it, j, lane, sb + SM_V + sl * 32768u, &tm_v, &tm_vt, bar + B_VFULL + 8 * sl);
+                load_tile(it, j, lane, z, sb + SM_V + sl * 32768u, &tm_v, &tm_vt, bar + B_VFULL + 8 * sl);
             }
         }
         for (int m = vn - 2; m < vn; ++m)
@@ -508,11 +619,11 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (qk_state == 0) {
                     const int slot = qk_k & (NRING - 1);
                     if (mbar_test_wait(bar + B_RFULL + 8 * slot, (qk_k / NRING) & 1)) {
-                        const int idx = ring[slot];
-                        if (idx < 0) {
+                        const int x = ring[4 * slot];
+                        if (x < 0) {
                             qk_state = 2;
                         } else {
-                            decode_item(a, idx, qi);
+                            decode_item(a, x, ring[4 * slot + 1], ring[4 * slot + 2], ring[4 * slot + 3], qi);
                             qk_state = 1;
                             qk_j = 0;
                         }
@@ -522,12 +633,13 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (pv_state == 0) {
                     const int slot = pv_k & (NRING - 1);
                     if (mbar_test_wait(bar + B_RFULL + 8 * slot, (pv_k / NRING) & 1)) {
-                        const int idx = ring[slot];
+                        const int x = ring[4 * slot];
+                        if (x >= 0)
+                            decode_item(a, x, ring[4 * slot + 1], ring[4 * slot + 2], ring[4 * slot + 3], pi);
                         mbar_arrive(bar + B_REMPTY + 8 * slot);
-                        if (idx < 0) {
+                        if (x < 0) {
                             pv_state = 2;
                         } else {
-                            decode_item(a, idx, pi);
                             pv_state = 1;
                             pv_j = 0;
                         }
@@ -635,11 +747,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int n = 0, ib = 0;
         bool alive = true;
         for (int k = 0; alive; ++k) {
-            int idx;
-            if (!ring_get(bar, ring, k, lane, true, abort_flag, a.status, idx) || idx < 0)
-                break;
             Item it;
-            decode_item(a, idx, it);
+            if (!ring_get(a, bar, ring, k, lane, abort_flag, it))
+                break;
             const int gr = it.rg * TILE + row;
             const bool row_ok = gr < PG;
             const int pos = gr >> a.g_shift, hl = gr & (a.G - 1);
@@ -761,9 +871,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!gsync(bar + B_LBAR + 8 * qw, k & 1, abort_flag, a.status))
                 break;
             const float lrow = (xlb[row] + xlb[128 + row]) + (xlb[256 + row] + xlb[384 + row]);
-            const bool single = (it.ns == 1);
-            const int nat = single ? 0 : __ldg(&a.rg_base[(it.r * a.Hkv + it.g) * a.RG + it.rg]) +
-                                             it.s * a.Hkv * a.RG;
+            const bool single = it.single;
+            const int nat = single ? 0 : part_slot(it.ps, *reinterpret_cast<volatile int *>(sgen + SM_BAR + B_TOTAL),
+                                                   blockIdx.x / a.Hkv, gridDim.x / a.Hkv, it.g, a.Hkv);
             const int64_t item_row0 = (int64_t)nat * ATT_ROWS;
             const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
             float *dst = a.out + (((int64_t)it.r * a.P + pos) * a.Hq + it.g * a.G + hl) * 128 + col0;
@@ -811,14 +921,12 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int nt = 0, tail_items = 0, ib = 0;
         bool alive = true;
         for (int k = 0; alive; ++k) {
-            int idx;
-            if (!ring_get(bar, ring, k, lane, true, abort_flag, a.status, idx) || idx < 0)
-                break;
             Item it;
-            decode_item(a, idx, it);
+            if (!ring_get(a, bar, ring, k, lane, abort_flag, it))
+                break;
             const int tail = it.has_tail ? a.tail_rows : 0;
             if (tail == 0) {
-                if (it.ns != 1)
+                if (!it.single)
                     split_combine(a, it, sgen, bar, ib, abort_flag, ttid + NMAIN, PG);
                 continue;
             }
@@ -932,9 +1040,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!gsync(bar + B_TLBAR, tail_items & 1, abort_flag, a.status))
                 break;
             ++tail_items;
-            const bool single = (it.ns == 1);
-            const int nat = single ? 0 : __ldg(&a.rg_base[(it.r * a.Hkv + it.g) * a.RG + it.rg]) +
-                                             it.s * a.Hkv * a.RG;
+            const bool single = it.single;
+            const int nat = single ? 0 : part_slot(it.ps, *reinterpret_cast<volatile int *>(sgen + SM_BAR + B_TOTAL),
+                                                   blockIdx.x / a.Hkv, gridDim.x / a.Hkv, it.g, a.Hkv);
             const int64_t item_row0 = (int64_t)nat * ATT_ROWS;
             uint32_t ov[16];
             if (it.ntiles > 0) {
@@ -976,181 +1084,6 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
 }
 
-// block-wide exclusive scan of arr[0..n) in place (blockDim.x == 1024); returns the total
-__device__ int block_excl_scan(int *arr, int n, int *s_wsum, int *s_carry)
-{
-    const int tid = threadIdx.x, nth = blockDim.x;
-    if (tid == 0)
-        *s_carry = 0;
-    __syncthreads();
-    for (int base = 0; base < n; base += nth) {
-        const int i = base + tid;
-        const int v = (i < n) ? arr[i] : 0;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if ((tid & 31) >= o)
-                x += y;
-        }
-        if ((tid & 31) == 31)
-            s_wsum[tid >> 5] = x;
-        __syncthreads();
-        if (tid < 32) {
-            int w = (tid < nth / 32) ? s_wsum[tid] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-                if (tid >= o)
-                    w += y;
-            }
-            s_wsum[tid] = w;  // inclusive prefix of the warp totals
-        }
-        __syncthreads();
-        const int excl = *s_carry + x - v + ((tid >> 5) > 0 ? s_wsum[(tid >> 5) - 1] : 0);
-        if (i < n)
-            arr[i] = excl;
-        __syncthreads();
-        if (tid == 0)
-            *s_carry += s_wsum[nth / 32 - 1];
-        __syncthreads();
-    }
-    return *s_carry;
-}
-
-// ---------------------------------------------------------------- plan
-// One CTA. Chooses the chunk length C (tiles) from the batch's total work,
-// cuts every (r, g, row group) context into ns = ceil(tiles / C) near-equal
-// chunks of whole tiles (the last one also carries the tree tile), and writes
-// the items sorted by size, largest first (order within a size is free).
-// meta[0] = item count, meta[1] = 0 (the work counter).
-__global__ void att_tc_plan_kernel(const int32_t *__restrict__ ctx_lens, int R, int Hkv, int RG,
-                                   int max_ctx, int cap, int num_sms, int4 *__restrict__ items,
-                                   int32_t *__restrict__ rg_base, int32_t *__restrict__ meta,
-                                   int32_t *__restrict__ status)
-{
-    extern __shared__ int sp[];
-    int *s_ctx = sp, *s_ns = sp + R, *s_len = sp + 2 * R, *s_off = sp + 3 * R;
-    int *s_hist = sp + 4 * R;                 // PLAN_BINS
-    __shared__ long long s_total;
-    __shared__ int s_wsum[32];
-    __shared__ int s_count;
-    const int tid = threadIdx.x, nth = blockDim.x;
-    const int per_req = Hkv * RG;
-    if (tid == 0)
-        s_total = 0;
-    for (int i = tid; i < PLAN_BINS; i += nth)
-        s_hist[i] = 0;
-    __syncthreads();
-    long long mine = 0;
-    for (int r = tid; r < R; r += nth) {
-        int c = ctx_lens[r];
-        if (c < 0 || c > max_ctx) {
-            set_status(status, DDT_DEV_BAD_PAGE);
-            c = c < 0 ? 0 : max_ctx;
-        }
-        s_ctx[r] = c;
-        mine += (long long)((c + TILE - 1) / TILE + 1) * per_req;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        mine += __shfl_xor_sync(0xFFFFFFFFu, mine, o);
-    if ((tid & 31) == 0 && mine != 0)
-        atomicAdd((unsigned long long *)&s_total, (unsigned long long)mine);
-    __syncthreads();
-    const long long T = s_total;
-    const long long npairs = (long long)R * per_req;
-    long long C = (T + 2LL * num_sms - 1) / (2LL * num_sms);
-    if (C < 4)
-        C = 4;
-    const long long room = (long long)cap - npairs;
-    if (room > 0) {
-        const long long cmin = (T + room - 1) / room;
-        if (C < cmin)
-            C = cmin;
-    } else {
-        C = 1LL << 30;  // one chunk per pair
-    }
-    for (int r = tid; r < R; r += nth) {
-        const int tiles = (s_ctx[r] + TILE - 1) / TILE;
-        const int ns = tiles > 0 ? (int)((tiles + C - 1) / C) : 1;
-        s_ns[r] = ns;
-        s_len[r] = tiles > 0 ? (tiles + ns - 1) / ns : 0;
-    }
-    __syncthreads();
-    // item offsets: exclusive scan of ns * per_req over r
-    for (int r = tid; r < R; r += nth)
-        s_off[r] = s_ns[r] * per_req;
-    __syncthreads();
-    const int n_items = block_excl_scan(s_off, R, s_wsum, &s_count);
-    // sizes -> histogram (largest first)
-    for (int i0 = 0; i0 < n_items; i0 += nth) {
-        const int i = i0 + tid;
-        int bin = -1;
-        if (i < n_items) {
-            int lo = 0, hi = R - 1;  // last r with s_off[r] <= i
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (s_off[mid] <= i)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            const int r = lo, rem = i - s_off[r], s = rem / per_req;
-            const int ctx = s_ctx[r], len = s_len[r] * TILE;
-            const int t0 = min(ctx, s * len), t1 = min(ctx, (s + 1) * len);
-            const int size = (t1 - t0 + TILE - 1) / TILE + (s == s_ns[r] - 1 ? 1 : 0);
-            bin = PLAN_BINS - 1 - min(size, PLAN_BINS - 1);
-        }
-        const unsigned same = __match_any_sync(0xFFFFFFFFu, bin);
-        if (bin >= 0 && (tid & 31) == __ffs(same) - 1)
-            atomicAdd(&s_hist[bin], __popc(same));
-    }
-    __syncthreads();
-    block_excl_scan(s_hist, PLAN_BINS, s_wsum, &s_count);
-    for (int i0 = 0; i0 < n_items; i0 += nth) {
-        const int i = i0 + tid;
-        int bin = -1, r = 0, s = 0, g = 0, rg = 0, ns = 0, t0 = 0, t1 = 0;
-        if (i < n_items) {
-            int lo = 0, hi = R - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (s_off[mid] <= i)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            r = lo;
-            const int rem = i - s_off[r];
-            s = rem / per_req;
-            g = (rem / RG) % Hkv;
-            rg = rem % RG;
-            const int ctx = s_ctx[r], len = s_len[r] * TILE;
-            ns = s_ns[r];
-            t0 = min(ctx, s * len);
-            t1 = min(ctx, (s + 1) * len);
-            const int size = (t1 - t0 + TILE - 1) / TILE + (s == ns - 1 ? 1 : 0);
-            bin = PLAN_BINS - 1 - min(size, PLAN_BINS - 1);
-        }
-        const unsigned same = __match_any_sync(0xFFFFFFFFu, bin);
-        const int leader = __ffs(same) - 1;
-        int base = 0;
-        if (bin >= 0 && (tid & 31) == leader)
-            base = atomicAdd(&s_hist[bin], __popc(same));
-        base = __shfl_sync(0xFFFFFFFFu, base, leader);
-        if (bin >= 0) {
-            const int at = base + __popc(same & ((1u << (tid & 31)) - 1u));
-            items[at] = make_int4(r | (ns << 12), g | (rg << 8) | (s << 16), t0, t1);
-            if (s == 0)
-                rg_base[((int64_t)r * Hkv + g) * RG + rg] = s_off[r] + g * RG + rg;
-        }
-    }
-    if (tid == 0) {
-        meta[0] = n_items;
-        meta[1] = 0;
-    }
-}
-
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1187,7 +1120,7 @@ bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int bh,
 }
 
 template <int TQ>
-cudaError_t launch_tq(const ddt_ctx *c, const CUtensorMap &tq, const CUtensorMap &tqt,
+cudaError_t launch_tq(int grid, const CUtensorMap &tq, const CUtensorMap &tqt,
                       const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tkt,
                       const CUtensorMap &tvt, const TcArgs &a, cudaStream_t s)
 {
@@ -1200,7 +1133,7 @@ cudaError_t launch_tq(const ddt_ctx *c, const CUtensorMap &tq, const CUtensorMap
             return e;
         attr_set = true;
     }
-    att_tc_kernel<TQ><<<c->num_sms, NTHREADS, SM_ALLOC, s>>>(tq, tqt, tk, tv, tkt, tvt, a);
+    att_tc_kernel<TQ><<<grid, NTHREADS, SM_ALLOC, s>>>(tq, tqt, tk, tv, tkt, tvt, a);
     return cudaGetLastError();
 }
 
@@ -1210,8 +1143,15 @@ bool attention_tc_supported(const ddt_config &cfg)
 {
     const int G = cfg.Hq / cfg.Hkv;
     const int pg = cfg.page_size;
-    return cfg.d == 128 && pg >= 16 && (pg & (pg - 1)) == 0 && G >= 1 && G <= 16 &&
-           (16 % G) == 0 && cfg.R_max < 4096 && encode_fn() != nullptr;
+    if (!(cfg.d == 128 && pg >= 16 && (pg & (pg - 1)) == 0 && G >= 1 && G <= 16 && (16 % G) == 0 &&
+          cfg.R_max < 4096 && cfg.Hkv < 256 && encode_fn() != nullptr))
+        return false;
+    int nm, tail, RG;
+    attention_tc_rows(cfg, &nm, &tail, &RG);
+    // the batch's tile count (and every tile index) must fit in 31 bits
+    const long long max_ctx = (long long)cfg.max_pages_per_req * cfg.page_size;
+    const long long tmax = (long long)cfg.R_max * cfg.Hkv * RG * ((max_ctx + TILE - 1) / TILE + 1);
+    return RG <= 16 && tmax < (1LL << 31);
 }
 
 void attention_tc_rows(const ddt_config &cfg, int *n_main, int *tail_rows, int *rowgroups)
@@ -1250,18 +1190,7 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
         !make_map(&tkt, k_tree, cfg.Hkv, rowsq, 1, 16) ||
         !make_map(&tvt, v_tree, cfg.Hkv, rowsq, 1, 16))
         return cudaErrorInvalidValue;
-    const int max_ctx = cfg.max_pages_per_req * cfg.page_size;
-    const size_t plan_smem = (size_t)(4 * R + PLAN_BINS) * sizeof(int);
-    att_tc_plan_kernel<<<1, 1024, plan_smem, s>>>(ctx_lens, R, cfg.Hkv, RG, max_ctx,
-                                                  c->att_max_items, c->num_sms, c->att_items,
-                                                  c->att_rg_base, c->att_meta, c->status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess)
-        return e;
     TcArgs a;
-    a.items = c->att_items;
-    a.meta = c->att_meta;
-    a.rg_base = c->att_rg_base;
     a.block_table = block_table;
     a.ctx_lens = ctx_lens;
     a.mask = mask;
@@ -1270,6 +1199,8 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     a.part_ml = c->att_part_ml;
     a.rg_cnt = c->att_rg_cnt;
     a.status = c->status;
+    a.R = R;
+    a.max_ctx = cfg.max_pages_per_req * cfg.page_size;
     a.P = P;
     a.Hq = cfg.Hq;
     a.Hkv = cfg.Hkv;
@@ -1287,7 +1218,14 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     a.tail_rows = tail;
     a.num_pages = cfg.num_pages;
     a.scale_log2 = 1.4426950408889634f / sqrtf(128.0f);
+    // groups of Hkv CTAs (one per KV head), two partial slots per CTA
+    int groups = c->num_sms / cfg.Hkv;
+    if (groups < 1)
+        groups = 1;
+    while (groups > 1 && groups * cfg.Hkv * 2 > c->att_max_items)
+        --groups;
+    const int grid = groups * cfg.Hkv;
     if (tail <= 4)
-        return launch_tq<4>(c, tq, tqt, tk, tv, tkt, tvt, a, s);
-    return launch_tq<16>(c, tq, tqt, tk, tv, tkt, tvt, a, s);
+        return launch_tq<4>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
+    return launch_tq<16>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
 }
