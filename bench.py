@@ -251,24 +251,10 @@ def main():
     R = cfg.R
 
     def step(att_events=None):
-        """One round through the four stage entry points (the kernels ddt_round
-        launches, in its order); CUDA events bracket the attention call."""
+        """One round: ddt_round (a1..a7); with att_events, the library records
+        the pair of CUDA events around the attention launch on `stream`."""
         d["ctx_lens"].copy_(ctx0, non_blocking=True)
-        ctx.ddt_topk_logprobs(bufs["draft_logits"], R, bufs["top_lp"], bufs["top_ids"], stream)
-        ctx.ddt_build_tree(bufs["top_lp"], bufs["top_ids"], R, bufs["tree_tokens"],
-                           bufs["parents"], bufs["depths"], bufs["n_nodes"], bufs["mask"], stream)
-        if att_events is not None:
-            att_events[0].record(stream)
-        ctx.ddt_tree_attention(bufs["q"], bufs["k_tree"], bufs["v_tree"], bufs["k_cache"],
-                               bufs["v_cache"], bufs["block_table"], bufs["ctx_lens"],
-                               bufs["mask"], R, bufs["attn_out"], stream)
-        if att_events is not None:
-            att_events[1].record(stream)
-        ctx.ddt_accept(bufs["target_logits"], bufs["tree_tokens"], bufs["parents"],
-                       bufs["n_nodes"], R, bufs["target_argmax"], bufs["acc_len"],
-                       bufs["acc_nodes"], bufs["acc_tokens"], bufs["bonus"], bufs["k_cache"],
-                       bufs["v_cache"], bufs["block_table"], bufs["k_tree"], bufs["v_tree"],
-                       bufs["ctx_lens"], stream)
+        ctx.ddt_round(R, bufs, stream, att_events=att_events)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -292,6 +278,10 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     att_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
+    for a_, b_ in att_ev:  # create the events (the library records them)
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
     e0.record(stream)
     for i in range(args.steps):
         step(att_ev[i])

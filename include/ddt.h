@@ -214,9 +214,18 @@ typedef struct ddt_round_args {
     int32_t *acc_nodes;         /* [R, L] */
     int32_t *acc_tokens;        /* [R, L+1] */
     int32_t *bonus;             /* [R] */
+    /* Optional timing hooks (cudaEvent_t, may be NULL): recorded on the
+     * round's stream immediately before and after the a4 launch. */
+    void *att_event_begin;
+    void *att_event_end;
 } ddt_round_args;
 
-/* a1..a7 chained on one stream with no host synchronisation. */
+/* a1..a7 with no host synchronisation. All work is ordered after what was
+ * already enqueued on `stream`, and everything later on `stream` is ordered
+ * after the whole round. Inside, a1..a3 run on a highest-priority stream of
+ * the context's own and a5 (which needs only the target logits) on a
+ * lowest-priority one, concurrently; a4 waits for both on `stream`, then
+ * a6/a7 follow there. */
 ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *args, void *stream);
 
 /* Wait for the context's device to finish all enqueued work, copy the

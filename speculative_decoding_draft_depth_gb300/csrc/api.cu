@@ -249,6 +249,33 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->att_part_ml = (float2 *)(w + L.att_part_ml);
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
+    // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so
+    // that a5's CTAs only fill what a1..a3 leave idle
+    int prio_least = 0, prio_greatest = 0;
+    e = cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest);
+    if (e == cudaSuccess)
+        e = cudaStreamCreateWithPriority(&ctx->hi, cudaStreamNonBlocking, prio_greatest);
+    if (e == cudaSuccess)
+        e = cudaStreamCreateWithPriority(&ctx->side, cudaStreamNonBlocking, prio_least);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&ctx->ev_tree, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+        if (ctx->ev_tree)
+            cudaEventDestroy(ctx->ev_tree);
+        if (ctx->ev_fork)
+            cudaEventDestroy(ctx->ev_fork);
+        if (ctx->side)
+            cudaStreamDestroy(ctx->side);
+        if (ctx->hi)
+            cudaStreamDestroy(ctx->hi);
+        cudaFree(ctx->ws);
+        free(ctx);
+        return cuda_fail(e);
+    }
     *out = ctx;
     return DDT_OK;
 }
@@ -260,6 +287,13 @@ void ddt_destroy(ddt_ctx *ctx)
     int cur = -1;
     cudaGetDevice(&cur);
     cudaSetDevice(ctx->device);
+    cudaStreamSynchronize(ctx->side);
+    cudaStreamSynchronize(ctx->hi);
+    cudaEventDestroy(ctx->ev_join);
+    cudaEventDestroy(ctx->ev_tree);
+    cudaEventDestroy(ctx->ev_fork);
+    cudaStreamDestroy(ctx->side);
+    cudaStreamDestroy(ctx->hi);
     cudaFree(ctx->ws);
     if (cur >= 0)
         cudaSetDevice(cur);
@@ -449,12 +483,25 @@ ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *a, void *stream)
     if ((st = set_device(ctx)) != DDT_OK)
         return st;
     cudaStream_t s = (cudaStream_t)stream;
-    DDT_TRY(launch_topk(ctx, a->draft_logits, R, a->top_lp, a->top_ids, s));
+    // a1..a3 on the highest-priority stream, a5 on the lowest beside them (the
+    // tree kernel leaves most SMs idle); both join `s` before a4
+    DDT_TRY(cudaEventRecord(ctx->ev_fork, s));
+    DDT_TRY(cudaStreamWaitEvent(ctx->hi, ctx->ev_fork, 0));
+    DDT_TRY(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
+    DDT_TRY(launch_topk(ctx, a->draft_logits, R, a->top_lp, a->top_ids, ctx->hi));
+    DDT_TRY(launch_argmax_partials(ctx, a->target_logits, R, ctx->side));
+    DDT_TRY(cudaEventRecord(ctx->ev_join, ctx->side));
     DDT_TRY(launch_build_tree(ctx, a->top_lp, a->top_ids, R, a->tree_tokens, a->parents,
-                              a->depths, a->n_nodes, a->mask, s));
+                              a->depths, a->n_nodes, a->mask, ctx->hi));
+    DDT_TRY(cudaEventRecord(ctx->ev_tree, ctx->hi));
+    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_tree, 0));
+    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_join, 0));
+    if (a->att_event_begin)
+        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_begin, s));
     DDT_TRY(launch_attention(ctx, a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache,
                              a->block_table, a->ctx_lens, a->mask, R, a->attn_out, s));
-    DDT_TRY(launch_argmax_partials(ctx, a->target_logits, R, s));
+    if (a->att_event_end)
+        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_end, s));
     DDT_TRY(launch_walk_compact(ctx, nullptr, true, a->target_argmax, a->tree_tokens, a->parents,
                                 a->n_nodes, R, a->acc_len, a->acc_nodes, a->acc_tokens, a->bonus,
                                 true, true, a->k_cache, a->v_cache, a->block_table, a->ctx_lens,

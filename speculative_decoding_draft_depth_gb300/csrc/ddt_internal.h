@@ -36,6 +36,9 @@ struct ddt_ctx {
     int num_sms;
     size_t ws_bytes;
     char *ws;                // one allocation, carved below
+    cudaStream_t hi;         // ddt_round: a1..a3 on a highest-priority stream,
+    cudaStream_t side;       //   a5 beside them on a lowest-priority one
+    cudaEvent_t ev_fork, ev_tree, ev_join;
     int32_t *status;         // device status word
     // a1 partials
     int tk_nch;              // chunks per row

@@ -497,12 +497,15 @@ DDT_DEVINL uint64_t shfl_xor64(uint64_t v, int m)
     return ((uint64_t)hi << 32) | lo;
 }
 
+constexpr int MERGE_LISTS = 16;  // chunk lists a warp stages in shared memory
+
 __global__ void __launch_bounds__(256)
 topk_merge_kernel(const float *__restrict__ part_val, const int32_t *__restrict__ part_idx,
                   const float2 *__restrict__ part_ms, int rows, int nch, int K,
                   float *__restrict__ top_lp, int32_t *__restrict__ top_ids,
                   int32_t *__restrict__ status)
 {
+    __shared__ uint64_t s_merge[8 * MERGE_LISTS * 32];
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
     if (row >= rows)
@@ -532,11 +535,18 @@ topk_merge_kernel(const float *__restrict__ part_val, const int32_t *__restrict_
     float *olp = top_lp + (int64_t)row * K;
     int32_t *oid = top_ids + (int64_t)row * K;
 
-    if (K <= 32) {
-        uint64_t cur = (lane < K) ? make_key(rv[lane], ri[lane]) : 0ull;
+    if (K <= 32 && nch <= MERGE_LISTS) {
+        // the row's lists into shared memory first (one round of loads), then
+        // absorb them one by one
+        uint64_t *sk = s_merge + (threadIdx.x >> 5) * MERGE_LISTS * 32;
+        for (int i = lane; i < nch * 32; i += 32) {
+            const int b = i >> 5, e = i & 31;
+            sk[i] = (e < K) ? make_key(rv[b * K + e], ri[b * K + e]) : 0ull;
+        }
+        __syncwarp();
+        uint64_t cur = sk[lane];
         for (int b = 1; b < nch; ++b) {
-            const int src = 31 - lane;  // the list reversed: ascending
-            const uint64_t o = (src < K) ? make_key(rv[b * K + src], ri[b * K + src]) : 0ull;
+            const uint64_t o = sk[b * 32 + 31 - lane];  // the list reversed: ascending
             cur = cur > o ? cur : o;
 #pragma unroll
             for (int j = 16; j > 0; j >>= 1) {

@@ -4,9 +4,11 @@
 // by rank tuples, pop the most probable, push its sibling (.., rho_d + 1)
 // and child (.., rho_d, 0)) and "SparklingTree ...", Step 3 (the heap loop
 // with its node numbering, parents and depths). One warp per request:
-//  * The frontier (at most B entries) lives in registers, 4 slots per lane.
-//    A pop is a warp-wide arg-best by xor-shuffles over (S, rank tuple):
-//    larger S first, equal S to the lexicographically smaller tuple.
+//  * The frontier (at most B + 1 entries) lives in registers, 4 slots per
+//    lane. A pop is a warp-wide arg-best over (S, rank tuple): larger S
+//    first, equal S to the lexicographically smaller tuple. S is compared as
+//    an order-preserving 64-bit integer key, by two 32-bit warp max
+//    reductions; the tuple's four words are reduced only when scores tie.
 //  * S is fp64: parent's S plus the entry's own fp32 log-prob, the same
 //    additions in the same order on every machine.
 //  * A rank tuple packs (rank + 1) into 7-bit fields, most significant
@@ -44,15 +46,29 @@ DDT_DEVINL void field_clear(uint64_t &hi, uint64_t &lo, int i)
     lo &= ~ml;
 }
 
-// does (Sa, ha, la) pop before (Sb, hb, lb)?
-DDT_DEVINL bool pops_before(double Sa, uint64_t ha, uint64_t la, double Sb, uint64_t hb,
+// order-preserving map of a (non-NaN) double to uint64; never 0 for a real value
+DDT_DEVINL uint64_t skey(double x)
+{
+    const uint64_t b = (uint64_t)__double_as_longlong(x + 0.0);
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+DDT_DEVINL double skey_inv(uint64_t k)
+{
+    return __longlong_as_double((long long)((k >> 63) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k));
+}
+
+// does (ka, ha, la) pop before (kb, hb, lb)? larger score key, then smaller tuple
+DDT_DEVINL bool pops_before(uint64_t ka, uint64_t ha, uint64_t la, uint64_t kb, uint64_t hb,
                             uint64_t lb)
 {
-    if (Sa != Sb)
-        return Sa > Sb;
-    if (ha != hb)
-        return ha < hb;
-    return la < lb;
+    return ka > kb || (ka == kb && (ha < hb || (ha == hb && la < lb)));
+}
+
+// the lanes whose value v is the warp maximum, among the lanes in cand
+DDT_DEVINL unsigned keep_max(unsigned cand, uint32_t v, int lane)
+{
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, ((cand >> lane) & 1u) ? v : 0u);
+    return cand & __ballot_sync(0xFFFFFFFFu, v == m);
 }
 
 __global__ void __launch_bounds__(32)
@@ -81,75 +97,61 @@ build_tree_kernel(const float *__restrict__ top_lp, const int32_t *__restrict__ 
     }
     __syncwarp();
 
-    // frontier slots (registers)
-    double S[SLOTS], pS[SLOTS];
-    uint64_t kh[SLOTS], kl[SLOTS];
+    // frontier slots (registers): score key (S = skey_inv(sk)), the parent's score
+    // key, rank tuple, parent node, depth and rank of the entry's last field; an
+    // empty slot has key 0
+    uint64_t sk[SLOTS], pk[SLOTS], kh[SLOTS], kl[SLOTS];
     int par[SLOTS], dep[SLOTS], rnk[SLOTS];
-    unsigned valid = 0;
 #pragma unroll
     for (int f = 0; f < SLOTS; ++f) {
-        S[f] = pS[f] = 0.0;
-        kh[f] = kl[f] = 0;
+        sk[f] = pk[f] = kh[f] = kl[f] = 0;
         par[f] = dep[f] = rnk[f] = 0;
     }
     if (lane == 0) {  // the single first entry: rank tuple (0,)
-        valid = 1u;
-        pS[0] = 0.0;
-        S[0] = 0.0 + (double)s_lp[0];
+        pk[0] = skey(0.0);
+        sk[0] = skey(0.0 + (double)s_lp[0]);
         field_or(kh[0], kl[0], 0, 1);
-        par[0] = 0;
         dep[0] = 1;
-        rnk[0] = 0;
     }
 
     int count = 0;
     while (count < B) {
         // lane-local best slot
-        int bf = -1;
-        double bS = -__builtin_huge_val();
-        uint64_t bh = ~0ull, bl = ~0ull;
-#pragma unroll
-        for (int f = 0; f < SLOTS; ++f)
-            if (((valid >> f) & 1u) && (bf < 0 || pops_before(S[f], kh[f], kl[f], bS, bh, bl))) {
-                bf = f;
-                bS = S[f];
-                bh = kh[f];
-                bl = kl[f];
-            }
-        int who = (bf < 0) ? -1 : (lane * SLOTS + bf);
-        // warp arg-best
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const double oS = __shfl_xor_sync(0xFFFFFFFFu, bS, off);
-            const uint64_t oh = __shfl_xor_sync(0xFFFFFFFFu, bh, off);
-            const uint64_t ol = __shfl_xor_sync(0xFFFFFFFFu, bl, off);
-            const int ow = __shfl_xor_sync(0xFFFFFFFFu, who, off);
-            const bool take = (ow >= 0) && (who < 0 || pops_before(oS, oh, ol, bS, bh, bl));
-            if (take) {
-                bS = oS;
-                bh = oh;
-                bl = ol;
-                who = ow;
-            }
-        }
-        if (who < 0)
-            break;  // the whole prefix space is smaller than B
-        const int wl = who / SLOTS, wf = who % SLOTS;
-        // broadcast the winner's remaining fields
-        double mypS = pS[0];
-        int mypar = par[0], mydep = dep[0], myrnk = rnk[0];
+        int bf = 0;
+        uint64_t bk = sk[0], bh = kh[0], bl = kl[0];
+        int bpar = par[0], bdep = dep[0], brnk = rnk[0];
 #pragma unroll
         for (int f = 1; f < SLOTS; ++f)
-            if (wf == f) {
-                mypS = pS[f];
-                mypar = par[f];
-                mydep = dep[f];
-                myrnk = rnk[f];
+            if (pops_before(sk[f], kh[f], kl[f], bk, bh, bl)) {
+                bf = f;
+                bk = sk[f];
+                bh = kh[f];
+                bl = kl[f];
+                bpar = par[f];
+                bdep = dep[f];
+                brnk = rnk[f];
             }
-        const double wpS = __shfl_sync(0xFFFFFFFFu, mypS, wl);
-        const int wpar = __shfl_sync(0xFFFFFFFFu, mypar, wl);
-        const int wdep = __shfl_sync(0xFFFFFFFFu, mydep, wl);
-        const int wrnk = __shfl_sync(0xFFFFFFFFu, myrnk, wl);
+        // warp arg-best: score key high then low word; the rank tuple only on a tie
+        unsigned cand = __ballot_sync(0xFFFFFFFFu, bk != 0);
+        if (cand == 0u)
+            break;  // the whole prefix space is smaller than B
+        cand = keep_max(cand, (uint32_t)(bk >> 32), lane);
+        cand = keep_max(cand, (uint32_t)bk, lane);
+        if (__popc(cand) > 1) {
+            cand = keep_max(cand, ~(uint32_t)(bh >> 32), lane);
+            cand = keep_max(cand, ~(uint32_t)bh, lane);
+            cand = keep_max(cand, ~(uint32_t)(bl >> 32), lane);
+            cand = keep_max(cand, ~(uint32_t)bl, lane);
+        }
+        const int wl = __ffs(cand) - 1;
+        // the winner's fields, to every lane
+        const uint64_t wk = __shfl_sync(0xFFFFFFFFu, bk, wl);
+        const uint64_t wh = __shfl_sync(0xFFFFFFFFu, bh, wl);
+        const uint64_t wlo = __shfl_sync(0xFFFFFFFFu, bl, wl);
+        const int wpar = __shfl_sync(0xFFFFFFFFu, bpar, wl);
+        const int wdep = __shfl_sync(0xFFFFFFFFu, bdep, wl);
+        const int wrnk = __shfl_sync(0xFFFFFFFFu, brnk, wl);
+        const double wS = skey_inv(wk);
 
         const int node = count + 1;
         if (lane == 0) {
@@ -158,31 +160,30 @@ build_tree_kernel(const float *__restrict__ top_lp, const int32_t *__restrict__ 
             s_dep[node] = wdep;
         }
         ++count;
-        if (lane == wl)
-            valid &= ~(1u << wf);
         if (count == B)
             break;
-
-        // sibling (.., rho_d + 1) takes the freed slot
-        if (wrnk + 1 < K && lane == wl) {
+        // the popped entry's slot: freed, or reused by its sibling (.., rho_d + 1),
+        // whose score is its parent's score plus the next rank's log-prob
+        if (lane == wl) {
 #pragma unroll
             for (int f = 0; f < SLOTS; ++f)
-                if (f == wf) {
-                    S[f] = wpS + (double)s_lp[(wdep - 1) * K + wrnk + 1];
-                    pS[f] = wpS;
-                    kh[f] = bh;
-                    kl[f] = bl;
-                    field_clear(kh[f], kl[f], wdep - 1);
-                    field_or(kh[f], kl[f], wdep - 1, (uint64_t)(wrnk + 2));
-                    par[f] = wpar;
-                    dep[f] = wdep;
-                    rnk[f] = wrnk + 1;
-                    valid |= 1u << f;
+                if (f == bf) {
+                    if (wrnk + 1 < K) {
+                        sk[f] = skey(skey_inv(pk[f]) + (double)s_lp[(wdep - 1) * K + wrnk + 1]);
+                        field_clear(kh[f], kl[f], wdep - 1);
+                        field_or(kh[f], kl[f], wdep - 1, (uint64_t)(wrnk + 2));
+                        rnk[f] = wrnk + 1;
+                    } else {
+                        sk[f] = 0;
+                    }
                 }
         }
         // child (.., rho_d, 0) goes to the lowest lane with a free slot
         if (wdep < L) {
-            const unsigned freeslots = (~valid) & ((1u << SLOTS) - 1u);
+            unsigned freeslots = 0;
+#pragma unroll
+            for (int f = 0; f < SLOTS; ++f)
+                freeslots |= (sk[f] == 0) ? (1u << f) : 0u;
             const unsigned lanes = __ballot_sync(0xFFFFFFFFu, freeslots != 0u);
             const int tl = __ffs(lanes) - 1;
             if (lane == tl) {
@@ -190,15 +191,14 @@ build_tree_kernel(const float *__restrict__ top_lp, const int32_t *__restrict__ 
 #pragma unroll
                 for (int f = 0; f < SLOTS; ++f)
                     if (f == f0) {
-                        S[f] = bS + (double)s_lp[wdep * K + 0];
-                        pS[f] = bS;
-                        kh[f] = bh;
-                        kl[f] = bl;
+                        sk[f] = skey(wS + (double)s_lp[wdep * K + 0]);
+                        pk[f] = wk;
+                        kh[f] = wh;
+                        kl[f] = wlo;
                         field_or(kh[f], kl[f], wdep, 1ull);
                         par[f] = node;
                         dep[f] = wdep + 1;
                         rnk[f] = 0;
-                        valid |= 1u << f;
                     }
             }
         }

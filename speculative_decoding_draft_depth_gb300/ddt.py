@@ -50,7 +50,7 @@ class RoundArgs(ctypes.Structure):
         "draft_logits", "target_logits", "q", "k_tree", "v_tree", "k_cache", "v_cache",
         "block_table", "ctx_lens", "top_lp", "top_ids", "tree_tokens", "parents", "depths",
         "n_nodes", "mask", "attn_out", "target_argmax", "acc_len", "acc_nodes", "acc_tokens",
-        "bonus")]
+        "bonus", "att_event_begin", "att_event_end")]
 
 
 _lib = None
@@ -192,12 +192,20 @@ class Context:
                                _ptr(block_table), _ptr(k_tree), _ptr(v_tree), _ptr(ctx_lens),
                                _stream(stream)), "ddt_accept")
 
-    def ddt_round(self, R, bufs, stream=None):
-        """bufs: dict of tensors named like the fields of ddt_round_args."""
+    def ddt_round(self, R, bufs, stream=None, att_events=None):
+        """bufs: dict of tensors named like the fields of ddt_round_args.
+        att_events: optional (begin, end) torch.cuda.Event pair, recorded by
+        the library around the attention launch (each already created, e.g.
+        by one earlier record())."""
         a = RoundArgs()
         a.R = R
         for name, _ in RoundArgs._fields_[1:]:
+            if name.startswith("att_event"):
+                continue
             setattr(a, name, _ptr(bufs.get(name)))
+        if att_events is not None:
+            a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
+            a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
         _check(_lib.ddt_round(self._h, ctypes.byref(a), _stream(stream)), "ddt_round")
 
     def ddt_device_status(self):
