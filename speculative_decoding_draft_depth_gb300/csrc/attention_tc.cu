@@ -14,7 +14,7 @@
 // ctx_lens (no plan kernel), and the Hkv CTAs of a group read the same
 // tokens' cache rows at about the same time. A pair cut by a share boundary
 // leaves per-CTA partials (two slots per CTA: its first and its last
-// segment), combined by whichever of its CTAs finishes last.
+// segment), combined after the main kernel by att_combine_kernel.
 //
 // Inside a CTA (one per SM), for one item:
 //  * main rows: 128 query rows = 128/G positions x G heads (row = pos*G+h);
@@ -56,7 +56,6 @@ namespace {
 constexpr int TILE = 128;
 constexpr int NMAIN = 512;                // main-row softmax threads (warps 0-15)
 constexpr int NTAILT = 128;               // tail-row softmax threads (warps 16-19)
-constexpr int NSOFT = NMAIN + NTAILT;
 constexpr int W_TAIL0 = 16, W_KPROD = 20, W_VPROD = 21, W_MMA = 22;
 constexpr int NTHREADS = 23 * 32;
 constexpr int NRING = 4;                  // ring of segments handed from the walker to the other roles
@@ -96,8 +95,7 @@ constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16, B_KFULL = 32, B_KEMPTY = 48, B_VF
                    B_TBAR = 312,    // [2] tail column-max exchange (128 arrivals)
                    B_LBAR = 328,    // [4 lane quarters] row-sum exchange (128 arrivals)
                    B_TLBAR = 360,   // tail-sum exchange (128 arrivals)
-                   B_IBAR = 368,    // all softmax threads, split-item combine (640 arrivals)
-                   B_TMEM = 376, B_ABORT = 380, B_LAST = 384,
+                   B_TMEM = 376, B_ABORT = 380,
                    B_RING = 400,    // [NRING][4] ints: segments (x = -1: end of the share)
                    B_TOTAL = 464,   // int: T, the batch's total tiles
                    B_RED = 512,     // 2 x [4 warps][16] floats: tail column max
@@ -117,7 +115,6 @@ struct TcArgs {
     float *out;
     float *part_o;
     float2 *part_ml;
-    unsigned *rg_cnt;
     int32_t *status;
     int R, P, Hq, Hkv, G, g_shift, W, page_shift, max_pages, RG, n_main, tail_rows, max_ctx;
     int64_t num_pages;
@@ -304,75 +301,6 @@ DDT_DEVINL float exps32(const uint32_t *sv, float scale, float m, uint32_t *pw)
     return (r0 + r1) + (r2 + r3);
 }
 
-// a finished split segment: all softmax threads publish their partials; the CTA
-// that arrives last for its pair combines every segment's into the output
-DDT_DEVINL void split_combine(const TcArgs &a, const Item &it, unsigned char *sgen, uint32_t bar,
-                              int &ib, volatile int *abort_flag, int tid, int PG)
-{
-    __threadfence();
-    if (!gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status))
-        return;
-    const long long T = *reinterpret_cast<volatile int *>(sgen + SM_BAR + B_TOTAL);
-    const int NG = gridDim.x / a.Hkv;
-    const long long ps = it.ps, pe = ps + pair_tiles(a, it.r);
-    const int c0 = share_of(ps, T, NG), c1 = share_of(pe - 1, T, NG);
-    int *s_last = reinterpret_cast<int *>(sgen + SM_BAR + B_LAST);
-    int *slots = reinterpret_cast<int *>(sgen + SM_BAR + B_XMAX + 2048);  // [<= 512]
-    const int pair = (it.r * a.Hkv + it.g) * a.RG + it.rg;
-    if (tid == 0) {
-        int ns = 0;  // groups with a segment of this pair (shares can be empty when T < NG)
-        for (int c = c0; c <= c1; ++c)
-            if (share_start(T, c, NG) < share_start(T, c + 1, NG))
-                slots[ns++] = part_slot(ps, T, c, NG, it.g, a.Hkv);
-        s_last[1] = ns;
-        s_last[0] = (atomicAdd(&a.rg_cnt[pair], 1u) == (unsigned)(ns - 1));
-    }
-    if (!gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status))
-        return;
-    if (*reinterpret_cast<volatile int *>(s_last) == 0)
-        return;
-    __threadfence();
-    const int ns = *reinterpret_cast<volatile int *>(s_last + 1);
-    const int nrows = TILE + (it.has_tail ? a.tail_rows : 0);
-    // pass 1: per row, the common reference and the total weight
-    float2 *fac = reinterpret_cast<float2 *>(sgen + SM_BAR + B_XMAX);  // [nrows] (M, 1/L)
-    if (tid < nrows) {
-        float M = DDT_NEG_INF;
-        for (int s = 0; s < ns; ++s)
-            M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)slots[s] * ATT_ROWS + tid]).x);
-        const float base = (M == DDT_NEG_INF) ? 0.f : M;
-        float Ls = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float2 ml = __ldcg(&a.part_ml[(int64_t)slots[s] * ATT_ROWS + tid]);
-            Ls += (ml.x == DDT_NEG_INF) ? 0.f : ml.y * ex2(ml.x - base);
-        }
-        fac[tid] = make_float2(base, Ls > 0.f ? 1.f / Ls : 0.f);
-    }
-    if (!gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status))
-        return;
-    // pass 2: every (row, d) element
-    const int d = tid & 127;
-    for (int rho = tid >> 7; rho < nrows; rho += NSOFT / 128) {
-        const int gr2 = (rho < TILE) ? it.rg * TILE + rho : a.n_main * TILE + (rho - TILE);
-        if (gr2 >= PG)
-            continue;
-        const float2 f = fac[rho];
-        float x = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const int64_t ir = (int64_t)slots[s] * ATT_ROWS + rho;
-            const float m = __ldcg(&a.part_ml[ir]).x;
-            if (m != DDT_NEG_INF)
-                x += __ldcg(&a.part_o[ir * 128 + d]) * ex2(m - f.x);
-        }
-        const int i2 = gr2 >> a.g_shift, h2 = gr2 & (a.G - 1);
-        a.out[(((int64_t)it.r * a.P + i2) * a.Hq + it.g * a.G + h2) * 128 + d] = x * f.y;
-    }
-    if (tid == 0)
-        a.rg_cnt[pair] = 0u;
-    // the fac and slot scratch is reused by the next segment's row-max exchange
-    gsync(bar + B_IBAR, ib++ & 1, abort_flag, a.status);
-}
-
 template <int TQ>
 __global__ void __launch_bounds__(NTHREADS, 1)
 att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qt,
@@ -412,7 +340,6 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int i = 0; i < 4; ++i)
             mbar_init(bar + B_LBAR + 8 * i, 128);
         mbar_init(bar + B_TLBAR, NTAILT);
-        mbar_init(bar + B_IBAR, NSOFT);
         mbar_init(bar + B_ODONE, 1);
         mbar_init(bar + B_OTDONE, 1);
         mbar_init(bar + B_FINAL, 1);
@@ -744,7 +671,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t col0 = 32u * cq;
         float *xmax = reinterpret_cast<float *>(sgen + SM_BAR + B_XMAX);
         float *xl = reinterpret_cast<float *>(sgen + SM_BAR + B_XL);
-        int n = 0, ib = 0;
+        int n = 0;
         bool alive = true;
         for (int k = 0; alive; ++k) {
             Item it;
@@ -907,29 +834,23 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!single && cq == 0)
                 a.part_ml[item_row0 + row] = make_float2(m_used, lrow);
             tc_fence_before();
-            if (!single)
-                split_combine(a, it, sgen, bar, ib, abort_flag, tid, PG);
         }
     } else {
         // ============================================================ tail-row softmax
         const int tq = warp - W_TAIL0;       // lane quarter
         const int row = tq * 32 + lane;      // TMEM lane = tail token (S_t^T) = head-dim index (O_t^T)
-        const int ttid = tid - NMAIN;        // 0..127
         const uint32_t lane_addr = (uint32_t)(tq * 32) << 16;
         float *red = reinterpret_cast<float *>(sgen + SM_BAR + B_RED);
         float *sums = reinterpret_cast<float *>(sgen + SM_BAR + B_SUM);
-        int nt = 0, tail_items = 0, ib = 0;
+        int nt = 0, tail_items = 0;
         bool alive = true;
         for (int k = 0; alive; ++k) {
             Item it;
             if (!ring_get(a, bar, ring, k, lane, abort_flag, it))
                 break;
             const int tail = it.has_tail ? a.tail_rows : 0;
-            if (tail == 0) {
-                if (!it.single)
-                    split_combine(a, it, sgen, bar, ib, abort_flag, ttid + NMAIN, PG);
+            if (tail == 0)
                 continue;
-            }
             const int tail_pos0 = a.n_main * pos_per_main;
             uint32_t tail_bits = 0;  // bit q: this thread's tree position is visible to tail row q
             if (it.last && row < a.P)
@@ -1071,8 +992,6 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             tc_fence_before();
-            if (!single)
-                split_combine(a, it, sgen, bar, ib, abort_flag, ttid + NMAIN, PG);
         }
     }
 
@@ -1081,6 +1000,149 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (warp == W_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+
+// ---------------------------------------------------------------- split combine
+// After the main kernel: one CTA per (share boundary, KV head). A boundary
+// that falls inside a (request, row group) run of tiles split that run; the
+// CTA of the first such boundary combines the run's partials (one per share
+// that holds a segment of it) into the output rows.
+constexpr int CB_THREADS = 512;
+constexpr int CB_SEGS = 16;  // segment weights held per combine pass
+
+__global__ void __launch_bounds__(CB_THREADS)
+att_combine_kernel(const TcArgs a, int NG)
+{
+    __shared__ float s_fac[CB_SEGS * ATT_ROWS];
+    __shared__ int s_slots[512];
+    __shared__ long long s_ps, s_T;
+    __shared__ int s_r, s_rg, s_go, s_ns;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int bnd = blockIdx.x / a.Hkv + 1, g = blockIdx.x % a.Hkv;
+    if (tid < 32) {
+        // T, and the run holding the boundary's first tile
+        const int per_lane = (a.R + 31) / 32;
+        long long mine = 0;
+        for (int i = 0; i < per_lane; ++i) {
+            const int r = lane * per_lane + i;
+            if (r < a.R)
+                mine += (long long)pair_tiles(a, r) * a.RG;
+        }
+        long long incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        const long long T = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const long long t = share_start(T, bnd, NG), excl = incl - mine;
+        const unsigned holder = __ballot_sync(0xFFFFFFFFu, t < T && excl <= t && t < excl + mine);
+        if (tid == 0)
+            s_go = 0;
+        if (holder != 0 && lane == __ffs(holder) - 1) {
+            long long acc = excl;
+            for (int i = 0; i < per_lane; ++i) {
+                const int r = lane * per_lane + i;
+                const long long tp = pair_tiles(a, r), span = tp * a.RG;
+                if (t < acc + span) {
+                    const int rg = (int)((t - acc) / tp);
+                    const long long ps = acc + rg * tp;
+                    s_r = r;
+                    s_rg = rg;
+                    s_ps = ps;
+                    s_T = T;
+                    // cut inside the run, and the first boundary that cuts it
+                    s_go = (t > ps && bnd == share_of(ps, T, NG) + 1) ? 1 : 0;
+                    break;
+                }
+                acc += span;
+            }
+        }
+    }
+    __syncthreads();
+    if (!s_go)
+        return;
+    const long long T = s_T, ps = s_ps, pe = ps + pair_tiles(a, s_r);
+    const int r = s_r, rg = s_rg;
+    if (tid == 0) {
+        const int c0 = share_of(ps, T, NG), c1 = share_of(pe - 1, T, NG);
+        int ns = 0;
+        for (int c = c0; c <= c1; ++c)
+            if (share_start(T, c, NG) < share_start(T, c + 1, NG))
+                s_slots[ns++] = part_slot(ps, T, c, NG, g, a.Hkv);
+        s_ns = ns;
+    }
+    __syncthreads();
+    const int ns = s_ns;
+    const int PG = a.P * a.G;
+    const int nrows = TILE + ((rg == 0 && a.tail_rows > 0) ? a.tail_rows : 0);
+    for (int s0 = 0; s0 < ns; s0 += CB_SEGS) {
+        const int sn = min(CB_SEGS, ns - s0);
+        // per row: every segment's weight exp2(m_s - M) / L
+        if (tid < nrows) {
+            float M = DDT_NEG_INF;
+            for (int s = 0; s < ns; ++s)
+                M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]).x);
+            float Ls = 0.f;
+            for (int s = 0; s < ns; ++s) {
+                const float2 ml = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]);
+                Ls += (ml.x == DDT_NEG_INF) ? 0.f : ml.y * ex2(ml.x - M);
+            }
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            for (int s = 0; s < sn; ++s) {
+                const float m = __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + tid]).x;
+                s_fac[s * ATT_ROWS + tid] = (m == DDT_NEG_INF) ? 0.f : ex2(m - M) * inv;
+            }
+        }
+        __syncthreads();
+        // every (row, 4 columns): independent float4 loads, several in flight
+        constexpr int PER = (ATT_ROWS * 32 + CB_THREADS - 1) / CB_THREADS;
+        float4 acc[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u)
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s = 0; s < sn; ++s) {
+            const float4 *po =
+                reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slots[s0 + s] * ATT_ROWS * 128);
+#pragma unroll
+            for (int u = 0; u < PER; ++u) {
+                const int e = tid + u * CB_THREADS, rho = e >> 5;
+                if (rho < nrows) {
+                    const float f = s_fac[s * ATT_ROWS + rho];
+                    const float4 v = __ldcg(po + e);
+                    acc[u].x += v.x * f;
+                    acc[u].y += v.y * f;
+                    acc[u].z += v.z * f;
+                    acc[u].w += v.w * f;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = tid + u * CB_THREADS, rho = e >> 5, d4 = (e & 31) * 4;
+            if (rho >= nrows)
+                continue;
+            const int gr2 = (rho < TILE) ? rg * TILE + rho : a.n_main * TILE + (rho - TILE);
+            if (gr2 >= PG)
+                continue;
+            const int i2 = gr2 >> a.g_shift, h2 = gr2 & (a.G - 1);
+            float4 *dst = reinterpret_cast<float4 *>(
+                a.out + (((int64_t)r * a.P + i2) * a.Hq + g * a.G + h2) * 128 + d4);
+            if (s0 == 0) {
+                *dst = acc[u];
+            } else {
+                float4 o = *dst;
+                o.x += acc[u].x;
+                o.y += acc[u].y;
+                o.z += acc[u].z;
+                o.w += acc[u].w;
+                *dst = o;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -1197,7 +1259,6 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     a.out = out;
     a.part_o = c->att_part_o;
     a.part_ml = c->att_part_ml;
-    a.rg_cnt = c->att_rg_cnt;
     a.status = c->status;
     a.R = R;
     a.max_ctx = cfg.max_pages_per_req * cfg.page_size;
@@ -1225,7 +1286,10 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     while (groups > 1 && groups * cfg.Hkv * 2 > c->att_max_items)
         --groups;
     const int grid = groups * cfg.Hkv;
-    if (tail <= 4)
-        return launch_tq<4>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
-    return launch_tq<16>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
+    cudaError_t e = (tail <= 4) ? launch_tq<4>(grid, tq, tqt, tk, tv, tkt, tvt, a, s)
+                                : launch_tq<16>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
+    if (e != cudaSuccess || groups == 1)
+        return e;
+    att_combine_kernel<<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
+    return cudaGetLastError();
 }
