@@ -26,9 +26,10 @@
 //  * the softmax writes P (bf16) back over its own S columns in TMEM and the
 //    P V product reads its A operand straight from TMEM, so P never touches
 //    shared memory and a tile's softmax does not wait for the previous P V.
-//  * K and V tiles of 128 tokens arrive by TMA in two 2-deep rings, one box
-//    per 16-token page run and d-half (16 rows of 128 B, 128-byte swizzle),
-//    issued by 8 lanes of the loader warp at once; Q is double-buffered.
+//  * K and V tiles of 128 tokens arrive by TMA in a 2-deep K ring and a
+//    3-deep V ring (a V slot frees only after its P V), one box per 16-token
+//    page run and d-half (16 rows of 128 B, 128-byte swizzle), issued by 8
+//    lanes of the loader warp at once.
 //  * warps 0-15: main-row softmax and epilogue, four warps per TMEM lane
 //    quarter, each on 32 of the 128 columns; warps 16-19: tail-row softmax;
 //    warp 20: walks the CTA's share and loads Q and K; warp 21: V loads; warp 22: TMEM
@@ -70,11 +71,14 @@ constexpr long long WAIT_LIMIT = 4000000000LL;   // cycles (about 2 s)
 constexpr long long DRAIN_LIMIT = 200000000LL;   // cycles, for the wind-down waits
 
 // shared memory (offsets from a 1024-byte aligned base)
+constexpr int NQ = 1;                          // Q slots
+constexpr int NKS = 2;                         // K ring stages
+constexpr int NVS = 3;                         // V ring stages
 constexpr uint32_t QSLOT = 36864;              // main 2 x 16 KB d-halves + tail 2 x 2 KB
-constexpr uint32_t SM_Q = 0;                   // 2 slots
-constexpr uint32_t SM_K = SM_Q + 2 * QSLOT;    // 2 slots x 32 KB (2 x 16 KB d-halves)
-constexpr uint32_t SM_V = SM_K + 65536;        // 2 slots x 32 KB
-constexpr uint32_t SM_PT = SM_V + 65536;       // 2 buffers x (2 x 2 KB token halves of P_t^T)
+constexpr uint32_t SM_Q = 0;                   // NQ slots
+constexpr uint32_t SM_K = SM_Q + NQ * QSLOT;   // NKS slots x 32 KB (2 x 16 KB d-halves)
+constexpr uint32_t SM_V = SM_K + NKS * 32768;  // NVS slots x 32 KB
+constexpr uint32_t SM_PT = SM_V + NVS * 32768; // 2 buffers x (2 x 2 KB token halves of P_t^T)
 constexpr uint32_t SM_BAR = SM_PT + 8192;
 constexpr uint32_t SM_TOTAL = SM_BAR + 10240;
 constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
@@ -83,21 +87,25 @@ constexpr uint32_t SM_ALLOC = SM_TOTAL + 1024;
 // Two-slot barriers ([2], indexed by tile parity) are the ones whose producer can
 // run a full tile ahead of the consumer; a single barrier would then complete two
 // phases before the consumer looks, and a parity wait cannot tell them apart.
-constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16, B_KFULL = 32, B_KEMPTY = 48, B_VFULL = 64,
-                   B_VEMPTY = 80, B_SFULL = 96, B_STFULL = 112,
-                   B_PFULL = 128,   // [2] main P of a tile in TMEM (512 arrivals)
-                   B_ODONE = 144,
-                   B_PTFULL = 152,  // [2] tail P of a tail tile in shared memory (128 arrivals)
-                   B_OTDONE = 168, B_FINAL = 176,
-                   B_RFULL = 184,   // [NRING] item ring entry written
-                   B_REMPTY = 216,  // [NRING] item ring entry read by every consumer
-                   B_XBAR = 248,    // [4 lane quarters][2] row-max exchange (128 arrivals)
-                   B_TBAR = 312,    // [2] tail column-max exchange (128 arrivals)
-                   B_LBAR = 328,    // [4 lane quarters] row-sum exchange (128 arrivals)
-                   B_TLBAR = 360,   // tail-sum exchange (128 arrivals)
-                   B_TMEM = 376, B_ABORT = 380,
-                   B_RING = 400,    // [NRING][4] ints: segments (x = -1: end of the share)
-                   B_TOTAL = 464,   // int: T, the batch's total tiles
+constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16,
+                   B_KFULL = 32,    // [NKS <= 3]
+                   B_KEMPTY = 56,   // [NKS <= 3]
+                   B_VFULL = 80,    // [NVS <= 3]
+                   B_VEMPTY = 104,  // [NVS <= 3]
+                   B_SFULL = 128, B_STFULL = 144,
+                   B_PFULL = 160,   // [2] main P of a tile in TMEM (512 arrivals)
+                   B_ODONE = 176,
+                   B_PTFULL = 184,  // [2] tail P of a tail tile in shared memory (128 arrivals)
+                   B_OTDONE = 200, B_FINAL = 208,
+                   B_RFULL = 216,   // [NRING] item ring entry written
+                   B_REMPTY = 248,  // [NRING] item ring entry read by every consumer
+                   B_XBAR = 280,    // [4 lane quarters][2] row-max exchange (128 arrivals)
+                   B_TBAR = 344,    // [2] tail column-max exchange (128 arrivals)
+                   B_LBAR = 360,    // [4 lane quarters] row-sum exchange (128 arrivals)
+                   B_TLBAR = 392,   // tail-sum exchange (128 arrivals)
+                   B_TMEM = 400, B_ABORT = 404,
+                   B_RING = 416,    // [NRING][4] ints: segments (x = -1: end of the share)
+                   B_TOTAL = 480,   // int: T, the batch's total tiles
                    B_RED = 512,     // 2 x [4 warps][16] floats: tail column max
                    B_SUM = 1024,    // 2 x [4 warps][16] floats: tail sums
                    B_XMAX = 1536,   // 2 x [4 column quarters][128 rows] floats: row max
@@ -321,15 +329,21 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar + B_QFULL + 8 * i, 1);
             mbar_init(bar + B_QEMPTY + 8 * i, 1);
-            mbar_init(bar + B_KFULL + 8 * i, 1);
-            mbar_init(bar + B_KEMPTY + 8 * i, 1);
-            mbar_init(bar + B_VFULL + 8 * i, 1);
-            mbar_init(bar + B_VEMPTY + 8 * i, 1);
+
+
             mbar_init(bar + B_SFULL + 8 * i, 1);
             mbar_init(bar + B_STFULL + 8 * i, 1);
             mbar_init(bar + B_TBAR + 8 * i, NTAILT);
             mbar_init(bar + B_PFULL + 8 * i, NMAIN);
             mbar_init(bar + B_PTFULL + 8 * i, NTAILT);
+        }
+        for (int i = 0; i < NKS; ++i) {
+            mbar_init(bar + B_KFULL + 8 * i, 1);
+            mbar_init(bar + B_KEMPTY + 8 * i, 1);
+        }
+        for (int i = 0; i < NVS; ++i) {
+            mbar_init(bar + B_VFULL + 8 * i, 1);
+            mbar_init(bar + B_VEMPTY + 8 * i, 1);
         }
         for (int i = 0; i < NRING; ++i) {
             mbar_init(bar + B_RFULL + 8 * i, 1);
@@ -462,9 +476,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 break;
             Item it;
             decode_item(a, ix, iy, iz, iw, it);
-            // Q of item k into slot k & 1
-            const int qs = k & 1;
-            if (k >= 2 && !wait_warp(bar + B_QEMPTY + 8 * qs, ((k >> 1) - 1) & 1, abort_flag, a.status))
+            // Q of item k into slot k % NQ
+            const int qs = k % NQ;
+            if (k >= NQ && !wait_warp(bar + B_QEMPTY + 8 * qs, ((k / NQ) - 1) & 1, abort_flag, a.status))
                 break;
             if (lane == 0) {
                 const uint32_t qb = sb + SM_Q + qs * QSLOT, fb = bar + B_QFULL + 8 * qs;
@@ -479,10 +493,10 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
             for (int j = 0; j < it.ntiles; ++j, ++kn) {
-                const int sl = kn & 1;
+                const int sl = kn % NKS;
                 const int z = (lane < 8) ? group_row(a, it, j, lane) : 0;
-                if (kn >= 2 &&
-                    !wait_warp(bar + B_KEMPTY + 8 * sl, ((kn - 2) >> 1) & 1, abort_flag, a.status)) {
+                if (kn >= NKS &&
+                    !wait_warp(bar + B_KEMPTY + 8 * sl, ((kn / NKS) - 1) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
@@ -490,9 +504,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
         }
         // wind down: the last K tiles this warp issued have landed
-        for (int m = kn - 2; m < kn; ++m)
+        for (int m = kn - NKS; m < kn; ++m)
             if (m >= 0)
-                drain_bar(bar + B_KFULL + 8 * (m & 1), (m >> 1) & 1);
+                drain_bar(bar + B_KFULL + 8 * (m % NKS), (m / NKS) & 1);
     } else if (warp == W_VPROD) {
         // ============================================================ V loads
         if (lane == 0) {
@@ -506,19 +520,19 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!ring_get(a, bar, ring, k, lane, abort_flag, it))
                 break;
             for (int j = 0; j < it.ntiles; ++j, ++vn) {
-                const int sl = vn & 1;
+                const int sl = vn % NVS;
                 const int z = (lane < 8) ? group_row(a, it, j, lane) : 0;
-                if (vn >= 2 &&
-                    !wait_warp(bar + B_VEMPTY + 8 * sl, ((vn - 2) >> 1) & 1, abort_flag, a.status)) {
+                if (vn >= NVS &&
+                    !wait_warp(bar + B_VEMPTY + 8 * sl, ((vn / NVS) - 1) & 1, abort_flag, a.status)) {
                     ok = false;
                     break;
                 }
                 load_tile(it, j, lane, z, sb + SM_V + sl * 32768u, &tm_v, &tm_vt, bar + B_VFULL + 8 * sl);
             }
         }
-        for (int m = vn - 2; m < vn; ++m)
+        for (int m = vn - NVS; m < vn; ++m)
             if (m >= 0)
-                drain_bar(bar + B_VFULL + 8 * (m & 1), (m >> 1) & 1);
+                drain_bar(bar + B_VFULL + 8 * (m % NVS), (m / NVS) & 1);
     } else if (warp == W_MMA) {
         // ============================================================ MMA issuer
         if (lane == 0) {
@@ -576,11 +590,11 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 // ---- Q K^T of tile qk_n: its K has landed and S buffer qk_n & 1 is free
                 //      (P V of tile qk_n - 2 has been issued)
                 if (qk_state == 1 && qk_n <= pv_n + 1) {
-                    const int sl = qk_n & 1, qs = qk_k & 1;
-                    if ((qk_j > 0 || mbar_test_wait(bar + B_QFULL + 8 * qs, (qk_k >> 1) & 1)) &&
-                        mbar_test_wait(bar + B_KFULL + 8 * sl, (qk_n >> 1) & 1)) {
+                    const int sl = qk_n & 1, ks = qk_n % NKS, qs = qk_k % NQ;
+                    if ((qk_j > 0 || mbar_test_wait(bar + B_QFULL + 8 * qs, (qk_k / NQ) & 1)) &&
+                        mbar_test_wait(bar + B_KFULL + 8 * ks, (qk_n / NKS) & 1)) {
                         tc_fence_after();
-                        const uint64_t dK = dK0 + sl * (32768u >> 4);
+                        const uint64_t dK = dK0 + ks * (32768u >> 4);
                         const uint64_t dQ = dQ0 + qs * (QSLOT >> 4);
                         const uint32_t s_t = tmem + TM_S + 128u * sl;
 #pragma unroll
@@ -601,7 +615,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             mma_commit(bar + B_STFULL + 8 * (qt_n & 1));
                             ++qt_n;
                         }
-                        mma_commit(bar + B_KEMPTY + 8 * sl);
+                        mma_commit(bar + B_KEMPTY + 8 * ks);
                         ++qk_n;
                         if (++qk_j == qi.ntiles) {
                             mma_commit(bar + B_QEMPTY + 8 * qs);
@@ -613,13 +627,13 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 // ---- P V of tile pv_n: its P (and tail P) and V are ready
                 if (pv_state == 1 && pv_n < qk_n) {
-                    const int sl = pv_n & 1;
+                    const int sl = pv_n & 1, vs = pv_n % NVS;
                     if (mbar_test_wait(bar + B_PFULL + 8 * sl, (pv_n >> 1) & 1) &&
-                        mbar_test_wait(bar + B_VFULL + 8 * sl, (pv_n >> 1) & 1) &&
+                        mbar_test_wait(bar + B_VFULL + 8 * vs, (pv_n / NVS) & 1) &&
                         (!pi.has_tail ||
                          mbar_test_wait(bar + B_PTFULL + 8 * (pt_n & 1), (pt_n >> 1) & 1))) {
                         tc_fence_after();
-                        const uint64_t dV = dV0 + sl * (32768u >> 4);
+                        const uint64_t dV = dV0 + vs * (32768u >> 4);
                         const uint32_t p_t = tmem + TM_S + 128u * sl;
 #pragma unroll
                         for (int kt = 0; kt < 8; ++kt) {
@@ -639,7 +653,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             mma_commit(bar + B_OTDONE);
                             ++pt_n;
                         }
-                        mma_commit(bar + B_VEMPTY + 8 * sl);
+                        mma_commit(bar + B_VEMPTY + 8 * vs);
                         ++pv_n;
                         if (++pv_j == pi.ntiles) {
                             ++pv_k;
