@@ -203,6 +203,22 @@ def draw_round_inputs(cfg, seed=None):
                 agree=agree)
 
 
+def draw_next_round(cfg, k, seed=None):
+    """Round k >= 1 of a multi-round workload: new draft logits, queries and
+    tree K/V (the cache and the context lengths carry over from round k - 1,
+    as compaction left them). Seeded by (seed, k)."""
+    base = cfg.seed if seed is None else seed
+    rng = np.random.default_rng([base, k])
+    draft = draw_draft_logits(cfg, rng)
+    P = cfg.P
+    q = _normal_bf16(rng, (cfg.R, P, cfg.Hq, cfg.d))
+    k_tree = _normal_bf16(rng, (cfg.R, P, cfg.Hkv, cfg.d))
+    v_tree = _normal_bf16(rng, (cfg.R, P, cfg.Hkv, cfg.d))
+    agree = draw_agreement(cfg, rng)
+    return dict(draft=draft, draft_logits=draft.z, q=q, k_tree=k_tree, v_tree=v_tree,
+                agree=agree)
+
+
 # ---------------------------------------------------------------- target
 def draw_agreement(cfg, rng):
     """Per request: (base, decay) of the target's agreement with draft top-1."""

@@ -74,3 +74,48 @@ class RoundCase:
     def oracle_tree_from_gpu_lp(self):
         return oracle.build_tree(self.g["top_lp"].astype(np.float64), self.g["top_ids"],
                                  self.cfg.B)
+
+
+# ------------------------------------------------------------------ tree checks
+TIE_EPS = 1e-6
+
+
+def prefix_scores(lp, ids, tokens, parents, depths, n):
+    """S of each node of one tree, recomputed from its token paths (rank lookup)."""
+    S = np.zeros(len(parents))
+    for node in range(1, n + 1):
+        d = depths[node] - 1
+        rank = int(np.nonzero(ids[d] == tokens[node - 1])[0][0])
+        S[node] = S[parents[node]] + lp[d, rank]
+    return S
+
+
+def tree_paths(tokens, parents, n):
+    paths = {0: ()}
+    for node in range(1, n + 1):
+        paths[node] = paths[int(parents[node])] + (int(tokens[node - 1]),)
+    return [paths[i] for i in range(1, n + 1)]
+
+
+def check_tie_band(B, o_lp, o_ids, otree, g_tokens, g_parents, g_depths, g_n_nodes, rows):
+    """End-to-end node set of the GPU tree (built from fp32 log-probs) against
+    the oracle's (fp64): prefix scores within TIE_EPS nats of the B-th count as
+    tied; every prefix above the band must be present, none below it, and the
+    band must hold as many nodes on both sides."""
+    for r in rows:
+        n = int(otree.n_nodes[r])
+        assert int(g_n_nodes[r]) == n
+        So = otree.S[r, 1:n + 1]
+        Sg = prefix_scores(o_lp[r], o_ids[r], g_tokens[r], g_parents[r], g_depths[r], n)[1:]
+        if n < B:  # the whole prefix space: identical sets
+            assert sorted(So) == sorted(Sg)
+            continue
+        SB = So.min()
+        paths_o = tree_paths(otree.tokens[r], otree.parents[r], n)
+        paths_g = tree_paths(g_tokens[r], g_parents[r], n)
+        sure_o = {p for p, s in zip(paths_o, So) if s > SB + TIE_EPS}
+        assert sure_o <= set(paths_g)
+        assert all(s >= SB - TIE_EPS for s in Sg)
+        band_o = {p for p, s in zip(paths_o, So) if abs(s - SB) <= TIE_EPS}
+        band_g = {p for p, s in zip(paths_g, Sg) if abs(s - SB) <= TIE_EPS}
+        assert len(band_o) == len(band_g)

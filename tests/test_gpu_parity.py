@@ -13,14 +13,13 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import RoundCase, dev, host, make_ctx
+from gpu_helpers import RoundCase, check_tie_band, dev, host, make_ctx
 from speculative_decoding_draft_depth_gb300 import ddt, synth
 
 pytestmark = pytest.mark.gpu
 
 LP_TOL = 1e-5
 ATT_TOL = 1e-2
-TIE_EPS = 1e-6
 
 CASES = {
     "tiny": dict(name="tiny"),
@@ -61,45 +60,10 @@ def _check_tree_stagewise(rc):
     return t
 
 
-def _prefix_scores(lp, ids, tokens, parents, depths, n):
-    """S of each node, recomputed from a tree's token paths (rank lookup)."""
-    S = np.zeros(len(parents))
-    for node in range(1, n + 1):
-        d = depths[node] - 1
-        rank = int(np.nonzero(ids[d] == tokens[node - 1])[0][0])
-        S[node] = S[parents[node]] + lp[d, rank]
-    return S
-
-
 def _check_tree_tie_band(rc):
     """End-to-end node set: GPU tree (from fp32 lp) vs oracle tree (fp64 lp)."""
-    B = rc.cfg.B
-    for r in range(rc.cfg.R):
-        ot, n = rc.o_tree, rc.o_tree.n_nodes[r]
-        assert rc.g["n_nodes"][r] == n
-        # prefix scores of both trees under the oracle's fp64 log-probs
-        So = ot.S[r, 1:n + 1]
-        Sg = _prefix_scores(rc.o_lp[r], rc.o_ids[r], rc.g["tree_tokens"][r], rc.g["parents"][r],
-                            rc.g["depths"][r], n)[1:]
-        if n < B:  # the whole prefix space: identical sets
-            assert sorted(So) == sorted(Sg)
-            continue
-        SB = So.min()
-        paths_o = _paths(ot.tokens[r], ot.parents[r], n)
-        paths_g = _paths(rc.g["tree_tokens"][r], rc.g["parents"][r], n)
-        sure_o = {p for p, s in zip(paths_o, So) if s > SB + TIE_EPS}
-        assert sure_o <= set(paths_g)
-        assert all(s >= SB - TIE_EPS for s in Sg)
-        band_o = {p for p, s in zip(paths_o, So) if abs(s - SB) <= TIE_EPS}
-        band_g = {p for p, s in zip(paths_g, Sg) if abs(s - SB) <= TIE_EPS}
-        assert len(band_o) == len(band_g)
-
-
-def _paths(tokens, parents, n):
-    paths = {0: ()}
-    for node in range(1, n + 1):
-        paths[node] = paths[int(parents[node])] + (int(tokens[node - 1]),)
-    return [paths[i] for i in range(1, n + 1)]
+    check_tie_band(rc.cfg.B, rc.o_lp, rc.o_ids, rc.o_tree, rc.g["tree_tokens"], rc.g["parents"],
+                   rc.g["depths"], rc.g["n_nodes"], range(rc.cfg.R))
 
 
 def _check_mask(rc, gtree):
