@@ -395,9 +395,13 @@ def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):
     return res
 
 
-def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps):
+def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps, n_copy=4):
     """Same metric through the C ABI with the step's inputs in pinned host
-    memory: H2D of the per-round inputs, the round, D2H of the results."""
+    memory: every step copies its inputs host->device, runs ddt_round and
+    reads its results back, all inside the timed region. The copies are cut
+    into chunks on n_copy streams (several DMA engines), and inputs are
+    double-buffered on the device so that step i+1's copies overlap step i's
+    round."""
     import torch
     names = ("draft_logits", "target_logits", "q", "k_tree", "v_tree")
     host = {}
@@ -411,24 +415,48 @@ def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps):
             for k in ("acc_len", "acc_tokens", "bonus")}
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_ctx.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in outs.values())
+    sets = [{k: bufs[k] for k in names}, {k: torch.empty_like(bufs[k]) for k in names}]
+    cstreams = [torch.cuda.Stream() for _ in range(n_copy)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    copied = [[ev() for _ in range(n_copy)] for _ in range(2)]
+    used = [ev(), ev()]  # the round that last read each input set is done
 
-    def step():
-        for k in names:
-            bufs[k].copy_(host[k], non_blocking=True)
+    def step(i, first):
+        cur = sets[i & 1]
+        for c, cs in enumerate(cstreams):
+            if not first[i & 1]:
+                cs.wait_event(used[i & 1])
+            with torch.cuda.stream(cs):
+                for k in names:
+                    src, dst = host[k].view(-1), cur[k].view(-1)
+                    n = src.numel()
+                    lo, hi = n * c // n_copy, n * (c + 1) // n_copy
+                    dst[lo:hi].copy_(src[lo:hi], non_blocking=True)
+            copied[i & 1][c].record(cs)
+        first[i & 1] = False
+        for e in copied[i & 1]:
+            stream.wait_event(e)
         d["ctx_lens"].copy_(host_ctx, non_blocking=True)
-        ctx.ddt_round(cfg.R, bufs, stream)
+        rb = dict(bufs)
+        rb.update(cur)
+        ctx.ddt_round(cfg.R, rb, stream)
+        used[i & 1].record(stream)
         for k, t in outs.items():
             t.copy_(bufs[k], non_blocking=True)
 
-    for _ in range(3):
-        step()
+    first = [True, True]
+    for i in range(3):
+        step(i, first)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        step()
+    for cs in cstreams:
+        cs.wait_event(a)
+    first = [False, False]
+    for i in range(steps):
+        step(i, first)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
@@ -438,7 +466,8 @@ def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps):
         ms = float(t.item())
     d["ctx_lens"].copy_(ctx0)
     return {"value": round(world * steps / (ms / 1e3), 2), "unit": UNIT,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "copy_streams": n_copy}
 
 
 def run_reference(cfg, args):
