@@ -58,6 +58,9 @@ def lib():
         L.orc_argmax.restype = i32
         L.orc_walk.argtypes = [p, p, p, p, i32, i32, i32, p, p, p, p]
         L.orc_walk.restype = None
+        L.orc_cond_tree.argtypes = [p, i32, p, p, i32, p, i32, i32, i64, i32, i32, i32, i32,
+                                    p, p, p, p, p, p, p, p, p, p]
+        L.orc_cond_tree.restype = i32
         L.orc_compact.argtypes = [p, p, p, i32, i64, p, p, p, p, p, i32, i32, i32, i32, i32, i32]
         L.orc_compact.restype = i32
         L.orc_num_threads.argtypes = []
@@ -262,3 +265,47 @@ def round_(inputs, target_logits_fn=None, target_logits=None, B=None, K=None):
     return dict(lp=lp, ids=ids, tree=tree, mask=mask, attn=attn, a=a, acc_len=acc_len,
                 acc_nodes=acc_nodes, acc_tokens=acc_tokens, bonus=bonus, ctx_lens=ctx,
                 flags=f1 | f2 | f3 | f4)
+
+
+class CondTree:
+    """Outputs of the parent-conditioned tree for R requests."""
+
+    def __init__(self, R, D, k, F, N):
+        P = N + 1
+        self.tokens = np.full((R, N), -1, np.int32)
+        self.parents = np.full((R, P), -1, np.int32)
+        self.depths = np.full((R, P), -1, np.int32)
+        self.S = np.zeros((R, P), np.float64)
+        self.n_nodes = np.zeros(R, np.int32)
+        self.cand_lp = np.zeros((R, D, F, k), np.float64)
+        self.cand_ids = np.zeros((R, D, F, k), np.int32)
+        self.frontier_tok = np.zeros((R, D, F), np.int32)
+
+
+def cond_tree(ell, W, E, anchors, k, F, N, replay_lp=None, replay_ids=None):
+    """Parent-conditioned tree ("Robot2050/TreeSpark", items 1-2): per-depth
+    logits ell [R, D, V] plus the Markov bias W e(t_u) (W, E [V, H], same
+    dtype), per-parent top-k, frontier of F by path score, top-N packing.
+    With replay_lp / replay_ids [R, D, F, k] the per-parent lists are taken
+    as given (the frontier and packing logic runs on them)."""
+    ell = np.ascontiguousarray(ell)
+    W = np.ascontiguousarray(W)
+    E = np.ascontiguousarray(E)
+    anchors = np.ascontiguousarray(anchors, dtype=np.int32)
+    R, D, V = ell.shape
+    H = W.shape[1]
+    t = CondTree(R, D, k, F, N)
+    rl = ri = None
+    if replay_lp is not None:
+        rl = np.ascontiguousarray(replay_lp, dtype=np.float64)
+        ri = np.ascontiguousarray(replay_ids, dtype=np.int32)
+    rc = lib().orc_cond_tree(_ptr(ell), _logit_dtype(ell), _ptr(W), _ptr(E), _logit_dtype(W),
+                             _ptr(anchors), R, D, V, H, k, F, N,
+                             _ptr(rl) if rl is not None else None,
+                             _ptr(ri) if ri is not None else None,
+                             _ptr(t.tokens), _ptr(t.parents), _ptr(t.depths), _ptr(t.S),
+                             _ptr(t.n_nodes), _ptr(t.cand_lp), _ptr(t.cand_ids),
+                             _ptr(t.frontier_tok))
+    if rc:
+        raise ValueError("bad arguments to cond_tree")
+    return t

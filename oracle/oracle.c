@@ -642,3 +642,205 @@ int orc_num_threads(void)
     return 1;
 #endif
 }
+
+/* ------------------------------------------------------------------------
+ * NEXT row 1: the parent-conditioned tree ["Robot2050/TreeSpark", items 1
+ * and 2: one backbone pass gives per-depth logits l_d; a first-order Markov
+ * head specialises depth d to a parent token, z_d(u) = l_d + W e(t_u);
+ * trees grow by per-parent top-k expansion with joint path-score frontier
+ * pruning, and are packed to N non-root nodes by global top-N].
+ *
+ * Readings (the page gives the policy, not its arithmetic):
+ *   - a parent's children are the k largest z_d(u) (equal values: lower
+ *     token id first); a child's path score is S(u) + lp with
+ *     lp = z - logsumexp(z) in fp64, S(root) = 0;
+ *   - depth d's candidates are all children of depth d-1's frontier, in
+ *     creation order (frontier slot, then child rank); the frontier of
+ *     depth d is its F best candidates by (S desc, creation order asc);
+ *     depth 1's frontier parent is the root (the anchor token);
+ *   - packing takes the N best candidates of all depths by (S desc, depth
+ *     asc, creation order asc), which is prefix-closed (lp <= 0, a parent
+ *     sorts before its children); node n is the n-th of them.
+ *   With k = F = 4 and 7 depths the candidates number 4 + 6 * 16 = 100,
+ *   the page's "up to 100 candidates before packing".
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double S;
+    int32_t depth, order, parent_cand, token;
+} cond_cand;
+
+static int cond_prune_cmp(const void *pa, const void *pb)
+{
+    const cond_cand *a = (const cond_cand *)pa, *b = (const cond_cand *)pb;
+    if (a->S != b->S)
+        return a->S > b->S ? -1 : 1;
+    return (a->order > b->order) - (a->order < b->order);
+}
+
+static int cond_pack_cmp(const void *pa, const void *pb)
+{
+    const cond_cand *a = (const cond_cand *)pa, *b = (const cond_cand *)pb;
+    if (a->S != b->S)
+        return a->S > b->S ? -1 : 1;
+    if (a->depth != b->depth)
+        return a->depth < b->depth ? -1 : 1;
+    return (a->order > b->order) - (a->order < b->order);
+}
+
+/* z = l + W e(tok) for one parent, its log-partition and top-k */
+static void cond_parent(const void *ell_row, int ell_dtype, const void *W, const void *E, int w_dtype,
+                        int64_t V, int H, int tok, int k, double *zbuf, double *lp, int32_t *ids)
+{
+    double m = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double b = 0.0;
+        for (int h = 0; h < H; ++h)
+            b += widen(W, w_dtype, v * H + h) * widen(E, w_dtype, (int64_t)tok * H + h);
+        const double z = widen(ell_row, ell_dtype, v) + b;
+        zbuf[v] = z;
+        if (z > m)
+            m = z;
+    }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        s += exp(zbuf[v] - m);
+    const double logz = m + log(s);
+    for (int j = 0; j < k; ++j) {
+        ids[j] = -1;
+        lp[j] = -INFINITY;
+    }
+    for (int64_t v = 0; v < V; ++v) {  /* insertion: value desc, lower id first */
+        const double z = zbuf[v];
+        if (ids[k - 1] >= 0 && !(z > lp[k - 1]))
+            continue;
+        int j = k - 1;
+        while (j > 0 && (ids[j - 1] < 0 || z > lp[j - 1])) {
+            lp[j] = lp[j - 1];
+            ids[j] = ids[j - 1];
+            --j;
+        }
+        lp[j] = z;
+        ids[j] = (int32_t)v;
+    }
+    for (int j = 0; j < k; ++j)
+        lp[j] -= logz;
+}
+
+/*
+ * ell [R, D, V] (dtype as widen), W and E [V, H] (w_dtype), anchors [R].
+ * Outputs (P = N + 1): tree_tokens [R, N], parents / depths [R, P] (root 0,
+ * parents[0] = -1), node_S [R, P], n_nodes [R]; optional per-parent lists
+ * cand_lp / cand_ids [R, D, F, k] and the parent token of each frontier slot
+ * frontier_tok [R, D, F] (-1 where a depth has fewer parents).
+ * replay_lp / replay_ids [R, D, F, k], when not NULL, replace the computed
+ * per-parent lists (the frontier and packing logic then runs on them).
+ */
+int orc_cond_tree(const void *ell, int ell_dtype, const void *W, const void *E, int w_dtype,
+                  const int32_t *anchors, int R, int D, int64_t V, int H, int k, int F, int N,
+                  const double *replay_lp, const int32_t *replay_ids, int32_t *tree_tokens,
+                  int32_t *parents, int32_t *depths, double *node_S, int32_t *n_nodes,
+                  double *cand_lp, int32_t *cand_ids, int32_t *frontier_tok)
+{
+    if (R < 1 || D < 1 || V < 1 || k < 1 || k > V || F < 1 || N < 1 || (replay_lp == NULL && H < 1))
+        return ORC_BAD_ARG;
+    const int P = N + 1;
+    const int64_t cmax = (int64_t)k + (int64_t)(D - 1) * F * k;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        cond_cand *cand = (cond_cand *)malloc(sizeof(cond_cand) * (size_t)cmax);
+        cond_cand *tmp = (cond_cand *)malloc(sizeof(cond_cand) * (size_t)(F * k + 1));
+        int32_t *front = (int32_t *)malloc(sizeof(int32_t) * (size_t)F);  /* candidate index, -1 root */
+        double *zbuf = replay_lp ? NULL : (double *)malloc(sizeof(double) * (size_t)V);
+        double *lp = (double *)malloc(sizeof(double) * (size_t)k);
+        int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+        int nf = 1, nc = 0;
+        front[0] = -1;
+        for (int d = 1; d <= D; ++d) {
+            const int first = nc;
+            for (int f = 0; f < F; ++f) {
+                const int64_t slot = ((int64_t)r * D + (d - 1)) * F + f;
+                if (frontier_tok)
+                    frontier_tok[slot] = (f < nf) ? (front[f] < 0 ? anchors[r] : cand[front[f]].token) : -1;
+                if (f >= nf) {
+                    if (cand_lp)
+                        for (int j = 0; j < k; ++j) {
+                            cand_lp[slot * k + j] = -INFINITY;
+                            cand_ids[slot * k + j] = -1;
+                        }
+                    continue;
+                }
+                const int u = front[f];
+                const int tok = (u < 0) ? anchors[r] : cand[u].token;
+                const double Su = (u < 0) ? 0.0 : cand[u].S;
+                if (replay_lp) {
+                    for (int j = 0; j < k; ++j) {
+                        lp[j] = replay_lp[slot * k + j];
+                        ids[j] = replay_ids[slot * k + j];
+                    }
+                } else {
+                    const char *row = (const char *)ell +
+                                      (((int64_t)r * D + (d - 1)) * V) * (ell_dtype == 1 ? 2 : ell_dtype == 0 ? 4 : 8);
+                    cond_parent(row, ell_dtype, W, E, w_dtype, V, H, tok, k, zbuf, lp, ids);
+                }
+                for (int j = 0; j < k; ++j) {
+                    if (cand_lp) {
+                        cand_lp[slot * k + j] = lp[j];
+                        cand_ids[slot * k + j] = ids[j];
+                    }
+                    cond_cand *c = &cand[nc];
+                    c->S = Su + lp[j];
+                    c->depth = d;
+                    c->order = nc;
+                    c->parent_cand = u;
+                    c->token = ids[j];
+                    ++nc;
+                }
+            }
+            /* frontier of the next depth: the F best of this depth's candidates */
+            const int nd = nc - first;
+            memcpy(tmp, cand + first, sizeof(cond_cand) * (size_t)nd);
+            qsort(tmp, (size_t)nd, sizeof(cond_cand), cond_prune_cmp);
+            nf = nd < F ? nd : F;
+            for (int f = 0; f < nf; ++f)
+                front[f] = tmp[f].order;
+        }
+        /* packing: the N best of all candidates */
+        cond_cand *all = (cond_cand *)malloc(sizeof(cond_cand) * (size_t)nc);
+        memcpy(all, cand, sizeof(cond_cand) * (size_t)nc);
+        qsort(all, (size_t)nc, sizeof(cond_cand), cond_pack_cmp);
+        const int n = nc < N ? nc : N;
+        int32_t *node_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)nc);
+        for (int i = 0; i < nc; ++i)
+            node_of[i] = -1;
+        int32_t *tok = tree_tokens + (int64_t)r * N;
+        int32_t *par = parents + (int64_t)r * P;
+        int32_t *dep = depths + (int64_t)r * P;
+        double *ns = node_S + (int64_t)r * P;
+        for (int j = 0; j < N; ++j)
+            tok[j] = -1;
+        for (int j = 0; j < P; ++j) {
+            par[j] = -1;
+            dep[j] = -1;
+            ns[j] = 0.0;
+        }
+        dep[0] = 0;
+        for (int i = 0; i < n; ++i) {
+            const cond_cand *c = &all[i];
+            node_of[c->order] = i + 1;
+            tok[i] = c->token;
+            par[i + 1] = (c->parent_cand < 0) ? 0 : node_of[c->parent_cand];
+            dep[i + 1] = c->depth;
+            ns[i + 1] = c->S;
+        }
+        n_nodes[r] = n;
+        free(node_of);
+        free(all);
+        free(ids);
+        free(lp);
+        free(zbuf);
+        free(front);
+        free(tmp);
+        free(cand);
+    }
+    return 0;
+}
