@@ -85,6 +85,9 @@ typedef struct ddt_config {
     int64_t num_pages;         /* pages in the KV pool (bounds checks) */
     int32_t draft_dtype;       /* ddt_dtype of draft logits */
     int32_t target_dtype;      /* ddt_dtype of target logits */
+    /* parent-conditioned tree (ddt_build_tree_conditioned); 0 = not used */
+    int32_t markov_dim;        /* H of the Markov head W, E [V, H]: 64..256, multiple of 64 */
+    int32_t frontier;          /* F: parents kept per depth (1..8); F * K <= 32 */
 } ddt_config;
 
 typedef struct ddt_ctx ddt_ctx; /* opaque */
@@ -188,6 +191,30 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
                       int32_t *acc_tokens, int32_t *bonus, uint16_t *k_cache, uint16_t *v_cache,
                       const int32_t *block_table, const uint16_t *k_tree, const uint16_t *v_tree,
                       int32_t *ctx_lens, void *stream);
+
+/* Parent-conditioned tree ("Robot2050/TreeSpark", items 1 and 2): a
+ * backbone's per-depth logits l_d (draft_logits [R, L, V], bf16) specialised
+ * to each parent token t_u by a first-order Markov head,
+ *     z_d(u) = l_d + W e(t_u),        W, E: [V, H] bf16 (H = markov_dim),
+ * the K best children of every parent (log-probs of z_d(u); equal values:
+ * lower token id first), the F best children of a depth by path score
+ * S = S(parent) + lp (fp64; S(root) = 0) as the next depth's parents
+ * (frontier), and the B best candidates of all depths by (S desc, depth asc,
+ * creation order asc) packed as nodes 1..B -- a prefix-closed tree, written
+ * in the layout of ddt_build_tree (root 0 = the anchor token, anchors [R]).
+ * The config's L is the number of depths, K the children per parent (<= 8),
+ * B the node budget; R * F <= 128.
+ * Optional outputs (NULL to skip): cand_lp / cand_ids [R, L, F, K] fp32 /
+ * int32, the children lists of each depth's frontier slots (-inf / -1 past
+ * the frontier), and frontier_tok [R, L, F], the parent token of each slot.
+ * mask [R, P, W] (optional) as in ddt_build_tree. DDT_EUNSUPPORTED if the
+ * context was not created for this tree (markov_dim == 0) or the limits are
+ * exceeded. */
+ddt_status ddt_build_tree_conditioned(ddt_ctx *ctx, const void *draft_logits, const uint16_t *W,
+                                      const uint16_t *E, const int32_t *anchors, int32_t R,
+                                      float *cand_lp, int32_t *cand_ids, int32_t *frontier_tok,
+                                      int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *n_nodes, uint32_t *mask, void *stream);
 
 /* Everything one round reads and writes (shapes as above). */
 typedef struct ddt_round_args {

@@ -61,6 +61,9 @@ def lib():
         L.orc_cond_tree.argtypes = [p, i32, p, p, i32, p, i32, i32, i64, i32, i32, i32, i32,
                                     p, p, p, p, p, p, p, p, p, p]
         L.orc_cond_tree.restype = i32
+        L.orc_cond_parent_lists.argtypes = [p, i32, p, p, i32, i32, i32, i64, i32, i32, i64,
+                                            p, p, p, p, p]
+        L.orc_cond_parent_lists.restype = i32
         L.orc_compact.argtypes = [p, p, p, i32, i64, p, p, p, p, p, i32, i32, i32, i32, i32, i32]
         L.orc_compact.restype = i32
         L.orc_num_threads.argtypes = []
@@ -309,3 +312,24 @@ def cond_tree(ell, W, E, anchors, k, F, N, replay_lp=None, replay_ids=None):
     if rc:
         raise ValueError("bad arguments to cond_tree")
     return t
+
+
+def cond_parent_lists(ell, W, E, req, depth, tok, k):
+    """Children lists (lp [n, k] fp64, ids [n, k]) of given parents: request
+    req[i], depth row depth[i] (0-based), parent token tok[i]."""
+    ell = np.ascontiguousarray(ell)
+    W = np.ascontiguousarray(W)
+    E = np.ascontiguousarray(E)
+    req = np.ascontiguousarray(req, dtype=np.int32)
+    depth = np.ascontiguousarray(depth, dtype=np.int32)
+    tok = np.ascontiguousarray(tok, dtype=np.int32)
+    R, D, V = ell.shape
+    n = len(req)
+    lp = np.empty((n, k), np.float64)
+    ids = np.empty((n, k), np.int32)
+    rc = lib().orc_cond_parent_lists(_ptr(ell), _logit_dtype(ell), _ptr(W), _ptr(E),
+                                     _logit_dtype(W), R, D, V, W.shape[1], k, n, _ptr(req),
+                                     _ptr(depth), _ptr(tok), _ptr(lp), _ptr(ids))
+    if rc:
+        raise ValueError("bad arguments to cond_parent_lists")
+    return lp, ids

@@ -844,3 +844,26 @@ int orc_cond_tree(const void *ell, int ell_dtype, const void *W, const void *E, 
     }
     return 0;
 }
+
+/* One parent's children lists of the parent-conditioned tree, for given
+ * (request, depth, parent token) triples: z = l[r, d] + W e(tok), lp = z -
+ * logsumexp(z) (fp64), the k largest (equal values: lower id first).
+ * lp, ids: [n, k]. */
+int orc_cond_parent_lists(const void *ell, int ell_dtype, const void *W, const void *E,
+                          int w_dtype, int R, int D, int64_t V, int H, int k, int64_t n,
+                          const int32_t *req, const int32_t *depth, const int32_t *tok,
+                          double *lp, int32_t *ids)
+{
+    if (k < 1 || k > V || H < 1)
+        return ORC_BAD_ARG;
+    const int esz = ell_dtype == 1 ? 2 : ell_dtype == 0 ? 4 : 8;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n; ++i) {
+        double *zbuf = (double *)malloc(sizeof(double) * (size_t)V);
+        const char *row = (const char *)ell + (((int64_t)req[i] * D + depth[i]) * V) * esz;
+        cond_parent(row, ell_dtype, W, E, w_dtype, V, H, tok[i], k, zbuf, lp + i * k, ids + i * k);
+        free(zbuf);
+    }
+    (void)R;
+    return 0;
+}

@@ -48,13 +48,18 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
     if (max_ctx > (int64_t)64 * ATT_CHUNK || c.R_max > 2048)
         return DDT_EUNSUPPORTED;
+    if (c.markov_dim < 0 || c.frontier < 0)
+        return DDT_EINVAL;
+    if (c.markov_dim > 0 && (c.draft_dtype != DDT_BF16 || !cond_tree_supported(c)))
+        return DDT_EUNSUPPORTED;
     *out = c;
     return DDT_OK;
 }
 
 struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
-        att_rg_base, att_part_o, att_part_ml, total;
+        att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
+        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, total;
     int tk_nch, am_nch, rowgroups, max_items;
 };
 
@@ -99,6 +104,18 @@ Layout layout_for(const ddt_config &c)
     L.att_rg_base = take(rg * sizeof(int32_t));
     L.att_part_o = take((size_t)L.max_items * ATT_ROWS * c.d * sizeof(float));
     L.att_part_ml = take((size_t)L.max_items * ATT_ROWS * sizeof(float2));
+    // parent-conditioned tree (sized for up to CG_GRID_MAX CTAs of its GEMM)
+    const size_t np = c.markov_dim > 0 ? (size_t)c.R_max * c.frontier : 0;
+    const size_t cmax = c.markov_dim > 0 ? (size_t)cond_tree_cmax(c) : 0;
+    const size_t nfr = c.markov_dim > 0 ? (size_t)c.R_max * c.frontier : 0;
+    L.cg_part_ms = take(np * CG_GRID_MAX * sizeof(float2));
+    L.cg_part_top = take(np * CG_GRID_MAX * 8 * sizeof(uint64_t));
+    L.cg_fr_tok = take(nfr * sizeof(int32_t));
+    L.cg_fr_cand = take(nfr * sizeof(int32_t));
+    L.cg_fr_n = take((c.markov_dim > 0 ? (size_t)c.R_max : 0) * sizeof(int32_t));
+    L.cg_fr_S = take(nfr * sizeof(double));
+    L.cg_c_S = take((size_t)(c.markov_dim > 0 ? c.R_max : 0) * cmax * sizeof(double));
+    L.cg_c_meta = take((size_t)(c.markov_dim > 0 ? c.R_max : 0) * cmax * 3 * sizeof(int32_t));
     L.total = off;
     return L;
 }
@@ -247,6 +264,15 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->att_rg_base = (int32_t *)(w + L.att_rg_base);
     ctx->att_part_o = (float *)(w + L.att_part_o);
     ctx->att_part_ml = (float2 *)(w + L.att_part_ml);
+    ctx->cg_grid = ctx->num_sms < CG_GRID_MAX ? ctx->num_sms : CG_GRID_MAX;
+    ctx->cg_part_ms = (float2 *)(w + L.cg_part_ms);
+    ctx->cg_part_top = (uint64_t *)(w + L.cg_part_top);
+    ctx->cg_fr_tok = (int32_t *)(w + L.cg_fr_tok);
+    ctx->cg_fr_cand = (int32_t *)(w + L.cg_fr_cand);
+    ctx->cg_fr_n = (int32_t *)(w + L.cg_fr_n);
+    ctx->cg_fr_S = (double *)(w + L.cg_fr_S);
+    ctx->cg_c_S = (double *)(w + L.cg_c_S);
+    ctx->cg_c_meta = (int32_t *)(w + L.cg_c_meta);
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so
@@ -333,6 +359,36 @@ ddt_status ddt_build_tree(ddt_ctx *ctx, const float *top_lp, const int32_t *top_
         return st;
     DDT_TRY(launch_build_tree(ctx, top_lp, top_ids, R, tree_tokens, parents, depths, n_nodes, mask,
                               (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_build_tree_conditioned(ddt_ctx *ctx, const void *draft_logits, const uint16_t *W,
+                                      const uint16_t *E, const int32_t *anchors, int32_t R,
+                                      float *cand_lp, int32_t *cand_ids, int32_t *frontier_tok,
+                                      int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                                      int32_t *n_nodes, uint32_t *mask, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (ctx->cfg.markov_dim <= 0)
+        return DDT_EUNSUPPORTED;
+    if (R == 0)
+        return DDT_OK;
+    DDT_CHECK(draft_logits && W && E && anchors && tree_tokens && parents && depths && n_nodes);
+    DDT_CHECK(aligned16(W) && aligned16(E) && aligned4(anchors) && aligned4(tree_tokens) &&
+              aligned4(parents) && aligned4(depths) && aligned4(n_nodes));
+    DDT_CHECK((cand_lp == nullptr) == (cand_ids == nullptr));
+    DDT_CHECK(!cand_lp || (aligned4(cand_lp) && aligned4(cand_ids)));
+    DDT_CHECK(!frontier_tok || aligned4(frontier_tok));
+    DDT_CHECK(!mask || aligned4(mask));
+    if (R * ctx->cfg.frontier > 128)
+        return DDT_EUNSUPPORTED;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_cond_tree(ctx, (const uint16_t *)draft_logits, W, E, anchors, R, cand_lp,
+                             cand_ids, frontier_tok, tree_tokens, parents, depths, n_nodes, mask,
+                             (cudaStream_t)stream));
     return DDT_OK;
 }
 

@@ -1095,21 +1095,35 @@ att_combine_kernel(const TcArgs a, int NG)
     const int nrows = TILE + ((rg == 0 && a.tail_rows > 0) ? a.tail_rows : 0);
     for (int s0 = 0; s0 < ns; s0 += CB_SEGS) {
         const int sn = min(CB_SEGS, ns - s0);
-        // per row: every segment's weight exp2(m_s - M) / L
+        // per row: every segment's weight exp2(m_s - M) / L (the pairs of up to
+        // CB_SEGS segments loaded at once)
         if (tid < nrows) {
-            float M = DDT_NEG_INF;
-            for (int s = 0; s < ns; ++s)
-                M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]).x);
-            float Ls = 0.f;
-            for (int s = 0; s < ns; ++s) {
-                const float2 ml = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]);
-                Ls += (ml.x == DDT_NEG_INF) ? 0.f : ml.y * ex2(ml.x - M);
+            float2 ml[CB_SEGS];
+#pragma unroll
+            for (int s = 0; s < CB_SEGS; ++s)
+                ml[s] = (s0 + s < ns) ? __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + tid])
+                                      : make_float2(DDT_NEG_INF, 0.f);
+            float M = DDT_NEG_INF, Ls = 0.f;
+            if (ns <= CB_SEGS) {
+#pragma unroll
+                for (int s = 0; s < CB_SEGS; ++s)
+                    M = fmaxf(M, ml[s].x);
+#pragma unroll
+                for (int s = 0; s < CB_SEGS; ++s)
+                    Ls += (ml[s].x == DDT_NEG_INF) ? 0.f : ml[s].y * ex2(ml[s].x - M);
+            } else {
+                for (int s = 0; s < ns; ++s)
+                    M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]).x);
+                for (int s = 0; s < ns; ++s) {
+                    const float2 v = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]);
+                    Ls += (v.x == DDT_NEG_INF) ? 0.f : v.y * ex2(v.x - M);
+                }
             }
             const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-            for (int s = 0; s < sn; ++s) {
-                const float m = __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + tid]).x;
-                s_fac[s * ATT_ROWS + tid] = (m == DDT_NEG_INF) ? 0.f : ex2(m - M) * inv;
-            }
+#pragma unroll
+            for (int s = 0; s < CB_SEGS; ++s)
+                if (s < sn)
+                    s_fac[s * ATT_ROWS + tid] = (ml[s].x == DDT_NEG_INF) ? 0.f : ex2(ml[s].x - M) * inv;
         }
         __syncthreads();
         // every (row, 4 columns): independent float4 loads, several in flight

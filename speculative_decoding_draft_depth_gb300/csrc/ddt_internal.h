@@ -30,6 +30,9 @@ constexpr int ATT_ROWS = ATT_MTILES * 16;  // query rows per row group (144)
 constexpr int ATT_THREADS = ATT_MTILES * 32;
 constexpr int ATT_STAGES = 3;
 
+// parent-conditioned tree: most CTAs of its per-depth GEMM (partials per CTA)
+constexpr int CG_GRID_MAX = 256;
+
 struct ddt_ctx {
     ddt_config cfg;  // with K resolved
     int device;
@@ -59,6 +62,14 @@ struct ddt_ctx {
     int32_t *att_rg_base;    // [R_max * Hkv * rowgroups] first item of each (r, g, rowgroup)
     float *att_part_o;       // [max_items, ATT_ROWS, d]
     float2 *att_part_ml;     // [max_items, ATT_ROWS]
+    // parent-conditioned tree (markov_dim > 0)
+    int cg_grid;             // CTAs of the per-depth GEMM
+    float2 *cg_part_ms;      // [R_max * F, cg_grid] (max, sum of exp)
+    uint64_t *cg_part_top;   // [R_max * F, cg_grid, 8] top-k keys
+    int32_t *cg_fr_tok, *cg_fr_cand, *cg_fr_n;  // [R_max, F], [R_max, F], [R_max]
+    double *cg_fr_S;         // [R_max, F]
+    double *cg_c_S;          // [R_max, Cmax] candidate scores
+    int32_t *cg_c_meta;      // [R_max, Cmax, 3] depth, parent candidate, token
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };
@@ -96,6 +107,15 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
                                 float *out, cudaStream_t s);
 cudaError_t launch_att_plan(const ddt_ctx *c, const int32_t *ctx_lens, int R, int RG, int max_ctx,
                             cudaStream_t s);
+
+// the parent-conditioned tree (cond_tree.cu)
+bool cond_tree_supported(const ddt_config &cfg);
+int cond_tree_cmax(const ddt_config &cfg);
+cudaError_t launch_cond_tree(const ddt_ctx *c, const uint16_t *ell, const uint16_t *W,
+                             const uint16_t *E, const int32_t *anchors, int R, float *cand_lp,
+                             int32_t *cand_ids, int32_t *frontier_tok, int32_t *tree_tokens,
+                             int32_t *parents, int32_t *depths, int32_t *n_nodes, uint32_t *mask,
+                             cudaStream_t s);
 
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,

@@ -19,7 +19,7 @@ BF16, F32 = 0, 1
 DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
 
 EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
-           "ddt_build_tree", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
+           "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
            "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_device_status",
            "ddt_strerror", "ddt_last_cuda_error")
 
@@ -39,7 +39,8 @@ class Config(ctypes.Structure):
                 ("B", ctypes.c_int32), ("K", ctypes.c_int32), ("Hq", ctypes.c_int32),
                 ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_req", ctypes.c_int32), ("num_pages", ctypes.c_int64),
-                ("draft_dtype", ctypes.c_int32), ("target_dtype", ctypes.c_int32)]
+                ("draft_dtype", ctypes.c_int32), ("target_dtype", ctypes.c_int32),
+                ("markov_dim", ctypes.c_int32), ("frontier", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -72,6 +73,8 @@ def load(path=LIB_PATH):
         "ddt_topk_logprobs": ([_P, _P, i32, _P, _P, _P], i32),
         "ddt_build_tree": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
         "ddt_build_mask": ([_P, _P, _P, i32, _P, _P], i32),
+        "ddt_build_tree_conditioned": ([_P, _P, _P, _P, _P, i32, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P], i32),
         "ddt_tree_attention": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, i32, _P, _P], i32),
         "ddt_target_argmax": ([_P, _P, i32, _P, _P], i32),
         "ddt_walk": ([_P, _P, _P, _P, _P, i32, _P, _P, _P, _P, _P], i32),
@@ -113,9 +116,9 @@ def _check(status, where):
 
 
 def make_config(R_max, L, V, B, Hq, Hkv, d, page_size, max_pages_per_req, num_pages, K=0,
-                draft_dtype=BF16, target_dtype=BF16):
+                draft_dtype=BF16, target_dtype=BF16, markov_dim=0, frontier=0):
     return Config(R_max, L, V, B, K, Hq, Hkv, d, page_size, max_pages_per_req, num_pages,
-                  draft_dtype, target_dtype)
+                  draft_dtype, target_dtype, markov_dim, frontier)
 
 
 def workspace_bytes(cfg):
@@ -156,6 +159,14 @@ class Context:
         _check(_lib.ddt_build_tree(self._h, _ptr(top_lp), _ptr(top_ids), R, _ptr(tree_tokens),
                                    _ptr(parents), _ptr(depths), _ptr(n_nodes), _ptr(mask),
                                    _stream(stream)), "ddt_build_tree")
+
+    def ddt_build_tree_conditioned(self, draft_logits, W, E, anchors, R, tree_tokens, parents,
+                                   depths, n_nodes, mask=None, cand_lp=None, cand_ids=None,
+                                   frontier_tok=None, stream=None):
+        _check(_lib.ddt_build_tree_conditioned(
+            self._h, _ptr(draft_logits), _ptr(W), _ptr(E), _ptr(anchors), R, _ptr(cand_lp),
+            _ptr(cand_ids), _ptr(frontier_tok), _ptr(tree_tokens), _ptr(parents), _ptr(depths),
+            _ptr(n_nodes), _ptr(mask), _stream(stream)), "ddt_build_tree_conditioned")
 
     def ddt_build_mask(self, parents, n_nodes, R, mask, stream=None):
         _check(_lib.ddt_build_mask(self._h, _ptr(parents), _ptr(n_nodes), R, _ptr(mask),

@@ -21,6 +21,10 @@ draws stand in for them):
   wide256  R=256, B=K=64, ctx lognormal(ln 4096, 1) capped at 32768, logits
            of 'single' divided by T ~ U[0.3,1.5] per (request, depth),
            agreement 0.75, Qwen3-4B attention (32/8/128)            (seed 4)
+  treespark R=8, 7 depths, V=151936, parent-conditioned tree with k=4
+           children per parent, frontier F=4, N=32 nodes; backbone logits
+           bf16 N(0,1)*3, Markov head W and embeddings E bf16 N(0, 0.02)
+           [V, 256], anchors uniform; Qwen3-4B attention, ctx 2048  (seed 2)
 """
 from dataclasses import dataclass, field, replace
 
@@ -51,6 +55,8 @@ class RoundConfig:
     agree_args: tuple = (0.8, 0.03)
     rounds: int = 1
     spare_pages: int = 8
+    markov_dim: int = 0  # H of the parent-conditioned tree's Markov head
+    frontier: int = 0  # F of the parent-conditioned tree
 
     @property
     def P(self):
@@ -76,6 +82,10 @@ CONFIGS = {
                            d=128, page=16, logit_dtype="bf16", ctx_kind="lognormal",
                            ctx_args=(4096, 1.0, 32768), seed=4, temp_range=(0.3, 1.5),
                            agree_kind="const", agree_args=(0.75,), rounds=8),
+    "treespark": RoundConfig("treespark", R=8, L=7, V=VOCAB_QWEN3, B=32, K=4, Hq=32, Hkv=8,
+                             d=128, page=16, logit_dtype="bf16", ctx_kind="fixed",
+                             ctx_args=(2048,), seed=2, boost=False, agree_kind="const",
+                             agree_args=(0.75,), markov_dim=256, frontier=4),
 }
 
 
@@ -201,6 +211,17 @@ def draw_round_inputs(cfg, seed=None):
     return dict(draft=draft, draft_logits=draft.z, ctx_lens=ctx_lens, k_cache=k_cache,
                 v_cache=v_cache, block_table=block_table, q=q, k_tree=k_tree, v_tree=v_tree,
                 agree=agree)
+
+
+def draw_markov_head(cfg, seed=None):
+    """The parent-conditioned tree's Markov head: W, E [V, H] bf16 N(0, 0.02),
+    and one anchor (root) token per request."""
+    rng = np.random.default_rng([cfg.seed if seed is None else seed, 17])
+    H = cfg.markov_dim
+    W = _normal_bf16(rng, (cfg.V, H), scale=0.02)
+    E = _normal_bf16(rng, (cfg.V, H), scale=0.02)
+    anchors = rng.integers(0, cfg.V, size=cfg.R).astype(np.int32)
+    return W, E, anchors
 
 
 def draw_next_round(cfg, k, seed=None):

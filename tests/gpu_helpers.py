@@ -39,7 +39,8 @@ def make_ctx(cfg, inp, R_max=None):
         page_size=cfg.page, max_pages_per_req=inp["block_table"].shape[1],
         num_pages=inp["k_cache"].shape[0],
         draft_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32,
-        target_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32)
+        target_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32,
+        markov_dim=cfg.markov_dim, frontier=cfg.frontier)
     return ddt.Context(c)
 
 

@@ -115,3 +115,21 @@ def test_replay_reproduces():
     for name in ("tokens", "parents", "depths", "n_nodes", "frontier_tok"):
         np.testing.assert_array_equal(getattr(t2, name), getattr(t, name))
     np.testing.assert_array_equal(t2.S, t.S)
+
+
+def test_parent_lists_match_the_tree_lists():
+    ell, W, E, anchors = _inputs(R=2, D=3, V=40, H=8, seed=8)
+    t = oracle.cond_tree(ell, W, E, anchors, k=4, F=2, N=10)
+    req, dep, tok, want_lp, want_ids = [], [], [], [], []
+    for r in range(2):
+        for d in range(3):
+            for f in range(2):
+                if t.frontier_tok[r, d, f] >= 0:
+                    req.append(r)
+                    dep.append(d)
+                    tok.append(t.frontier_tok[r, d, f])
+                    want_lp.append(t.cand_lp[r, d, f])
+                    want_ids.append(t.cand_ids[r, d, f])
+    lp, ids = oracle.cond_parent_lists(ell, W, E, req, dep, tok, 4)
+    np.testing.assert_array_equal(ids, np.array(want_ids))
+    np.testing.assert_array_equal(lp, np.array(want_lp))
