@@ -187,6 +187,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true",
+                    help="skip the timing of the NEXT rows (parent-conditioned tree)")
     ap.add_argument("--stage", default="round",
                     choices=["round", "topk", "tree", "attention", "accept"],
                     help="time one stage alone (small profiling cases)")
@@ -333,6 +335,8 @@ def main():
            "clocks": clk,
            "acceptance": {"mean_acc_len": float(np.mean(acc_len))}}
 
+    if rank == 0 and not args.no_next:
+        out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline)}
     if not args.no_e2e:
         out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
                               steps=max(10, min(args.steps, 50)))
@@ -392,6 +396,65 @@ def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):
     run("accept", accept)
     d["ctx_lens"].copy_(ctx0)
     torch.cuda.synchronize()
+    return res
+
+
+def time_cond_tree(dev, reps=20, cpu=True):
+    """The parent-conditioned tree ("Robot2050/TreeSpark") on its own workload
+    (8 requests, 7 depths, V=151936, H=256, k=F=4, N=32): device time per
+    call, algorithmic bytes (W and the backbone rows once per depth), and the
+    oracle's time for one request scaled to the batch."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import ddt, synth
+    cfg = synth.config("treespark")
+    inp = synth.draw_round_inputs(cfg)
+    W, E, anchors = synth.draw_markov_head(cfg)
+    c = ddt.make_config(R_max=cfg.R, L=cfg.L, V=cfg.V, B=cfg.B, K=cfg.K, Hq=cfg.Hq, Hkv=cfg.Hkv,
+                        d=cfg.d, page_size=cfg.page,
+                        max_pages_per_req=inp["block_table"].shape[1],
+                        num_pages=inp["k_cache"].shape[0], markov_dim=cfg.markov_dim,
+                        frontier=cfg.frontier)
+    ctx = ddt.Context(c)
+
+    def td(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    ell, Wd, Ed, an = td(inp["draft_logits"]), td(W), td(E), td(anchors)
+    R, N, P = cfg.R, cfg.B, cfg.B + 1
+    i32 = dict(dtype=torch.int32, device=dev)
+    out = [torch.empty((R, N), **i32), torch.empty((R, P), **i32), torch.empty((R, P), **i32),
+           torch.empty((R,), **i32), torch.empty((R, P, (P + 31) // 32), **i32)]
+
+    def call():
+        ctx.ddt_build_tree_conditioned(ell, Wd, Ed, an, R, *out)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    nbytes = cfg.L * (cfg.V * cfg.markov_dim * 2 + R * cfg.V * 2) + R * (cfg.L * cfg.frontier *
+                                                                        cfg.markov_dim * 2)
+    peak, _ = _peaks()
+    res = {"workload": "treespark: R=8, 7 depths, V=151936, H=256, k=4, F=4, N=32, bf16",
+           "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+           "GBps": round(nbytes / (ms / 1e3) / 1e9, 1),
+           "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / peak, 4),
+           "note": "W (78 MB) is read once per depth and fits in L2"}
+    if cpu:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.cond_tree(inp["draft_logits"][:1], W, E, anchors[:1], k=cfg.K, F=cfg.frontier,
+                         N=cfg.B)
+        sec = (time.perf_counter() - t0) * R
+        res["cpu_oracle_ms"] = round(sec * 1e3, 1)
+        res["cpu_oracle_sample"] = "1 of 8 requests, scaled"
     return res
 
 

@@ -59,7 +59,7 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
-        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, total;
+        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, total;
     int tk_nch, am_nch, rowgroups, max_items;
 };
 
@@ -116,6 +116,10 @@ Layout layout_for(const ddt_config &c)
     L.cg_fr_S = take(nfr * sizeof(double));
     L.cg_c_S = take((size_t)(c.markov_dim > 0 ? c.R_max : 0) * cmax * sizeof(double));
     L.cg_c_meta = take((size_t)(c.markov_dim > 0 ? c.R_max : 0) * cmax * 3 * sizeof(int32_t));
+    L.cg_thr = take((c.markov_dim > 0 ? (size_t)c.L * CG_NP_MAX : 0) * sizeof(uint32_t));
+    const size_t nseed = c.markov_dim > 0 ? (size_t)c.R_max * c.L * c.K : 0;
+    L.cg_seed_lp = take(nseed * sizeof(float));
+    L.cg_seed_ids = take(nseed * sizeof(int32_t));
     L.total = off;
     return L;
 }
@@ -273,6 +277,9 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->cg_fr_S = (double *)(w + L.cg_fr_S);
     ctx->cg_c_S = (double *)(w + L.cg_c_S);
     ctx->cg_c_meta = (int32_t *)(w + L.cg_c_meta);
+    ctx->cg_thr = (uint32_t *)(w + L.cg_thr);
+    ctx->cg_seed_lp = (float *)(w + L.cg_seed_lp);
+    ctx->cg_seed_ids = (int32_t *)(w + L.cg_seed_ids);
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so

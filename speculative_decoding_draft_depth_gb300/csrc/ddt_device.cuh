@@ -30,6 +30,35 @@ DDT_DEVINL float ex2(float x)
     return y;
 }
 
+// packed fp32 pairs (two lanes of one 64-bit register)
+DDT_DEVINL uint64_t f2pack(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+DDT_DEVINL void f2unpack(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+DDT_DEVINL uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+DDT_DEVINL uint64_t f2add(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+// programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible; let the next grid start its
+// prologue (no-ops for a grid launched without the attribute)
+DDT_DEVINL void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DDT_DEVINL void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // streaming 16-byte global load that does not allocate in L1
 DDT_DEVINL uint4 ldg_stream(const void *p)
 {

@@ -32,6 +32,7 @@ constexpr int ATT_STAGES = 3;
 
 // parent-conditioned tree: most CTAs of its per-depth GEMM (partials per CTA)
 constexpr int CG_GRID_MAX = 256;
+constexpr int CG_NP_MAX = 128;  // parents of one depth of the conditioned tree (R * F)
 
 struct ddt_ctx {
     ddt_config cfg;  // with K resolved
@@ -70,6 +71,9 @@ struct ddt_ctx {
     double *cg_fr_S;         // [R_max, F]
     double *cg_c_S;          // [R_max, Cmax] candidate scores
     int32_t *cg_c_meta;      // [R_max, Cmax, 3] depth, parent candidate, token
+    uint32_t *cg_thr;        // [L, CG_NP_MAX] per-parent lower bounds of the k-th child (value keys)
+    float *cg_seed_lp;       // [R_max, L, K] log-probs of the draft's own top-K (unused)
+    int32_t *cg_seed_ids;    // [R_max, L, K] the draft's top-K columns per depth: bound seeds
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };

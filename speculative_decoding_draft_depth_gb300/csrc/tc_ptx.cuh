@@ -74,6 +74,35 @@ TC_DEVINL void tma_load_2d(uint32_t dst, const void *tmap, int x, int y, uint32_
         : "memory");
 }
 
+// the same with an L2 cache policy (createpolicy) for the loaded lines
+TC_DEVINL void tma_load_2d_hint(uint32_t dst, const void *tmap, int x, int y, uint32_t bar,
+                                uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// L2 policy: keep the lines resident ahead of normal traffic
+TC_DEVINL uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// contiguous global -> shared copy (16-byte aligned ends, size a multiple of 16)
+// that completes on an mbarrier's transaction count
+TC_DEVINL void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
 TC_DEVINL void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
@@ -86,6 +115,8 @@ TC_DEVINL void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// wait for every cp.async this thread issued
+TC_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // arrive on an mbarrier once every cp.async this thread issued so far has
 // landed (the barrier's expected count already includes this arrival)
 TC_DEVINL void cp_async_arrive_noinc(uint32_t bar)

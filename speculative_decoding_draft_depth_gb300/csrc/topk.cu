@@ -35,29 +35,6 @@ constexpr int SELECT_MAX = 512;  // above this many survivors, use the exact sea
 constexpr int VEC_CAP = 512;     // staged candidate vectors (more: the exact search)
 constexpr int IDX_PAD = 0x7FFFFFFF;  // id of a padding entry in a chunk list
 
-// packed fp32 pairs (two lanes of one 64-bit register)
-DDT_DEVINL uint64_t f2pack(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-DDT_DEVINL void f2unpack(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-DDT_DEVINL uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-DDT_DEVINL uint64_t f2add(uint64_t a, uint64_t b)
-{
-    uint64_t r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
 // 2^(x * log2 e - m * log2 e) for the two bf16 values of w (c2 = {log2 e, log2 e},
 // b2 = {-m log2 e, -m log2 e}), as a packed pair
 DDT_DEVINL uint64_t exp_pair(uint32_t w, uint64_t c2, uint64_t b2)
