@@ -213,13 +213,13 @@ def draw_round_inputs(cfg, seed=None):
                 agree=agree)
 
 
-def draw_markov_head(cfg, seed=None):
-    """The parent-conditioned tree's Markov head: W, E [V, H] bf16 N(0, 0.02),
-    and one anchor (root) token per request."""
+def draw_markov_head(cfg, seed=None, scale=0.02):
+    """The parent-conditioned tree's Markov head: W, E [V, H] bf16 N(0, scale)
+    (0.02 by default), and one anchor (root) token per request."""
     rng = np.random.default_rng([cfg.seed if seed is None else seed, 17])
     H = cfg.markov_dim
-    W = _normal_bf16(rng, (cfg.V, H), scale=0.02)
-    E = _normal_bf16(rng, (cfg.V, H), scale=0.02)
+    W = _normal_bf16(rng, (cfg.V, H), scale=scale)
+    E = _normal_bf16(rng, (cfg.V, H), scale=scale)
     anchors = rng.integers(0, cfg.V, size=cfg.R).astype(np.int32)
     return W, E, anchors
 

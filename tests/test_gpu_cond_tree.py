@@ -26,14 +26,21 @@ CASES = {
     "small": dict(name="treespark", R=3, L=4, V=1000, B=12, K=3, frontier=2, seed=21),
     "k1": dict(name="treespark", R=2, L=3, V=5000, B=5, K=1, frontier=4, seed=22),
     "wide_frontier": dict(name="treespark", R=4, L=5, V=3000, B=40, K=4, frontier=8, seed=23),
+    # a head whose bias is half the logits' spread: the seeded bounds are weak
+    "strong_head": dict(name="treespark", R=4, L=4, V=20000, B=24, K=4, frontier=4, seed=24,
+                        head_scale=0.3),
+    # V not a multiple of 8 (l by direct loads, a ragged last tile)
+    "ragged_v": dict(name="treespark", R=3, L=4, V=3001, B=16, K=3, frontier=3, seed=25),
+    # more requests than l stages hold, and seed rows that do not fit
+    "many_requests": dict(name="treespark", R=60, L=3, V=4096, B=10, K=2, frontier=2, seed=26),
 }
 
 
 class CondCase:
-    def __init__(self, cfg):
+    def __init__(self, cfg, head_scale=0.02):
         self.cfg = cfg
         self.inp = inp = synth.draw_round_inputs(cfg)
-        self.W, self.E, self.anchors = synth.draw_markov_head(cfg)
+        self.W, self.E, self.anchors = synth.draw_markov_head(cfg, scale=head_scale)
         ctx = self.ctx = make_ctx(cfg, inp)
         R, L, F, K, N = cfg.R, cfg.L, cfg.frontier, cfg.K, cfg.B
         P = N + 1
@@ -56,7 +63,8 @@ class CondCase:
 @pytest.fixture(scope="module", params=list(CASES))
 def case(request):
     kw = dict(CASES[request.param])
-    return CondCase(synth.config(kw.pop("name"), **kw))
+    scale = kw.pop("head_scale", 0.02)
+    return CondCase(synth.config(kw.pop("name"), **kw), head_scale=scale)
 
 
 def test_status_clean(case):
