@@ -190,8 +190,9 @@ def main():
     ap.add_argument("--no-next", action="store_true",
                     help="skip the timing of the NEXT rows (parent-conditioned tree)")
     ap.add_argument("--stage", default="round",
-                    choices=["round", "topk", "tree", "attention", "accept"],
-                    help="time one stage alone (small profiling cases)")
+                    choices=["round", "topk", "tree", "attention", "accept", "cond_tree"],
+                    help="time one stage alone (small profiling cases); cond_tree: the "
+                         "parent-conditioned tree's workload alone")
     ap.add_argument("--requests", type=int, default=0,
                     help="requests per round (default: the workload's 64)")
     args = ap.parse_args()
@@ -213,6 +214,14 @@ def main():
 
     import torch
     torch.cuda.set_device(local_rank)
+    if args.stage == "cond_tree":
+        from speculative_decoding_draft_depth_gb300 import ddt
+        ddt.load()
+        res = time_cond_tree(torch.device("cuda", local_rank), reps=max(args.steps, 1),
+                             cpu=not args.no_cpu_baseline)
+        if rank == 0:
+            print(json.dumps({"stage": "cond_tree", **res}))
+        return
     dist = None
     if world > 1:
         import torch.distributed as dist
