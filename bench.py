@@ -409,10 +409,14 @@ def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):
 
 
 def time_cond_tree(dev, reps=20, cpu=True):
-    """The parent-conditioned tree ("Robot2050/TreeSpark") on its own workload
-    (8 requests, 7 depths, V=151936, H=256, k=F=4, N=32): device time per
-    call, algorithmic bytes (W and the backbone rows once per depth), and the
-    oracle's time for one request scaled to the batch."""
+    """The parent-conditioned tree ("Robot2050/TreeSpark", items 1-2) on its own
+    workload (8 requests, 7 depths, V=151936, H=256, k=F=4, N=32, Qwen3-4B
+    attention at context 2048): the tree alone (ddt_build_tree_conditioned) and
+    the whole conditioned round (ddt_round_conditioned: the tree, then a4..a7),
+    each as device time per call over `reps` calls after 3 warm-up calls, with
+    algorithmic bytes (W and the backbone rows once per depth, then the
+    round's verification bytes), and the oracle's tree time for one request
+    scaled to the batch."""
     import torch
     from speculative_decoding_draft_depth_gb300 import ddt, synth
     cfg = synth.config("treespark")
@@ -430,32 +434,60 @@ def time_cond_tree(dev, reps=20, cpu=True):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
 
     ell, Wd, Ed, an = td(inp["draft_logits"]), td(W), td(E), td(anchors)
-    R, N, P = cfg.R, cfg.B, cfg.B + 1
-    i32 = dict(dtype=torch.int32, device=dev)
-    out = [torch.empty((R, N), **i32), torch.empty((R, P), **i32), torch.empty((R, P), **i32),
-           torch.empty((R,), **i32), torch.empty((R, P, (P + 31) // 32), **i32)]
+    R = cfg.R
+    bufs = ctx.alloc_outputs(R, device=dev)
+    d = {k: td(inp[k]) for k in ("q", "k_tree", "v_tree", "k_cache", "v_cache", "block_table",
+                                 "ctx_lens")}
+    ctx0 = d["ctx_lens"].clone()
+    bufs.update(d)
+    bufs["draft_logits"] = ell
 
-    def call():
-        ctx.ddt_build_tree_conditioned(ell, Wd, Ed, an, R, *out)
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
 
-    for _ in range(3):
-        call()
+    def tree():
+        ctx.ddt_build_tree_conditioned(ell, Wd, Ed, an, R, bufs["tree_tokens"], bufs["parents"],
+                                       bufs["depths"], bufs["n_nodes"], bufs["mask"])
+
+    ms = timed(tree)
+    # the synthetic target follows this tree (set-up, untimed)
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        call()
-    b.record()
-    torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / reps
+    target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+    bufs["target_logits"] = td(target.logits_for_tree(
+        bufs["tree_tokens"].cpu().numpy(), bufs["parents"].cpu().numpy(),
+        bufs["n_nodes"].cpu().numpy()))
+
+    def round_():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        ctx.ddt_round_conditioned(R, bufs, Wd, Ed, an)
+
+    ms_round = timed(round_)
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set in the conditioned round")
     nbytes = cfg.L * (cfg.V * cfg.markov_dim * 2 + R * cfg.V * 2) + R * (cfg.L * cfg.frontier *
                                                                         cfg.markov_dim * 2)
+    rb = round_bytes(cfg, inp["ctx_lens"], bufs["acc_len"].cpu().numpy())
+    nbytes_round = nbytes + rb["attention"] + rb["accept"]
     peak, _ = _peaks()
-    res = {"workload": "treespark: R=8, 7 depths, V=151936, H=256, k=4, F=4, N=32, bf16",
+    res = {"workload": "treespark: R=8, 7 depths, V=151936, H=256, k=4, F=4, N=32, "
+                       "Hq=32, Hkv=8, d=128, ctx 2048, bf16",
            "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
            "GBps": round(nbytes / (ms / 1e3) / 1e9, 1),
            "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / peak, 4),
-           "note": "W (78 MB) is read once per depth and fits in L2"}
+           "note": "W (78 MB) is read once per depth and fits in L2",
+           "round": {"ms": round(ms_round, 4), "rounds_per_s": round(1e3 / ms_round, 1),
+                     "algorithmic_bytes": int(nbytes_round),
+                     "GBps": round(nbytes_round / (ms_round / 1e3) / 1e9, 1),
+                     "frac_of_hbm": round(nbytes_round / (ms_round / 1e3) / 1e9 / peak, 4)}}
     if cpu:
         import oracle
         t0 = time.perf_counter()

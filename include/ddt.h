@@ -255,6 +255,19 @@ typedef struct ddt_round_args {
  * a6/a7 follow there. */
 ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *args, void *stream);
 
+/* The parent-conditioned round -- "Robot2050/TreeSpark", items 1 and 2 (the
+ * tree from one backbone pass with a first-order Markov head), then the same
+ * verification as ddt_round: the tree and its mask come from
+ * ddt_build_tree_conditioned on args->draft_logits (the backbone's per-depth
+ * logits l_d [R, L, V], bf16) with the head W, E [V, markov_dim] bf16 and the
+ * roots anchors [R] (the bonus tokens); a4..a7 follow as in ddt_round, with
+ * a5 beside the tree on a lowest-priority stream. args->top_lp and
+ * args->top_ids are not used (may be NULL); the tree has cfg.B nodes at
+ * most. Requires markov_dim > 0 (else DDT_EUNSUPPORTED); argument errors as
+ * for ddt_round and ddt_build_tree_conditioned. */
+ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *args, const uint16_t *W,
+                                 const uint16_t *E, const int32_t *anchors, void *stream);
+
 /* Wait for the context's device to finish all enqueued work, copy the
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);

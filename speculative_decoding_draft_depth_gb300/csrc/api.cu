@@ -523,6 +523,25 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
     return DDT_OK;
 }
 
+// a4 once the tree (ev_tree) and a5 (ev_join) are done, then a6/a7, on `s`
+static ddt_status round_verify(ddt_ctx *ctx, const ddt_round_args *a, cudaStream_t s)
+{
+    const int32_t R = a->R;
+    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_tree, 0));
+    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_join, 0));
+    if (a->att_event_begin)
+        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_begin, s));
+    DDT_TRY(launch_attention(ctx, a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache,
+                             a->block_table, a->ctx_lens, a->mask, R, a->attn_out, s));
+    if (a->att_event_end)
+        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_end, s));
+    DDT_TRY(launch_walk_compact(ctx, nullptr, true, a->target_argmax, a->tree_tokens, a->parents,
+                                a->n_nodes, R, a->acc_len, a->acc_nodes, a->acc_tokens, a->bonus,
+                                true, true, a->k_cache, a->v_cache, a->block_table, a->ctx_lens,
+                                a->k_tree, a->v_tree, s));
+    return DDT_OK;
+}
+
 ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *a, void *stream)
 {
     if (a == nullptr)
@@ -557,19 +576,50 @@ ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *a, void *stream)
     DDT_TRY(launch_build_tree(ctx, a->top_lp, a->top_ids, R, a->tree_tokens, a->parents,
                               a->depths, a->n_nodes, a->mask, ctx->hi));
     DDT_TRY(cudaEventRecord(ctx->ev_tree, ctx->hi));
-    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_tree, 0));
-    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_join, 0));
-    if (a->att_event_begin)
-        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_begin, s));
-    DDT_TRY(launch_attention(ctx, a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache,
-                             a->block_table, a->ctx_lens, a->mask, R, a->attn_out, s));
-    if (a->att_event_end)
-        DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_end, s));
-    DDT_TRY(launch_walk_compact(ctx, nullptr, true, a->target_argmax, a->tree_tokens, a->parents,
-                                a->n_nodes, R, a->acc_len, a->acc_nodes, a->acc_tokens, a->bonus,
-                                true, true, a->k_cache, a->v_cache, a->block_table, a->ctx_lens,
-                                a->k_tree, a->v_tree, s));
-    return DDT_OK;
+    return round_verify(ctx, a, s);
+}
+
+ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *a, const uint16_t *W,
+                                 const uint16_t *E, const int32_t *anchors, void *stream)
+{
+    if (a == nullptr)
+        return DDT_EINVAL;
+    const int32_t R = a->R;
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (ctx->cfg.markov_dim <= 0)
+        return DDT_EUNSUPPORTED;
+    if (R == 0)
+        return DDT_OK;
+    DDT_CHECK(a->draft_logits && aligned16(a->draft_logits) && W && E && anchors &&
+              aligned16(W) && aligned16(E) && aligned4(anchors));
+    DDT_CHECK(a->tree_tokens && a->parents && a->depths && a->n_nodes && aligned4(a->tree_tokens) &&
+              aligned4(a->parents) && aligned4(a->depths) && aligned4(a->n_nodes));
+    if ((st = chk_attn(a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache, a->block_table,
+                       a->ctx_lens, a->mask, a->attn_out)) != DDT_OK ||
+        (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
+                       a->acc_tokens, a->bonus)) != DDT_OK)
+        return st;
+    if (!a->target_logits || !aligned16(a->target_logits))
+        return DDT_EINVAL;
+    if (R * ctx->cfg.frontier > CG_NP_MAX)
+        return DDT_EUNSUPPORTED;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the conditioned tree (with its mask) on the highest-priority stream, a5
+    // beside it on the lowest; both join `s` before a4
+    DDT_TRY(cudaEventRecord(ctx->ev_fork, s));
+    DDT_TRY(cudaStreamWaitEvent(ctx->hi, ctx->ev_fork, 0));
+    DDT_TRY(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
+    DDT_TRY(launch_argmax_partials(ctx, a->target_logits, R, ctx->side));
+    DDT_TRY(cudaEventRecord(ctx->ev_join, ctx->side));
+    DDT_TRY(launch_cond_tree(ctx, (const uint16_t *)a->draft_logits, W, E, anchors, R, nullptr,
+                             nullptr, nullptr, a->tree_tokens, a->parents, a->depths, a->n_nodes,
+                             a->mask, ctx->hi));
+    DDT_TRY(cudaEventRecord(ctx->ev_tree, ctx->hi));
+    return round_verify(ctx, a, s);
 }
 
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out)

@@ -20,7 +20,8 @@ DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
 
 EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
            "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
-           "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_device_status",
+           "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_round_conditioned",
+           "ddt_device_status",
            "ddt_strerror", "ddt_last_cuda_error")
 
 
@@ -82,6 +83,7 @@ def load(path=LIB_PATH):
         "ddt_accept": ([_P, _P, _P, _P, _P, i32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
                        i32),
         "ddt_round": ([_P, ctypes.POINTER(RoundArgs), _P], i32),
+        "ddt_round_conditioned": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
         "ddt_last_cuda_error": ([], i32),
@@ -218,6 +220,22 @@ class Context:
             a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
             a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
         _check(_lib.ddt_round(self._h, ctypes.byref(a), _stream(stream)), "ddt_round")
+
+    def ddt_round_conditioned(self, R, bufs, W, E, anchors, stream=None, att_events=None):
+        """The parent-conditioned round: bufs as for ddt_round (draft_logits are
+        the backbone's per-depth logits; top_lp / top_ids unused), W, E [V, H]
+        bf16 and anchors [R] int32."""
+        a = RoundArgs()
+        a.R = R
+        for name, _ in RoundArgs._fields_[1:]:
+            if name.startswith("att_event"):
+                continue
+            setattr(a, name, _ptr(bufs.get(name)))
+        if att_events is not None:
+            a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
+            a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
+        _check(_lib.ddt_round_conditioned(self._h, ctypes.byref(a), _ptr(W), _ptr(E), _ptr(anchors),
+                                          _stream(stream)), "ddt_round_conditioned")
 
     def ddt_device_status(self):
         out = ctypes.c_int32(0)

@@ -68,6 +68,7 @@ def test_create_rejects_bad_config_without_a_gpu(lib):
 def test_calls_reject_null_context(lib):
     assert lib.ddt_topk_logprobs(None, None, 1, None, None, None) == ddt.EINVAL
     assert lib.ddt_round(None, None, None) == ddt.EINVAL
+    assert lib.ddt_round_conditioned(None, None, None, None, None, None) == ddt.EINVAL
     assert lib.ddt_device_status(None, None) == ddt.EINVAL
 
 
