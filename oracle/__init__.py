@@ -15,7 +15,10 @@ Pages cited (by title and section):
   "DDTree Explained: From Block Diffusion to Optimal Diffusion Draft Trees
       for Speculative Decoding", sections 3-5 (Prop. 1, Prop. 2, Lemma 1,
       Algorithm 1, implementation highlights).
-  "Robot2050/TreeSpark", item 4 and the batched engine description.
+  "Robot2050/TreeSpark", items 1, 2 and 4, and the batched engine
+      description.
+  "SparklingTree ...", "Building SparklingTree" and "Solving the candidate
+      tree construction" (the prefilter and the Markov table: NEXT row 2).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
 against something other than itself (closed forms, brute force, library
@@ -66,6 +69,12 @@ def lib():
         L.orc_cond_parent_lists.restype = i32
         L.orc_compact.argtypes = [p, p, p, i32, i64, p, p, p, p, p, i32, i32, i32, i32, i32, i32]
         L.orc_compact.restype = i32
+        L.orc_markov_table.argtypes = [p, i32, p, p, i32, p, i32, i32, i64, i32, i32, p, p]
+        L.orc_markov_table.restype = i32
+        L.orc_markov_tree.argtypes = [p, p, i32, i32, i32, i32, p, p, p, p, p, p]
+        L.orc_markov_tree.restype = i32
+        L.orc_markov_tree_bruteforce.argtypes = [p, p, i32, i32, i32, i64, p, p, p, p, p]
+        L.orc_markov_tree_bruteforce.restype = i64
         L.orc_num_threads.argtypes = []
         L.orc_num_threads.restype = i32
         _lib = L
@@ -333,3 +342,70 @@ def cond_parent_lists(ell, W, E, req, depth, tok, k):
     if rc:
         raise ValueError("bad arguments to cond_parent_lists")
     return lp, ids
+
+
+# ---------------------------------------------------------------- NEXT row 2
+def markov_table(ell, W, E, anchors, C):
+    """The SparklingTree prefilter and Markov table ("SparklingTree ...",
+    "Solving the candidate tree construction"): cand [R, L, C] the C best
+    tokens of every depth's logits (value desc, lower id first) and
+    tab [R, L, C, C] fp64 with tab[r, d, a, b] = lp_d(b | a), the log-softmax
+    over the kept tokens b of l_d[b] + W[b] . E[parent a] (parent a: the
+    anchor at d = 0, else the a-th kept token of depth d - 1; rows a >= 1 of
+    depth 0 are -inf)."""
+    ell = np.ascontiguousarray(ell)
+    W = np.ascontiguousarray(W)
+    E = np.ascontiguousarray(E)
+    anchors = np.ascontiguousarray(anchors, dtype=np.int32)
+    R, L, V = ell.shape
+    cand = np.empty((R, L, C), np.int32)
+    tab = np.empty((R, L, C, C), np.float64)
+    rc = lib().orc_markov_table(_ptr(ell), _logit_dtype(ell), _ptr(W), _ptr(E), _logit_dtype(W),
+                                _ptr(anchors), R, L, V, W.shape[1], C, _ptr(cand), _ptr(tab))
+    if rc:
+        raise ValueError("bad arguments to markov_table")
+    return cand, tab
+
+
+class MarkovTree:
+    """Outputs of the table heap for R requests (P = B + 1 positions)."""
+
+    def __init__(self, R, B):
+        P = B + 1
+        self.tokens = np.full((R, B), -1, np.int32)
+        self.parents = np.full((R, P), -1, np.int32)
+        self.depths = np.full((R, P), -1, np.int32)
+        self.S = np.zeros((R, P), np.float64)
+        self.cand = np.full((R, P), -1, np.int32)
+        self.n_nodes = np.zeros(R, np.int32)
+
+
+def markov_tree(cand, tab, B):
+    """Best-first tree over the table ("SparklingTree ...", "Building
+    SparklingTree", Steps 2-6, with each parent's list read from the table):
+    Algorithm 1 where a node's children are its table row ordered by
+    (lp desc, token asc). tab may be the GPU's fp32 table (widened exactly)."""
+    cand = np.ascontiguousarray(cand, dtype=np.int32)
+    tab = np.ascontiguousarray(tab, dtype=np.float64)
+    R, L, C = cand.shape
+    t = MarkovTree(R, B)
+    rc = lib().orc_markov_tree(_ptr(cand), _ptr(tab), R, L, C, B, _ptr(t.tokens), _ptr(t.parents),
+                               _ptr(t.depths), _ptr(t.S), _ptr(t.cand), _ptr(t.n_nodes))
+    if rc:
+        raise ValueError("bad arguments to markov_tree")
+    return t
+
+
+def markov_tree_bruteforce(cand, tab, B, max_prefixes=2_000_000):
+    """The same tree for one request by listing and sorting every prefix."""
+    cand = np.ascontiguousarray(cand, dtype=np.int32)
+    tab = np.ascontiguousarray(tab, dtype=np.float64)
+    R, L, C = cand.shape
+    assert R == 1
+    t = MarkovTree(1, B)
+    n = lib().orc_markov_tree_bruteforce(_ptr(cand), _ptr(tab), L, C, B, max_prefixes,
+                                         _ptr(t.tokens), _ptr(t.parents), _ptr(t.depths),
+                                         _ptr(t.S), _ptr(t.n_nodes))
+    if n < 0:
+        raise ValueError("too many prefixes for the brute force")
+    return t

@@ -867,3 +867,338 @@ int orc_cond_parent_lists(const void *ell, int ell_dtype, const void *W, const v
     (void)R;
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * NEXT row 2: the SparklingTree tree built from a table [SPARK, "Building
+ * SparklingTree", Steps 1-6, and "Solving the candidate tree construction":
+ * a top-C prefilter of every depth's logits, then a precomputed table of the
+ * Markov head's conditional rows that the heap only reads; the head of
+ * "First order markov model conditioning": a bias B(x_prev, .) =
+ * W1[x_prev] W2 on the next position's logits, written here as
+ *   z_d(b | a) = l_d[b] + sum_h W[b][h] E[a][h],   W, E [V, H]].
+ *
+ * Readings (the page gives the mechanism, not its arithmetic):
+ *   - prefilter: depth d keeps its C best tokens of l_d (value desc, lower
+ *     id first); every node's children are drawn from them;
+ *   - table: for depth d and parent candidate a (the anchor at d = 0, else
+ *     the a-th kept token of depth d-1),
+ *       lp_d(b | a) = z_d(b | a) - log sum_b' exp z_d(b' | a)
+ *     over the C kept tokens b' of depth d (the softmax is re-normalised
+ *     over what the prefilter kept); rows a >= 1 of depth 0 are -inf;
+ *   - heap: Algorithm 1 with a list per parent: a node's children are its
+ *     table row ordered by (lp desc, token id asc); the child of rank j
+ *     scores S(parent) + lp; pops go by (S desc, rank tuple asc, a prefix
+ *     before its extensions); node n is the n-th pop.
+ * ---------------------------------------------------------------------- */
+
+/* the C best entries of one logit row: value desc, lower id first */
+static void mk_prefilter_row(const void *ell, int dtype, int64_t base, int64_t V, int C,
+                             double *val, int32_t *out)
+{
+    for (int j = 0; j < C; ++j) {
+        val[j] = -INFINITY;
+        out[j] = -1;
+    }
+    for (int64_t v = 0; v < V; ++v) {
+        const double x = widen(ell, dtype, base + v);
+        if (out[C - 1] >= 0 && !(x > val[C - 1]))
+            continue;
+        int j = C - 1;
+        while (j > 0 && (out[j - 1] < 0 || x > val[j - 1])) {
+            val[j] = val[j - 1];
+            out[j] = out[j - 1];
+            --j;
+        }
+        val[j] = x;
+        out[j] = (int32_t)v;
+    }
+}
+
+/*
+ * ell [R, L, V] (dtype as widen), W and E [V, H] (w_dtype), anchors [R].
+ * Outputs: cand [R, L, C] the kept tokens of every depth (best first) and
+ * tab [R, L, C, C]: tab[r][d][a][b] = lp_d(b | a).
+ */
+int orc_markov_table(const void *ell, int ell_dtype, const void *W, const void *E, int w_dtype,
+                     const int32_t *anchors, int R, int L, int64_t V, int H, int C,
+                     int32_t *cand, double *tab)
+{
+    if (R < 1 || L < 1 || L > ORC_LMAX || C < 1 || C > V || H < 1)
+        return ORC_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t rd = 0; rd < (int64_t)R * L; ++rd) {
+        double *val = (double *)malloc(sizeof(double) * (size_t)C);
+        mk_prefilter_row(ell, ell_dtype, rd * V, V, C, val, cand + rd * C);
+        free(val);
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t rda = 0; rda < (int64_t)R * L * C; ++rda) {
+        const int64_t rd = rda / C;
+        const int a = (int)(rda % C);
+        const int r = (int)(rd / L), d = (int)(rd % L);
+        double *row = tab + rda * C;
+        const int parent = (d == 0) ? (a == 0 ? anchors[r] : -1)
+                                    : cand[((int64_t)r * L + d - 1) * C + a];
+        if (parent < 0 || parent >= V) {
+            for (int b = 0; b < C; ++b)
+                row[b] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int b = 0; b < C; ++b) {
+            const int tok = cand[rd * C + b];
+            double bias = 0.0;
+            for (int h = 0; h < H; ++h)
+                bias += widen(W, w_dtype, (int64_t)tok * H + h) * widen(E, w_dtype, (int64_t)parent * H + h);
+            row[b] = widen(ell, ell_dtype, rd * V + tok) + bias;
+            if (row[b] > m)
+                m = row[b];
+        }
+        double s = 0.0;
+        for (int b = 0; b < C; ++b)
+            s += exp(row[b] - m);
+        const double logz = m + log(s);
+        for (int b = 0; b < C; ++b)
+            row[b] -= logz;
+    }
+    return 0;
+}
+
+/* order of one table row: candidate indices by (lp desc, token id asc) */
+static void mk_sort_row(const double *row, const int32_t *toks, int C, int32_t *order)
+{
+    for (int j = 0; j < C; ++j) {
+        int32_t b = j;
+        int i = j;
+        while (i > 0) {
+            const int32_t c = order[i - 1];
+            const int before = row[b] > row[c] || (row[b] == row[c] && toks[b] < toks[c]);
+            if (!before)
+                break;
+            order[i] = c;
+            --i;
+        }
+        order[i] = b;
+    }
+}
+
+/*
+ * cand [R, L, C], tab [R, L, C, C] (lp, fp64; the GPU's fp32 values widen
+ * exactly). Outputs per request (P = B + 1): tree_tokens [R, B],
+ * parents / depths [R, P] (root 0, parents[0] = -1, depth 0), node_S [R, P],
+ * node_cand [R, P] (each node's index into its depth's kept tokens, -1 for
+ * the root) and n_nodes [R].
+ */
+int orc_markov_tree(const int32_t *cand, const double *tab, int R, int L, int C, int B,
+                    int32_t *tree_tokens, int32_t *parents, int32_t *depths, double *node_S,
+                    int32_t *node_cand, int32_t *n_nodes)
+{
+    if (R < 1 || L < 1 || L > ORC_LMAX || C < 1 || B < 1)
+        return ORC_BAD_ARG;
+    const int P = B + 1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        int32_t *tok = tree_tokens + (int64_t)r * B;
+        int32_t *par = parents + (int64_t)r * P;
+        int32_t *dep = depths + (int64_t)r * P;
+        double *ns = node_S + (int64_t)r * P;
+        int32_t *nc = node_cand + (int64_t)r * P;
+        for (int j = 0; j < B; ++j)
+            tok[j] = -1;
+        for (int j = 0; j < P; ++j) {
+            par[j] = -1;
+            dep[j] = -1;
+            ns[j] = 0.0;
+            nc[j] = -1;
+        }
+        dep[0] = 0;
+        /* each node's children: its row and that row's order */
+        const double **rows = (const double **)malloc(sizeof(double *) * (size_t)P);
+        int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)P * C);
+        heap_ent *heap = (heap_ent *)malloc(sizeof(heap_ent) * (size_t)(2 * B + 4));
+        int size = 0, count = 0;
+        /* the root's children: depth 0, parent candidate 0 (the anchor) */
+        rows[0] = tab + (((int64_t)r * L + 0) * C + 0) * C;
+        mk_sort_row(rows[0], cand + ((int64_t)r * L + 0) * C, C, order);
+        if (rows[0][order[0]] > -INFINITY) {
+            heap_ent e;
+            memset(&e, 0, sizeof e);
+            e.parent_S = 0.0;
+            e.S = rows[0][order[0]];
+            e.ranks[0] = 0;
+            e.len = 1;
+            e.parent = 0;
+            heap_push(heap, &size, &e);
+        }
+        while (size > 0 && count < B) {
+            heap_ent e = heap_pop(heap, &size);
+            const int depth = e.len, j = e.ranks[depth - 1], pn = e.parent;
+            const int b = order[(int64_t)pn * C + j];
+            const int node = count + 1;
+            tok[count] = cand[((int64_t)r * L + depth - 1) * C + b];
+            par[node] = pn;
+            dep[node] = depth;
+            ns[node] = e.S;
+            nc[node] = b;
+            ++count;
+            if (j + 1 < C) {
+                const double lp = rows[pn][order[(int64_t)pn * C + j + 1]];
+                if (lp > -INFINITY) {
+                    heap_ent s = e;
+                    s.ranks[depth - 1] = j + 1;
+                    s.S = e.parent_S + lp;
+                    heap_push(heap, &size, &s);
+                }
+            }
+            if (depth < L) {
+                rows[node] = tab + (((int64_t)r * L + depth) * C + b) * C;
+                mk_sort_row(rows[node], cand + ((int64_t)r * L + depth) * C, C,
+                            order + (int64_t)node * C);
+                const double lp = rows[node][order[(int64_t)node * C]];
+                if (lp > -INFINITY) {
+                    heap_ent c = e;
+                    c.ranks[depth] = 0;
+                    c.len = depth + 1;
+                    c.parent = node;
+                    c.parent_S = e.S;
+                    c.S = e.S + lp;
+                    heap_push(heap, &size, &c);
+                }
+            }
+        }
+        n_nodes[r] = count;
+        free(heap);
+        free(order);
+        free(rows);
+    }
+    return 0;
+}
+
+/*
+ * Second, independent construction for one request of a small table: list
+ * every prefix of depth 1..L over every rank, score it left to right through
+ * the per-parent orders, sort the whole list by (S desc, rank tuple asc,
+ * shorter first) and keep the first B [DDTX section 3, Prop. 2, with each
+ * parent's own list]. Returns the number of prefixes, or -1 above
+ * max_prefixes.
+ */
+int64_t orc_markov_tree_bruteforce(const int32_t *cand, const double *tab, int L, int C, int B,
+                                   int64_t max_prefixes, int32_t *tree_tokens, int32_t *parents,
+                                   int32_t *depths, double *node_S, int32_t *n_nodes)
+{
+    if (L < 1 || L > ORC_LMAX || C < 1 || B < 1)
+        return -1;
+    int64_t total = 0, layer = 1;
+    for (int d = 1; d <= L; ++d) {
+        layer *= C;
+        total += layer;
+        if (total > max_prefixes)
+            return -1;
+    }
+    /* the order of every row of the table */
+    int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)L * C * C);
+    for (int d = 0; d < L; ++d)
+        for (int a = 0; a < C; ++a)
+            mk_sort_row(tab + ((int64_t)d * C + a) * C, cand + (int64_t)d * C, C,
+                        order + ((int64_t)d * C + a) * C);
+    pref_ent *all = (pref_ent *)calloc((size_t)total, sizeof(pref_ent));
+    int32_t *last_b = (int32_t *)calloc((size_t)total, sizeof(int32_t));
+    int64_t n = 0;
+    int32_t digits[ORC_LMAX];
+    for (int d = 1; d <= L; ++d) {
+        for (int i = 0; i < d; ++i)
+            digits[i] = 0;
+        for (;;) {
+            double S = 0.0;
+            int a = 0, b = -1, ok = 1;
+            for (int i = 0; i < d; ++i) {
+                b = order[((int64_t)i * C + a) * C + digits[i]];
+                const double lp = tab[((int64_t)i * C + a) * C + b];
+                if (!(lp > -INFINITY)) {
+                    ok = 0;
+                    break;
+                }
+                S = S + lp;
+                a = b;
+            }
+            if (ok) {
+                pref_ent *p = &all[n];
+                p->len = d;
+                p->S = S;
+                for (int i = 0; i < d; ++i)
+                    p->ranks[i] = digits[i];
+                last_b[n] = cand[(int64_t)(d - 1) * C + b];
+                ++n;
+            }
+            int i = d - 1;
+            while (i >= 0 && ++digits[i] == C) {
+                digits[i] = 0;
+                --i;
+            }
+            if (i < 0)
+                break;
+        }
+    }
+    /* sort indices by the prefix order, keeping each prefix's token */
+    int64_t *idx = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    pref_ent *sorted = (pref_ent *)malloc(sizeof(pref_ent) * (size_t)(n > 0 ? n : 1));
+    for (int64_t i = 0; i < n; ++i)
+        idx[i] = i;
+    /* insertion sort: n is small here */
+    for (int64_t i = 1; i < n; ++i) {
+        const int64_t x = idx[i];
+        int64_t j = i;
+        while (j > 0 && pref_cmp(&all[x], &all[idx[j - 1]]) < 0) {
+            idx[j] = idx[j - 1];
+            --j;
+        }
+        idx[j] = x;
+    }
+    for (int64_t i = 0; i < n; ++i)
+        sorted[i] = all[idx[i]];
+    const int P = B + 1;
+    const int take = (int)(n < B ? n : B);
+    for (int j = 0; j < B; ++j)
+        tree_tokens[j] = -1;
+    for (int j = 0; j < P; ++j) {
+        parents[j] = -1;
+        depths[j] = -1;
+        node_S[j] = 0.0;
+    }
+    depths[0] = 0;
+    for (int j = 0; j < take; ++j) {
+        const pref_ent *p = &sorted[j];
+        const int node = j + 1;
+        tree_tokens[j] = last_b[idx[j]];
+        depths[node] = p->len;
+        node_S[node] = p->S;
+        int parent = -1;
+        if (p->len == 1) {
+            parent = 0;
+        } else {
+            for (int q = 0; q < j; ++q) {
+                const pref_ent *c = &sorted[q];
+                if (c->len != p->len - 1)
+                    continue;
+                int same = 1;
+                for (int i = 0; i < c->len; ++i)
+                    if (c->ranks[i] != p->ranks[i]) {
+                        same = 0;
+                        break;
+                    }
+                if (same) {
+                    parent = q + 1;
+                    break;
+                }
+            }
+        }
+        parents[node] = parent;
+    }
+    *n_nodes = take;
+    free(sorted);
+    free(idx);
+    free(last_b);
+    free(all);
+    free(order);
+    return n;
+}

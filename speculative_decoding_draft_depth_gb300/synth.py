@@ -25,6 +25,9 @@ draws stand in for them):
            children per parent, frontier F=4, N=32 nodes; backbone logits
            bf16 N(0,1)*3, Markov head W and embeddings E bf16 N(0, 0.02)
            [V, 256], anchors uniform; Qwen3-4B attention, ctx 2048  (seed 2)
+  sparkling R=64, L=15, V=151936, the SparklingTree table tree: top-C=128
+           prefilter per depth, Markov head W, E bf16 N(0, 0.02) [V, 256],
+           budget B=64; logits, contexts and agreement as batch64  (seed 5)
 """
 from dataclasses import dataclass, field, replace
 
@@ -57,6 +60,7 @@ class RoundConfig:
     spare_pages: int = 8
     markov_dim: int = 0  # H of the parent-conditioned tree's Markov head
     frontier: int = 0  # F of the parent-conditioned tree
+    prefilter: int = 0  # C of the SparklingTree table tree (kept tokens per depth)
 
     @property
     def P(self):
@@ -86,6 +90,10 @@ CONFIGS = {
                              d=128, page=16, logit_dtype="bf16", ctx_kind="fixed",
                              ctx_args=(2048,), seed=2, boost=False, agree_kind="const",
                              agree_args=(0.75,), markov_dim=256, frontier=4),
+    "sparkling": RoundConfig("sparkling", R=64, L=15, V=VOCAB_QWEN3, B=64, K=64, Hq=32, Hkv=8,
+                             d=128, page=16, logit_dtype="bf16", ctx_kind="uniform",
+                             ctx_args=(512, 16384), seed=5, agree_kind="per_request",
+                             agree_args=(0.5, 0.9, 0.03), markov_dim=256, prefilter=128),
 }
 
 
