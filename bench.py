@@ -190,7 +190,8 @@ def main():
     ap.add_argument("--no-next", action="store_true",
                     help="skip the timing of the NEXT rows (parent-conditioned tree)")
     ap.add_argument("--stage", default="round",
-                    choices=["round", "topk", "tree", "attention", "accept", "cond_tree"],
+                    choices=["round", "topk", "tree", "attention", "accept", "cond_tree",
+                             "markov"],
                     help="time one stage alone (small profiling cases); cond_tree: the "
                          "parent-conditioned tree's workload alone")
     ap.add_argument("--requests", type=int, default=0,
@@ -214,13 +215,14 @@ def main():
 
     import torch
     torch.cuda.set_device(local_rank)
-    if args.stage == "cond_tree":
+    if args.stage in ("cond_tree", "markov"):
         from speculative_decoding_draft_depth_gb300 import ddt
         ddt.load()
-        res = time_cond_tree(torch.device("cuda", local_rank), reps=max(args.steps, 1),
-                             cpu=not args.no_cpu_baseline)
+        fn = time_cond_tree if args.stage == "cond_tree" else time_markov
+        res = fn(torch.device("cuda", local_rank), reps=max(args.steps, 1),
+                 cpu=not args.no_cpu_baseline)
         if rank == 0:
-            print(json.dumps({"stage": "cond_tree", **res}))
+            print(json.dumps({"stage": args.stage, **res}))
         return
     dist = None
     if world > 1:
@@ -345,7 +347,8 @@ def main():
            "acceptance": {"mean_acc_len": float(np.mean(acc_len))}}
 
     if rank == 0 and not args.no_next:
-        out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline)}
+        out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline),
+                            "markov_table_tree": time_markov(dev, cpu=not args.no_cpu_baseline)}
     if not args.no_e2e:
         out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
                               steps=max(10, min(args.steps, 50)))
@@ -496,6 +499,100 @@ def time_cond_tree(dev, reps=20, cpu=True):
         sec = (time.perf_counter() - t0) * R
         res["cpu_oracle_ms"] = round(sec * 1e3, 1)
         res["cpu_oracle_sample"] = "1 of 8 requests, scaled"
+    return res
+
+
+def time_markov(dev, reps=20, cpu=True):
+    """The SparklingTree table tree ("SparklingTree ...", "Solving the
+    candidate tree construction") on its workload (R=64, L=15, V=151936,
+    C=128, B=64, H=256): the prefilter + table (ddt_markov_table), the tree
+    over the table (ddt_build_tree_markov) and the whole round
+    (ddt_round_markov: both, then a4..a7), each as device time per call over
+    `reps` calls after 3 warm-up calls, with algorithmic bytes; and the
+    oracle's table + tree time for one request scaled to the batch."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import ddt, synth
+    cfg = synth.config("sparkling")
+    inp = synth.draw_round_inputs(cfg)
+    W, E, anchors = synth.draw_markov_head(cfg)
+    c = ddt.make_config(R_max=cfg.R, L=cfg.L, V=cfg.V, B=cfg.B, K=cfg.K, Hq=cfg.Hq, Hkv=cfg.Hkv,
+                        d=cfg.d, page_size=cfg.page,
+                        max_pages_per_req=inp["block_table"].shape[1],
+                        num_pages=inp["k_cache"].shape[0], markov_dim=cfg.markov_dim,
+                        prefilter=cfg.prefilter)
+    ctx = ddt.Context(c)
+
+    def td(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    R, L, V, C, H, B = cfg.R, cfg.L, cfg.V, cfg.prefilter, cfg.markov_dim, cfg.B
+    ell, Wd, Ed, an = td(inp["draft_logits"]), td(W), td(E), td(anchors)
+    cand = torch.empty((R, L, C), dtype=torch.int32, device=dev)
+    tab = torch.empty((R, L, C, C), dtype=torch.float32, device=dev)
+    bufs = ctx.alloc_outputs(R, device=dev)
+    d = {k: td(inp[k]) for k in ("q", "k_tree", "v_tree", "k_cache", "v_cache", "block_table",
+                                 "ctx_lens")}
+    ctx0 = d["ctx_lens"].clone()
+    bufs.update(d)
+    bufs["draft_logits"] = ell
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    ms_table = timed(lambda: ctx.ddt_markov_table(ell, Wd, Ed, an, R, cand, tab))
+    ms_tree = timed(lambda: ctx.ddt_build_tree_markov(
+        cand, tab, R, bufs["tree_tokens"], bufs["parents"], bufs["depths"], bufs["n_nodes"],
+        bufs["mask"]))
+    torch.cuda.synchronize()
+    target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+    bufs["target_logits"] = td(target.logits_for_tree(
+        bufs["tree_tokens"].cpu().numpy(), bufs["parents"].cpu().numpy(),
+        bufs["n_nodes"].cpu().numpy()))
+
+    def round_():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        ctx.ddt_round_markov(R, bufs, Wd, Ed, an)
+
+    ms_round = timed(round_)
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set in the table-tree round")
+    # algorithmic bytes: the logits once (prefilter), the kept tokens' W rows
+    # and the parents' E rows (one parent at depth 0), the table written once;
+    # the tree reads the rows of the nodes it expands
+    b_table = (R * L * V * 2 + R * L * C * H * 2 + R * (1 + (L - 1) * C) * H * 2
+               + R * L * C * 4 + R * L * C * C * 4)
+    b_tree = R * L * C * 4 + R * (B + 1) * C * 4 + R * (B + 2 * (B + 1) + 1) * 4
+    rb = round_bytes(cfg, inp["ctx_lens"], bufs["acc_len"].cpu().numpy())
+    b_round = b_table + b_tree + rb["attention"] + rb["accept"]
+    peak, _ = _peaks()
+
+    def rate(nbytes, ms):
+        return {"ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                "GBps": round(nbytes / (ms / 1e3) / 1e9, 1),
+                "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / peak, 4)}
+
+    res = {"workload": "sparkling: R=64, L=15, V=151936, C=128, B=64, H=256, Hq=32, Hkv=8, "
+                       "d=128, ctx~U[512,16384], bf16",
+           "table": rate(b_table, ms_table), "tree": rate(b_tree, ms_tree),
+           "round": dict(rate(b_round, ms_round), rounds_per_s=round(1e3 / ms_round, 1))}
+    if cpu:
+        import oracle
+        t0 = time.perf_counter()
+        oc, ot = oracle.markov_table(inp["draft_logits"][:1], W, E, anchors[:1], C)
+        oracle.markov_tree(oc, ot, B)
+        sec = (time.perf_counter() - t0) * R
+        res["cpu_oracle_ms"] = round(sec * 1e3, 1)
+        res["cpu_oracle_sample"] = "1 of 64 requests (table + tree), scaled"
     return res
 
 

@@ -88,6 +88,10 @@ typedef struct ddt_config {
     /* parent-conditioned tree (ddt_build_tree_conditioned); 0 = not used */
     int32_t markov_dim;        /* H of the Markov head W, E [V, H]: 64..256, multiple of 64 */
     int32_t frontier;          /* F: parents kept per depth (1..8); F * K <= 32 */
+    /* SparklingTree table tree (ddt_markov_table, ddt_build_tree_markov); 0 =
+     * not used. C: tokens kept per depth by the prefilter, 1..128 and <= V;
+     * needs markov_dim > 0 and bf16 draft logits. */
+    int32_t prefilter;
 } ddt_config;
 
 typedef struct ddt_ctx ddt_ctx; /* opaque */
@@ -267,6 +271,45 @@ ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *args, void *stream);
  * for ddt_round and ddt_build_tree_conditioned. */
 ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *args, const uint16_t *W,
                                  const uint16_t *E, const int32_t *anchors, void *stream);
+
+/* NEXT row 2 -- "SparklingTree: 30-40% faster speculative decoding over
+ * DSpark", sections "Solving the candidate tree construction" (a top-k
+ * prefilter of every position's logits on the GPU, then a precomputed table
+ * of the Markov model's conditional rows that the tree loop only reads) and
+ * "Building SparklingTree" (the heap loop), with the Markov head of "First
+ * order markov model conditioning" (a bias W1[x_prev] W2 on the next
+ * position's logits, here z_d(b | a) = l_d[b] + W[b] . E[a]).
+ *
+ * ddt_markov_table: for every request r and depth d, cand_ids[r, d, :] are
+ * the C = cfg.prefilter largest draft_logits[r, d, :] (bf16 [R, L, V]; value
+ * descending, lower id first). tab_lp[r, d, a, b] (f32 [R, L, C, C]) is
+ * log-softmax over b of l_d[cand b] + W[cand b] . E[parent a], where parent a
+ * is anchors[r] at d = 0 (row a = 0; rows a >= 1 are -inf) and the a-th kept
+ * token of depth d - 1 otherwise; the softmax runs over the C kept tokens.
+ * W, E: [V, markov_dim] bf16, 16-byte aligned; anchors [R] int32. The
+ * products run on the tensor cores (bf16 in, fp32 accumulation). */
+ddt_status ddt_markov_table(ddt_ctx *ctx, const void *draft_logits, const uint16_t *W,
+                            const uint16_t *E, const int32_t *anchors, int32_t R,
+                            int32_t *cand_ids, float *tab_lp, void *stream);
+
+/* ddt_build_tree_markov: Algorithm 1 over the table: a node's children are
+ * its row of tab_lp (the root's: row 0 of depth 0; a node with candidate
+ * index b at depth d: row b of depth d) in order of (lp descending, token id
+ * ascending); a child scores S(parent) + lp in fp64; pops go by (S
+ * descending, rank tuple ascending, a prefix before its extensions); node n
+ * is the n-th pop. Outputs as ddt_build_tree (tree_tokens [R, B], parents /
+ * depths [R, P], n_nodes [R]) and, when mask is not NULL, the ancestor mask
+ * [R, P, W] of ddt_build_mask. */
+ddt_status ddt_build_tree_markov(ddt_ctx *ctx, const int32_t *cand_ids, const float *tab_lp,
+                                 int32_t R, int32_t *tree_tokens, int32_t *parents,
+                                 int32_t *depths, int32_t *n_nodes, uint32_t *mask, void *stream);
+
+/* The SparklingTree round: ddt_markov_table into the context's workspace,
+ * ddt_build_tree_markov (with the mask), then a4..a7 as in ddt_round, with a5
+ * beside the tree on a lowest-priority stream. args->draft_logits are the
+ * drafter's per-depth logits; args->top_lp / top_ids are not used. */
+ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *args, const uint16_t *W,
+                            const uint16_t *E, const int32_t *anchors, void *stream);
 
 /* Wait for the context's device to finish all enqueued work, copy the
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */

@@ -48,9 +48,17 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
     if (max_ctx > (int64_t)64 * ATT_CHUNK || c.R_max > 2048)
         return DDT_EUNSUPPORTED;
-    if (c.markov_dim < 0 || c.frontier < 0)
+    if (c.markov_dim < 0 || c.frontier < 0 || c.prefilter < 0)
         return DDT_EINVAL;
-    if (c.markov_dim > 0 && (c.draft_dtype != DDT_BF16 || !cond_tree_supported(c)))
+    if ((c.frontier > 0 || c.prefilter > 0) && c.markov_dim == 0)
+        return DDT_EINVAL;
+    if (c.markov_dim > 0 && c.frontier == 0 && c.prefilter == 0)
+        return DDT_EINVAL;
+    if (c.markov_dim > 0 && c.draft_dtype != DDT_BF16)
+        return DDT_EUNSUPPORTED;
+    if (c.frontier > 0 && !cond_tree_supported(c))
+        return DDT_EUNSUPPORTED;
+    if (c.prefilter > 0 && (c.prefilter > c.V || !markov_supported(c)))
         return DDT_EUNSUPPORTED;
     *out = c;
     return DDT_OK;
@@ -59,7 +67,8 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
-        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, total;
+        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
+        mk_tk_lp, mk_tk_val, mk_tk_idx, mk_tk_ms, mk_tk_cnt, total;
     int tk_nch, am_nch, rowgroups, max_items;
 };
 
@@ -120,6 +129,16 @@ Layout layout_for(const ddt_config &c)
     const size_t nseed = c.markov_dim > 0 ? (size_t)c.R_max * c.L * c.K : 0;
     L.cg_seed_lp = take(nseed * sizeof(float));
     L.cg_seed_ids = take(nseed * sizeof(int32_t));
+    // SparklingTree table tree: the round's table and the prefilter's scratch
+    const size_t mrows = c.prefilter > 0 ? (size_t)c.R_max * c.L : 0;
+    const size_t C = (size_t)c.prefilter;
+    L.mk_cand = take(mrows * C * sizeof(int32_t));
+    L.mk_tab = take(mrows * C * C * sizeof(float));
+    L.mk_tk_lp = take(mrows * C * sizeof(float));
+    L.mk_tk_val = take(mrows * L.tk_nch * C * sizeof(float));
+    L.mk_tk_idx = take(mrows * L.tk_nch * C * sizeof(int32_t));
+    L.mk_tk_ms = take(mrows * L.tk_nch * sizeof(float2));
+    L.mk_tk_cnt = take(mrows * sizeof(unsigned));
     L.total = off;
     return L;
 }
@@ -280,6 +299,14 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->cg_thr = (uint32_t *)(w + L.cg_thr);
     ctx->cg_seed_lp = (float *)(w + L.cg_seed_lp);
     ctx->cg_seed_ids = (int32_t *)(w + L.cg_seed_ids);
+    ctx->mk_cand = (int32_t *)(w + L.mk_cand);
+    ctx->mk_tab = (float *)(w + L.mk_tab);
+    ctx->mk_tk_lp = (float *)(w + L.mk_tk_lp);
+    ctx->mk_tk_val = (float *)(w + L.mk_tk_val);
+    ctx->mk_tk_idx = (int32_t *)(w + L.mk_tk_idx);
+    ctx->mk_tk_ms = (float2 *)(w + L.mk_tk_ms);
+    ctx->mk_tk_cnt = (unsigned *)(w + L.mk_tk_cnt);
+    ctx->mk_nch = L.tk_nch;
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so
@@ -378,7 +405,7 @@ ddt_status ddt_build_tree_conditioned(ddt_ctx *ctx, const void *draft_logits, co
     ddt_status st = check_R(ctx, R);
     if (st != DDT_OK)
         return st;
-    if (ctx->cfg.markov_dim <= 0)
+    if (ctx->cfg.markov_dim <= 0 || ctx->cfg.frontier <= 0)
         return DDT_EUNSUPPORTED;
     if (R == 0)
         return DDT_OK;
@@ -588,7 +615,7 @@ ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *a, const ui
     ddt_status st = check_R(ctx, R);
     if (st != DDT_OK)
         return st;
-    if (ctx->cfg.markov_dim <= 0)
+    if (ctx->cfg.markov_dim <= 0 || ctx->cfg.frontier <= 0)
         return DDT_EUNSUPPORTED;
     if (R == 0)
         return DDT_OK;
@@ -618,6 +645,91 @@ ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *a, const ui
     DDT_TRY(launch_cond_tree(ctx, (const uint16_t *)a->draft_logits, W, E, anchors, R, nullptr,
                              nullptr, nullptr, a->tree_tokens, a->parents, a->depths, a->n_nodes,
                              a->mask, ctx->hi));
+    DDT_TRY(cudaEventRecord(ctx->ev_tree, ctx->hi));
+    return round_verify(ctx, a, s);
+}
+
+ddt_status ddt_markov_table(ddt_ctx *ctx, const void *draft_logits, const uint16_t *W,
+                            const uint16_t *E, const int32_t *anchors, int32_t R,
+                            int32_t *cand_ids, float *tab_lp, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (ctx->cfg.prefilter <= 0)
+        return DDT_EUNSUPPORTED;
+    if (R == 0)
+        return DDT_OK;
+    DDT_CHECK(draft_logits && W && E && anchors && cand_ids && tab_lp);
+    DDT_CHECK(aligned16(draft_logits) && aligned16(W) && aligned16(E) && aligned4(anchors) &&
+              aligned4(cand_ids) && aligned16(tab_lp));
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_markov_table(ctx, (const uint16_t *)draft_logits, W, E, anchors, R, cand_ids,
+                                tab_lp, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_build_tree_markov(ddt_ctx *ctx, const int32_t *cand_ids, const float *tab_lp,
+                                 int32_t R, int32_t *tree_tokens, int32_t *parents,
+                                 int32_t *depths, int32_t *n_nodes, uint32_t *mask, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (ctx->cfg.prefilter <= 0)
+        return DDT_EUNSUPPORTED;
+    if (R == 0)
+        return DDT_OK;
+    DDT_CHECK(cand_ids && tab_lp && tree_tokens && parents && depths && n_nodes);
+    DDT_CHECK(aligned4(cand_ids) && aligned16(tab_lp) && aligned4(tree_tokens) &&
+              aligned4(parents) && aligned4(depths) && aligned4(n_nodes));
+    DDT_CHECK(!mask || aligned4(mask));
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_markov_tree(ctx, cand_ids, tab_lp, R, tree_tokens, parents, depths, n_nodes,
+                               mask, (cudaStream_t)stream));
+    return DDT_OK;
+}
+
+ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *a, const uint16_t *W,
+                            const uint16_t *E, const int32_t *anchors, void *stream)
+{
+    if (a == nullptr)
+        return DDT_EINVAL;
+    const int32_t R = a->R;
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (ctx->cfg.prefilter <= 0)
+        return DDT_EUNSUPPORTED;
+    if (R == 0)
+        return DDT_OK;
+    DDT_CHECK(a->draft_logits && aligned16(a->draft_logits) && W && E && anchors &&
+              aligned16(W) && aligned16(E) && aligned4(anchors));
+    DDT_CHECK(a->tree_tokens && a->parents && a->depths && a->n_nodes && aligned4(a->tree_tokens) &&
+              aligned4(a->parents) && aligned4(a->depths) && aligned4(a->n_nodes));
+    if ((st = chk_attn(a->q, a->k_tree, a->v_tree, a->k_cache, a->v_cache, a->block_table,
+                       a->ctx_lens, a->mask, a->attn_out)) != DDT_OK ||
+        (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
+                       a->acc_tokens, a->bonus)) != DDT_OK)
+        return st;
+    if (!a->target_logits || !aligned16(a->target_logits))
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    // the table and its tree (with the mask) on the highest-priority stream,
+    // a5 beside them on the lowest; both join `s` before a4
+    DDT_TRY(cudaEventRecord(ctx->ev_fork, s));
+    DDT_TRY(cudaStreamWaitEvent(ctx->hi, ctx->ev_fork, 0));
+    DDT_TRY(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
+    DDT_TRY(launch_markov_table(ctx, (const uint16_t *)a->draft_logits, W, E, anchors, R,
+                                ctx->mk_cand, ctx->mk_tab, ctx->hi));
+    DDT_TRY(launch_argmax_partials(ctx, a->target_logits, R, ctx->side));
+    DDT_TRY(cudaEventRecord(ctx->ev_join, ctx->side));
+    DDT_TRY(launch_markov_tree(ctx, ctx->mk_cand, ctx->mk_tab, R, a->tree_tokens, a->parents,
+                               a->depths, a->n_nodes, a->mask, ctx->hi));
     DDT_TRY(cudaEventRecord(ctx->ev_tree, ctx->hi));
     return round_verify(ctx, a, s);
 }

@@ -74,6 +74,15 @@ struct ddt_ctx {
     uint32_t *cg_thr;        // [L, CG_NP_MAX] per-parent lower bounds of the k-th child (value keys)
     float *cg_seed_lp;       // [R_max, L, K] log-probs of the draft's own top-K (unused)
     int32_t *cg_seed_ids;    // [R_max, L, K] the draft's top-K columns per depth: bound seeds
+    // SparklingTree table tree (prefilter > 0)
+    int32_t *mk_cand;        // [R_max, L, C] kept tokens (ddt_round_markov)
+    float *mk_tab;           // [R_max, L, C, C] the table (ddt_round_markov)
+    float *mk_tk_lp;         // [R_max, L, C] the prefilter's log-probs (unused)
+    float *mk_tk_val;        // prefilter scratch: [R_max * L, nch, C]
+    int32_t *mk_tk_idx;      // [R_max * L, nch, C]
+    float2 *mk_tk_ms;        // [R_max * L, nch]
+    unsigned *mk_tk_cnt;     // [R_max * L]
+    int mk_nch;              // prefilter chunks per row
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };
@@ -120,6 +129,15 @@ cudaError_t launch_cond_tree(const ddt_ctx *c, const uint16_t *ell, const uint16
                              int32_t *cand_ids, int32_t *frontier_tok, int32_t *tree_tokens,
                              int32_t *parents, int32_t *depths, int32_t *n_nodes, uint32_t *mask,
                              cudaStream_t s);
+
+// the SparklingTree table tree (markov.cu)
+bool markov_supported(const ddt_config &cfg);
+cudaError_t launch_markov_table(const ddt_ctx *c, const uint16_t *ell, const uint16_t *W,
+                                const uint16_t *E, const int32_t *anchors, int R, int32_t *cand,
+                                float *tab, cudaStream_t s);
+cudaError_t launch_markov_tree(const ddt_ctx *c, const int32_t *cand, const float *tab, int R,
+                               int32_t *tree_tokens, int32_t *parents, int32_t *depths,
+                               int32_t *n_nodes, uint32_t *mask, cudaStream_t s);
 
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,

@@ -21,7 +21,7 @@ DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
 EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
            "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
            "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_round_conditioned",
-           "ddt_device_status",
+           "ddt_markov_table", "ddt_build_tree_markov", "ddt_round_markov", "ddt_device_status",
            "ddt_strerror", "ddt_last_cuda_error")
 
 
@@ -41,7 +41,8 @@ class Config(ctypes.Structure):
                 ("Hkv", ctypes.c_int32), ("d", ctypes.c_int32), ("page_size", ctypes.c_int32),
                 ("max_pages_per_req", ctypes.c_int32), ("num_pages", ctypes.c_int64),
                 ("draft_dtype", ctypes.c_int32), ("target_dtype", ctypes.c_int32),
-                ("markov_dim", ctypes.c_int32), ("frontier", ctypes.c_int32)]
+                ("markov_dim", ctypes.c_int32), ("frontier", ctypes.c_int32),
+                ("prefilter", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -84,6 +85,9 @@ def load(path=LIB_PATH):
                        i32),
         "ddt_round": ([_P, ctypes.POINTER(RoundArgs), _P], i32),
         "ddt_round_conditioned": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
+        "ddt_markov_table": ([_P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
+        "ddt_build_tree_markov": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
+        "ddt_round_markov": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
         "ddt_last_cuda_error": ([], i32),
@@ -118,9 +122,9 @@ def _check(status, where):
 
 
 def make_config(R_max, L, V, B, Hq, Hkv, d, page_size, max_pages_per_req, num_pages, K=0,
-                draft_dtype=BF16, target_dtype=BF16, markov_dim=0, frontier=0):
+                draft_dtype=BF16, target_dtype=BF16, markov_dim=0, frontier=0, prefilter=0):
     return Config(R_max, L, V, B, K, Hq, Hkv, d, page_size, max_pages_per_req, num_pages,
-                  draft_dtype, target_dtype, markov_dim, frontier)
+                  draft_dtype, target_dtype, markov_dim, frontier, prefilter)
 
 
 def workspace_bytes(cfg):
@@ -220,6 +224,37 @@ class Context:
             a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
             a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
         _check(_lib.ddt_round(self._h, ctypes.byref(a), _stream(stream)), "ddt_round")
+
+    def ddt_markov_table(self, draft_logits, W, E, anchors, R, cand_ids, tab_lp, stream=None):
+        _check(_lib.ddt_markov_table(self._h, _ptr(draft_logits), _ptr(W), _ptr(E), _ptr(anchors),
+                                     R, _ptr(cand_ids), _ptr(tab_lp), _stream(stream)),
+               "ddt_markov_table")
+
+    def ddt_build_tree_markov(self, cand_ids, tab_lp, R, tree_tokens, parents, depths, n_nodes,
+                              mask=None, stream=None):
+        _check(_lib.ddt_build_tree_markov(self._h, _ptr(cand_ids), _ptr(tab_lp), R,
+                                          _ptr(tree_tokens), _ptr(parents), _ptr(depths),
+                                          _ptr(n_nodes), _ptr(mask), _stream(stream)),
+               "ddt_build_tree_markov")
+
+    def ddt_round_markov(self, R, bufs, W, E, anchors, stream=None, att_events=None):
+        """The SparklingTree round: bufs as for ddt_round (top_lp / top_ids
+        unused), W, E [V, H] bf16 and anchors [R] int32."""
+        a = self._round_args(R, bufs, att_events)
+        _check(_lib.ddt_round_markov(self._h, ctypes.byref(a), _ptr(W), _ptr(E), _ptr(anchors),
+                                     _stream(stream)), "ddt_round_markov")
+
+    def _round_args(self, R, bufs, att_events):
+        a = RoundArgs()
+        a.R = R
+        for name, _ in RoundArgs._fields_[1:]:
+            if name.startswith("att_event"):
+                continue
+            setattr(a, name, _ptr(bufs.get(name)))
+        if att_events is not None:
+            a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
+            a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
+        return a
 
     def ddt_round_conditioned(self, R, bufs, W, E, anchors, stream=None, att_events=None):
         """The parent-conditioned round: bufs as for ddt_round (draft_logits are

@@ -40,7 +40,7 @@ def make_ctx(cfg, inp, R_max=None):
         num_pages=inp["k_cache"].shape[0],
         draft_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32,
         target_dtype=ddt.BF16 if cfg.logit_dtype == "bf16" else ddt.F32,
-        markov_dim=cfg.markov_dim, frontier=cfg.frontier)
+        markov_dim=cfg.markov_dim, frontier=cfg.frontier, prefilter=cfg.prefilter)
     return ddt.Context(c)
 
 

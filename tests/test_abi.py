@@ -55,6 +55,14 @@ def test_workspace_bytes_and_validation(lib):
         assert ddt.workspace_bytes(_cfg(**bad)) == 0, bad
     for unsupported in (dict(L=19), dict(B=128), dict(d=96)):
         assert ddt.workspace_bytes(_cfg(**unsupported)) == 0, unsupported
+    # the Markov-head trees: the head's width is required, and the table's
+    # workspace grows with the prefilter width
+    assert ddt.workspace_bytes(_cfg(prefilter=128)) == 0
+    assert ddt.workspace_bytes(_cfg(markov_dim=256)) == 0
+    assert ddt.workspace_bytes(_cfg(markov_dim=96, prefilter=128)) == 0
+    assert ddt.workspace_bytes(_cfg(markov_dim=256, prefilter=129)) == 0
+    mk = ddt.workspace_bytes(_cfg(markov_dim=256, prefilter=128))
+    assert mk > ws + 64 * 15 * 128 * 128 * 4
 
 
 def test_create_rejects_bad_config_without_a_gpu(lib):
@@ -69,6 +77,10 @@ def test_calls_reject_null_context(lib):
     assert lib.ddt_topk_logprobs(None, None, 1, None, None, None) == ddt.EINVAL
     assert lib.ddt_round(None, None, None) == ddt.EINVAL
     assert lib.ddt_round_conditioned(None, None, None, None, None, None) == ddt.EINVAL
+    assert lib.ddt_round_markov(None, None, None, None, None, None) == ddt.EINVAL
+    assert lib.ddt_markov_table(None, None, None, None, None, 1, None, None, None) == ddt.EINVAL
+    assert lib.ddt_build_tree_markov(None, None, None, 1, None, None, None, None, None,
+                                     None) == ddt.EINVAL
     assert lib.ddt_device_status(None, None) == ddt.EINVAL
 
 
