@@ -67,8 +67,7 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
-        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
-        mk_tk_lp, mk_tk_val, mk_tk_idx, mk_tk_ms, mk_tk_cnt, total;
+        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab, total;
     int tk_nch, am_nch, rowgroups, max_items;
 };
 
@@ -129,16 +128,11 @@ Layout layout_for(const ddt_config &c)
     const size_t nseed = c.markov_dim > 0 ? (size_t)c.R_max * c.L * c.K : 0;
     L.cg_seed_lp = take(nseed * sizeof(float));
     L.cg_seed_ids = take(nseed * sizeof(int32_t));
-    // SparklingTree table tree: the round's table and the prefilter's scratch
+    // SparklingTree table tree: the round's kept tokens and table
     const size_t mrows = c.prefilter > 0 ? (size_t)c.R_max * c.L : 0;
     const size_t C = (size_t)c.prefilter;
     L.mk_cand = take(mrows * C * sizeof(int32_t));
     L.mk_tab = take(mrows * C * C * sizeof(float));
-    L.mk_tk_lp = take(mrows * C * sizeof(float));
-    L.mk_tk_val = take(mrows * L.tk_nch * C * sizeof(float));
-    L.mk_tk_idx = take(mrows * L.tk_nch * C * sizeof(int32_t));
-    L.mk_tk_ms = take(mrows * L.tk_nch * sizeof(float2));
-    L.mk_tk_cnt = take(mrows * sizeof(unsigned));
     L.total = off;
     return L;
 }
@@ -301,12 +295,6 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->cg_seed_ids = (int32_t *)(w + L.cg_seed_ids);
     ctx->mk_cand = (int32_t *)(w + L.mk_cand);
     ctx->mk_tab = (float *)(w + L.mk_tab);
-    ctx->mk_tk_lp = (float *)(w + L.mk_tk_lp);
-    ctx->mk_tk_val = (float *)(w + L.mk_tk_val);
-    ctx->mk_tk_idx = (int32_t *)(w + L.mk_tk_idx);
-    ctx->mk_tk_ms = (float2 *)(w + L.mk_tk_ms);
-    ctx->mk_tk_cnt = (unsigned *)(w + L.mk_tk_cnt);
-    ctx->mk_nch = L.tk_nch;
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so

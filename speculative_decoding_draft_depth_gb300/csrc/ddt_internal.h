@@ -77,12 +77,6 @@ struct ddt_ctx {
     // SparklingTree table tree (prefilter > 0)
     int32_t *mk_cand;        // [R_max, L, C] kept tokens (ddt_round_markov)
     float *mk_tab;           // [R_max, L, C, C] the table (ddt_round_markov)
-    float *mk_tk_lp;         // [R_max, L, C] the prefilter's log-probs (unused)
-    float *mk_tk_val;        // prefilter scratch: [R_max * L, nch, C]
-    int32_t *mk_tk_idx;      // [R_max * L, nch, C]
-    float2 *mk_tk_ms;        // [R_max * L, nch]
-    unsigned *mk_tk_cnt;     // [R_max * L]
-    int mk_nch;              // prefilter chunks per row
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };

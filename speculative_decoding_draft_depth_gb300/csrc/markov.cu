@@ -4,8 +4,8 @@
 // order markov model conditioning": a bias W1[x_prev] W2 on the next
 // position's logits, written z_d(b | a) = l_d[b] + W[b] . E[a]).
 //
-//  * The prefilter keeps every depth's C best draft tokens: a1's kernels with
-//    K = C.
+//  * mk_prefilter_kernel keeps every depth's C best draft tokens: a lower
+//    bound from per-thread maxima, then the few values above it, ranked.
 //  * mk_table_kernel: one CTA per (request, depth). The parents' E rows
 //    (the anchor at depth 0, else depth d-1's kept tokens) and the children's
 //    W rows (depth d's kept tokens) are gathered by cp.async into 128-byte
@@ -33,7 +33,6 @@ namespace {
 constexpr int MK_THREADS = 128;  // table kernel: 4 warps = the 4 TMEM lane quarters (parent rows)
 constexpr int MK_N = 128;        // children per tile (N of the MMA)
 constexpr int MK_CMAX = 128;     // largest prefilter width
-constexpr int MK_TROW = MK_N + 1;  // row stride of the staged table (floats, bank-conflict free)
 constexpr long long MK_WAIT = 4000000000LL;
 
 // order-preserving map of a (non-NaN) float to uint32
@@ -60,6 +59,173 @@ DDT_DEVINL bool mk_wait(uint32_t bar, uint32_t parity, int32_t *status)
     return true;
 }
 
+// ---------------------------------------------------------------- prefilter
+// One CTA per (request, depth) row of bf16 logits. Pass 1: every thread's
+// max; the C-th largest of the 256 maxima is a value that C elements reach,
+// so no element below it is among the C best. Pass 2 re-reads the row (from
+// L2) and collects the elements at or above it, typically a few hundred; a
+// rank count sorts them by (value desc, id asc). Rows with more survivors
+// than the buffer holds (heavy ties) take an exact bitwise search instead.
+constexpr int PF_THREADS = 256;
+constexpr int PF_CAP = 2048;
+
+DDT_DEVINL uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+DDT_DEVINL float vmax8(const uint4 &v)
+{
+    const uint32_t w = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+    return fmaxf(bf16lo(w), bf16hi(w));
+}
+DDT_DEVINL float elem8(const uint4 &v, int e)
+{
+    const uint32_t w = (e < 2) ? v.x : (e < 4) ? v.y : (e < 6) ? v.z : v.w;
+    return (e & 1) ? bf16hi(w) : bf16lo(w);
+}
+// candidate key: ordered value high, complemented id low (lower id wins a tie)
+DDT_DEVINL uint64_t pf_key(float v, int id) { return ((uint64_t)mk_fkey(v) << 32) | (uint32_t)~(uint32_t)id; }
+
+DDT_DEVINL int pf_block_sum(int v, int *s_acc)
+{
+    __syncthreads();
+    if (threadIdx.x == 0)
+        *s_acc = 0;
+    __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if ((threadIdx.x & 31) == 0)
+        atomicAdd(s_acc, v);
+    __syncthreads();
+    return *s_acc;
+}
+
+__global__ void __launch_bounds__(PF_THREADS)
+mk_prefilter_kernel(const uint16_t *__restrict__ ell, int V, int C, int vec, int32_t *__restrict__ cand)
+{
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const uint16_t *z = ell + (int64_t)row * V;
+    __shared__ uint32_t s_tmax[PF_THREADS];
+    __shared__ uint64_t s_key[PF_CAP];
+    __shared__ uint32_t s_t;
+    __shared__ int s_n, s_acc;
+    const int nvec = vec ? V / 8 : 0;
+    const uint4 *zv = reinterpret_cast<const uint4 *>(z);
+    // pass 1: this thread's max (NaN never wins)
+    float m = DDT_NEG_INF;
+#pragma unroll 4
+    for (int i = tid; i < nvec; i += PF_THREADS)
+        m = fmaxf(m, vmax8(__ldg(zv + i)));
+    for (int i = nvec * 8 + tid; i < V; i += PF_THREADS)
+        m = fmaxf(m, bf16_to_f32(z[i]));
+    const uint32_t mk = mk_fkey(m);
+    s_tmax[tid] = mk;
+    if (tid == 0)
+        s_n = 0;
+    __syncthreads();
+    int rank = 0;
+#pragma unroll 8
+    for (int t = 0; t < PF_THREADS; ++t) {
+        const uint32_t o = s_tmax[t];
+        rank += (o > mk || (o == mk && t < tid)) ? 1 : 0;
+    }
+    if (rank == C - 1)
+        s_t = mk;
+    __syncthreads();
+    const float T = mk_fkey_inv(s_t);
+    // pass 2: the elements at or above T
+#pragma unroll 4
+    for (int i0 = 0; i0 < nvec; i0 += PF_THREADS) {
+        const int i = i0 + tid;
+        uint4 v = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        if (i < nvec)
+            v = __ldg(zv + i);
+        const bool any = vmax8(v) >= T;
+        if (__any_sync(0xFFFFFFFFu, any)) {
+            uint32_t hit = 0;
+            if (any)
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    hit |= (elem8(v, e) >= T) ? (1u << e) : 0u;
+            const int cnt = __popc(hit);
+            int x = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+                if (lane >= o)
+                    x += y;
+            }
+            const int wtot = __shfl_sync(0xFFFFFFFFu, x, 31);
+            int wbase = 0;
+            if (lane == 31)
+                wbase = atomicAdd(&s_n, wtot);
+            int base = __shfl_sync(0xFFFFFFFFu, wbase, 31) + x - cnt;
+            while (hit) {
+                const int e = __ffs(hit) - 1;
+                hit &= hit - 1;
+                if (base < PF_CAP)
+                    s_key[base] = pf_key(elem8(v, e), i * 8 + e);
+                ++base;
+            }
+        }
+    }
+    for (int i = nvec * 8 + tid; i < V; i += PF_THREADS) {
+        const float x = bf16_to_f32(z[i]);
+        if (x >= T) {
+            const int base = atomicAdd(&s_n, 1);
+            if (base < PF_CAP)
+                s_key[base] = pf_key(x, i);
+        }
+    }
+    __syncthreads();
+    int n = s_n;
+    if (n > PF_CAP) {
+        // exact: the C-th largest key by bits, then every key above it
+        uint64_t t = 0;
+        for (int b = 63; b >= 0; --b) {
+            const uint64_t cb = t | (1ull << b);
+            int c = 0;
+#pragma unroll 1
+            for (int i = tid; i < V; i += PF_THREADS) {
+                const float x = bf16_to_f32(z[i]);
+                c += (x == x && pf_key(x, i) >= cb) ? 1 : 0;
+            }
+            if (pf_block_sum(c, &s_acc) >= C)
+                t = cb;
+        }
+        if (tid == 0)
+            s_n = 0;
+        __syncthreads();
+#pragma unroll 1
+        for (int i = tid; i < V; i += PF_THREADS) {
+            const float x = bf16_to_f32(z[i]);
+            if (x == x && pf_key(x, i) >= t)
+                s_key[atomicAdd(&s_n, 1)] = pf_key(x, i);  // exactly C of them
+        }
+        __syncthreads();
+        n = s_n;
+    }
+    // ranks: four threads per survivor, each counting a quarter of the others
+    for (int i0 = 0; i0 < n; i0 += PF_THREADS / 4) {
+        const int i = i0 + (tid >> 2);
+        const bool have = i < n;
+        const uint64_t ki = have ? s_key[i] : 0ull;
+        int rk = 0;
+        if (have) {
+#pragma unroll 4
+            for (int j = tid & 3; j < n; j += 4)
+                rk += (s_key[j] > ki) ? 1 : 0;
+        }
+        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 1);
+        rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 2);
+        if (have && (tid & 3) == 0 && rk < C)
+            cand[(int64_t)row * C + rk] = (int)~(uint32_t)ki;
+    }
+}
+
 struct TableArgs {
     const uint16_t *ell;     // [R, L, V] bf16
     const uint16_t *W, *E;   // [V, H] bf16
@@ -71,27 +237,26 @@ struct TableArgs {
 };
 
 // shared memory of the table kernel (offsets from a 1024-byte aligned base):
-// A and B operand tiles, then (after the MMA) the staged table over both
+// the operand tiles of one half of H (A then B, two 64-column blocks each),
+// reused for the staged table once the last MMA has completed; small enough
+// for three CTAs per SM
+constexpr uint32_t MK_HALF = 2 * 16384u;  // one operand tile of 128 rows x 128 columns of H
 struct TableSmem {
     uint32_t a, b, lv, bar, total;
 };
 __host__ __device__ inline TableSmem table_layout(int H)
 {
+    (void)H;
     TableSmem S;
-    const uint32_t nblk = (uint32_t)H / 64;
     S.a = 0;
-    S.b = nblk * 16384u;
-    uint32_t end = 2 * nblk * 16384u;
-    const uint32_t stage = (uint32_t)MK_CMAX * MK_TROW * 4u;
-    if (end < stage)
-        end = stage;
-    S.lv = (end + 15u) & ~15u;  // l of the kept children: [128] floats
+    S.b = MK_HALF;
+    S.lv = 2 * MK_HALF;         // l of the kept children: [128] floats
     S.bar = S.lv + 4u * MK_N;   // [0]: MMA done, [8]: TMEM address
     S.total = S.bar + 16;
     return S;
 }
 
-__global__ void __launch_bounds__(MK_THREADS, 1)
+__global__ void __launch_bounds__(MK_THREADS)
 mk_table_kernel(const TableArgs a)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -112,47 +277,69 @@ mk_table_kernel(const TableArgs a)
         tmem_alloc(bar + 8, MK_N);
         tmem_relinquish();
     }
-    // A: the parents' E rows; B: the kept children's W rows (zero rows pad to 128)
     const int32_t *cd = a.cand + (int64_t)rd * a.C;
     const int32_t *cp = a.cand + (int64_t)(rd - (d > 0 ? 1 : 0)) * a.C;
-    const int per = a.H / 8;  // 16-byte chunks per row
-    for (int i = tid; i < MK_N * per; i += MK_THREADS) {
-        const int p = i / per, c = i - p * per;
-        const uint32_t off = (uint32_t)(c >> 3) * 16384u + (uint32_t)p * 128u + ((uint32_t)((c & 7) ^ (p & 7)) << 4);
-        int pt = -1, ct = -1;
-        if (d == 0)
-            pt = (p == 0) ? a.anchors[r] : -1;
-        else if (p < a.C)
-            pt = cp[p];
-        if (p < a.C)
-            ct = cd[p];
-        const bool pok = pt >= 0 && pt < a.V, cok = ct >= 0 && ct < a.V;
-        cp_async_16(sb + S.a + off, pok ? (const void *)(a.E + (int64_t)pt * a.H + c * 8) : (const void *)a.E,
-                    pok ? 16u : 0u);
-        cp_async_16(sb + S.b + off, cok ? (const void *)(a.W + (int64_t)ct * a.H + c * 8) : (const void *)a.W,
-                    cok ? 16u : 0u);
-    }
+    // this thread's rows: the parents' E rows (A) and the kept children's W
+    // rows (B), zero past the kept ones
+    int pt[MK_N / MK_THREADS], ct[MK_N / MK_THREADS];
+    (void)pt;
     for (int b = tid; b < MK_N; b += MK_THREADS) {
-        const int ct = (b < a.C) ? cd[b] : -1;
-        s_l[b] = (ct >= 0 && ct < a.V) ? bf16_to_f32(a.ell[(int64_t)rd * a.V + ct]) : DDT_NEG_INF;
+        const int c = (b < a.C) ? cd[b] : -1;
+        s_l[b] = (c >= 0 && c < a.V) ? bf16_to_f32(a.ell[(int64_t)rd * a.V + c]) : DDT_NEG_INF;
     }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + S.bar + 8);
-    if (tid == 0) {
-        const uint32_t idesc = idesc_bf16(128, MK_N, false, false);
-        const uint64_t dA = sdesc_sw128(sb + S.a, 16, 1024), dB = sdesc_sw128(sb + S.b, 16, 1024);
-        for (int kk = 0; kk < a.H / 16; ++kk) {
-            const uint32_t off = ((uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u) >> 4;
-            mma_bf16(tmem, dA + off, dB + off, idesc, kk > 0 ? 1u : 0u);
+    for (int u = 0; u < MK_N / MK_THREADS; ++u) {
+        const int p = tid + u * MK_THREADS;
+        int t = -1;
+        if (d == 0)
+            t = (p == 0) ? a.anchors[r] : -1;
+        else if (p < a.C)
+            t = cp[p];
+        pt[u] = (t >= 0 && t < a.V) ? t : -1;
+        const int c = (p < a.C) ? cd[p] : -1;
+        ct[u] = (c >= 0 && c < a.V) ? c : -1;
+    }
+    const int nblk = a.H / 64, nhalf = (nblk + 1) / 2;
+    bool ok = true;
+    __syncthreads();  // the barrier is initialised
+    for (int hf = 0; hf < nhalf; ++hf) {
+        const int b0 = 2 * hf, nb = (nblk - b0 < 2) ? nblk - b0 : 2;
+        // gather this half: row p = this thread's rows, 16-byte chunks of 8 values
+        for (int u = 0; u < MK_N / MK_THREADS; ++u) {
+            const int p = tid + u * MK_THREADS;
+            for (int c = 0; c < nb * 8; ++c) {
+                const uint32_t off = (uint32_t)(c >> 3) * 16384u + (uint32_t)p * 128u +
+                                     ((uint32_t)((c & 7) ^ (p & 7)) << 4);
+                const int h = (b0 * 8 + c) * 8;  // first of the chunk's 8 values of H
+                cp_async_16(sb + S.a + off,
+                            pt[u] >= 0 ? (const void *)(a.E + (int64_t)pt[u] * a.H + h) : (const void *)a.E,
+                            pt[u] >= 0 ? 16u : 0u);
+                cp_async_16(sb + S.b + off,
+                            ct[u] >= 0 ? (const void *)(a.W + (int64_t)ct[u] * a.H + h) : (const void *)a.W,
+                            ct[u] >= 0 ? 16u : 0u);
+            }
         }
-        mma_commit(bar);
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + S.bar + 8);
+        if (tid == 0) {
+            const uint32_t idesc = idesc_bf16(128, MK_N, false, false);
+            const uint64_t dA = sdesc_sw128(sb + S.a, 16, 1024), dB = sdesc_sw128(sb + S.b, 16, 1024);
+            for (int kk = 0; kk < nb * 4; ++kk) {
+                const uint32_t off = ((uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u) >> 4;
+                mma_bf16(tmem, dA + off, dB + off, idesc, (hf > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar);
+        }
+        // the tiles are free (and the sum complete after the last half) once the MMAs are done
+        ok = __syncthreads_and((ok && mk_wait(bar, hf & 1, a.status)) ? 1 : 0) != 0;
+        tc_fence_after();
+        if (!ok)
+            break;
     }
-    const bool ok = __syncthreads_and(mk_wait(bar, 0, a.status) ? 1 : 0) != 0;
-    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + S.bar + 8);
     // thread = parent row (its TMEM lane): max, then the sum of exp, then lp
     const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16);
     float m = DDT_NEG_INF, ssum = 0.f;
@@ -182,7 +369,10 @@ mk_table_kernel(const TableArgs a)
     const float lse = m + logf(ssum);
     // rows that hold a table row: the anchor's at depth 0, every kept parent's after
     const bool valid = (d == 0) ? (tid == 0) : (tid < a.C);
-    float *T = reinterpret_cast<float *>(sgen);  // [128][MK_TROW], over the operand tiles
+    // the staged table over the operand tiles: row a, column b at a * 128 +
+    // (b ^ (a & 31)) (conflict-free both when a thread writes its row and when
+    // a warp reads one)
+    float *T = reinterpret_cast<float *>(sgen);
     if (ok) {
 #pragma unroll 1
         for (int c0 = 0; c0 < MK_N; c0 += 32) {
@@ -192,7 +382,8 @@ mk_table_kernel(const TableArgs a)
             tmem_wait_ld();
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-                T[tid * MK_TROW + c0 + j] = valid ? (__uint_as_float(acc[j]) + s_l[c0 + j]) - lse : DDT_NEG_INF;
+                T[tid * MK_N + ((c0 + j) ^ (tid & 31))] =
+                    valid ? (__uint_as_float(acc[j]) + s_l[c0 + j]) - lse : DDT_NEG_INF;
         }
     }
     tc_fence_before();
@@ -201,11 +392,11 @@ mk_table_kernel(const TableArgs a)
         float *dst = a.tab + (int64_t)rd * a.C * a.C;
         for (int row = warp; row < a.C; row += MK_THREADS / 32)
             for (int b = lane; b < a.C; b += 32)
-                dst[(int64_t)row * a.C + b] = T[row * MK_TROW + b];
+                dst[(int64_t)row * a.C + b] = T[row * MK_N + (b ^ (row & 31))];
     }
-    if (!ok && tid == 0) {  // a wait gave up: let the MMA finish before the TMEM goes (bounded)
+    if (!ok && tid == 0) {  // a wait gave up: let the MMAs finish before the TMEM goes (bounded)
         const long long t0 = clock64();
-        while (!mbar_try_wait(bar, 0) && clock64() - t0 < 200000000LL) {
+        while (!mbar_try_wait(bar, (nhalf - 1) & 1) && clock64() - t0 < 200000000LL) {
         }
     }
     __syncthreads();
@@ -529,9 +720,7 @@ bool markov_supported(const ddt_config &cfg)
 {
     const int H = cfg.markov_dim, C = cfg.prefilter;
     return H >= 64 && H <= 256 && H % 64 == 0 && C >= 1 && C <= MK_CMAX && cfg.B + 1 <= DDT_MAX_P &&
-           cfg.L <= DDT_MAX_L && tree_smem(cfg.L, C, cfg.B) <= 200 * 1024 &&
-           (int64_t)((cfg.V + topk_chunk_elems(cfg.draft_dtype) - 1) / topk_chunk_elems(cfg.draft_dtype)) * C <=
-               TOPK_CAND_CAP;
+           cfg.L <= DDT_MAX_L && tree_smem(cfg.L, C, cfg.B) <= 200 * 1024;
 }
 
 cudaError_t launch_markov_table(const ddt_ctx *c, const uint16_t *ell, const uint16_t *W,
@@ -540,10 +729,10 @@ cudaError_t launch_markov_table(const ddt_ctx *c, const uint16_t *ell, const uin
 {
     const ddt_config &cfg = c->cfg;
     const int C = cfg.prefilter, L = cfg.L;
-    // the prefilter: a1's kernels with K = C (their log-probs are not used)
-    cudaError_t e = launch_topk_scratch(ell, DDT_BF16, R * L, cfg.V, C, c->mk_nch, c->mk_tk_val,
-                                        c->mk_tk_idx, c->mk_tk_ms, c->mk_tk_cnt, c->mk_tk_lp, cand,
-                                        c->status, s);
+    // the prefilter: each row's C best tokens
+    const int vec = (cfg.V % 8 == 0 && ((uintptr_t)ell & 15u) == 0) ? 1 : 0;
+    mk_prefilter_kernel<<<R * L, PF_THREADS, 0, s>>>(ell, cfg.V, C, vec, cand);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     static size_t attr = 0;

@@ -198,6 +198,8 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     __shared__ int s_vbase[VEC_CAP];
     __shared__ int s_count, s_acc, s_nvec;
     __shared__ double s_logz;
+    __shared__ uint32_t s_lmax[TOPK_THREADS];  // lane max keys (K > 32)
+    __shared__ uint32_t s_t0;
 
     // ---- load this thread's vectors (coalesced: consecutive threads, consecutive 16 B)
     uint4 raw[NV];
@@ -252,6 +254,21 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
     }
     const float lane_max = m;
 
+    // ---- K > 32: the threshold is the K-th largest lane max of the CTA (each of
+    // those K lanes holds a value at or above it); its rank by counting
+    if (K > 32) {
+        const uint32_t mk = okey(lane_max == lane_max ? lane_max : DDT_NEG_INF);
+        s_lmax[tid] = mk;
+        __syncthreads();
+        int rank = 0;
+#pragma unroll 8
+        for (int t = 0; t < TOPK_THREADS; ++t) {
+            const uint32_t o = s_lmax[t];
+            rank += (o > mk || (o == mk && t < tid)) ? 1 : 0;
+        }
+        if (rank == K - 1)
+            s_t0 = mk;
+    }
     // ---- per-warp quota threshold: the ceil(K/8)-th largest lane max, found by
     // removing the warp's largest lane max (one lane at a time) quota - 1 times
     const int quota = (K + (TOPK_THREADS / 32) - 1) / (TOPK_THREADS / 32);
@@ -284,6 +301,10 @@ topk_chunk_kernel(const T *__restrict__ z, int V, int K, int nch, float *__restr
 #pragma unroll
     for (int w = 1; w < TOPK_THREADS / 32; ++w)
         T0 = fminf(T0, s_wt[w]);
+    if (K > 32) {
+        const uint32_t t0 = s_t0;
+        T0 = (t0 & 0x80000000u) ? __uint_as_float(t0 & 0x7FFFFFFFu) : __uint_as_float(~t0);
+    }
     float cm = DDT_NEG_INF, cs = 0.f;  // the chunk's (max, sum): thread 0 only
     if (tid == 0) {
         cm = s_wm[0];
@@ -573,6 +594,96 @@ topk_merge_kernel(const float *__restrict__ part_val, const int32_t *__restrict_
 }  // namespace
 
 namespace {
+// rows with K > 32: one CTA per row, the chunk lists staged in shared memory;
+// every entry's rank is its rank in its own list plus, per other list, the
+// number of entries that beat it (a binary search)
+constexpr int WIDE_THREADS = 256;
+
+__global__ void __launch_bounds__(WIDE_THREADS)
+topk_merge_wide_kernel(const float *__restrict__ part_val, const int32_t *__restrict__ part_idx,
+                       const float2 *__restrict__ part_ms, int nch, int K,
+                       float *__restrict__ top_lp, int32_t *__restrict__ top_ids,
+                       int32_t *__restrict__ status)
+{
+    extern __shared__ uint64_t s_keys[];  // [nch * K]
+    __shared__ double s_lz;
+    __shared__ int s_nreal;
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const int n = nch * K;
+    const float *rv = part_val + (int64_t)row * n;
+    const int32_t *ri = part_idx + (int64_t)row * n;
+    if (tid == 0)
+        s_nreal = 0;
+    __syncthreads();
+    int real = 0;
+    for (int i = tid; i < n; i += WIDE_THREADS) {
+        const int id = ri[i];
+        s_keys[i] = (id == IDX_PAD) ? 0ull : make_key(rv[i], id);
+        real += (id == IDX_PAD) ? 0 : 1;
+    }
+    if (tid < 32) {  // log-partition over the chunks' (max, sum) pairs
+        float M = DDT_NEG_INF, S = 0.f;
+        for (int c0 = 0; c0 < nch; c0 += 32) {
+            const int c = c0 + tid;
+            float2 ms = make_float2(DDT_NEG_INF, 0.f);
+            if (c < nch)
+                ms = part_ms[(int64_t)row * nch + c];
+            float wm = ms.x;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, off));
+            float t = (ms.x != DDT_NEG_INF) ? ms.y * ex2((ms.x - wm) * DDT_LOG2E)
+                                            : (ms.y != ms.y ? ms.y : 0.f);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                t += __shfl_xor_sync(0xFFFFFFFFu, t, off);
+            ms_combine(M, S, wm, t);
+        }
+        if (tid == 0) {
+            if (S != S)
+                set_status(status, DDT_DEV_NAN_LOGITS);
+            s_lz = (double)M + log((double)S);
+        }
+    }
+    atomicAdd(&s_nreal, real);
+    __syncthreads();
+    const double logz = s_lz;
+    float *olp = top_lp + (int64_t)row * K;
+    int32_t *oid = top_ids + (int64_t)row * K;
+    const int filled = s_nreal < K ? s_nreal : K;
+    for (int r = filled + tid; r < K; r += WIDE_THREADS) {  // unfilled ranks: padding
+        olp[r] = DDT_NEG_INF;
+        oid[r] = -1;
+    }
+    for (int i = tid; i < n; i += WIDE_THREADS) {
+        const uint64_t ki = s_keys[i];
+        if (ki == 0ull)
+            continue;
+        const int a = i / K, rho = i - a * K;
+        int rank = rho;
+        for (int b = 0; b < nch && rank < K; ++b) {
+            if (b == a)
+                continue;
+            const uint64_t *lb = s_keys + b * K;
+            int lo = 0, hi = K;  // entries of list b that beat entry i (lists descend; pads are 0)
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (lb[mid] > ki)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank < K) {
+            olp[rank] = (float)((double)key_val(ki) - logz);
+            oid[rank] = key_idx(ki);
+        }
+    }
+}
+}  // namespace
+
+namespace {
 cudaError_t launch_merge(int rows, int V, int K, int nch, const float *part_val,
                          const int32_t *part_idx, const float2 *part_ms, float *top_lp,
                          int32_t *top_ids, int32_t *status, cudaStream_t s)
@@ -581,6 +692,22 @@ cudaError_t launch_merge(int rows, int V, int K, int nch, const float *part_val,
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || nch == 1 || rows == 0)
         return e;
+    if (K > 32) {
+        const size_t smem = (size_t)nch * K * sizeof(uint64_t);
+        if (smem > 48 * 1024) {
+            static size_t attr = 0;
+            if (attr < smem) {
+                if ((e = cudaFuncSetAttribute(topk_merge_wide_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)smem)) != cudaSuccess)
+                    return e;
+                attr = smem;
+            }
+        }
+        topk_merge_wide_kernel<<<rows, WIDE_THREADS, smem, s>>>(part_val, part_idx, part_ms, nch,
+                                                                K, top_lp, top_ids, status);
+        return cudaGetLastError();
+    }
     topk_merge_kernel<<<(rows + 7) / 8, 256, 0, s>>>(part_val, part_idx, part_ms, rows, nch, K,
                                                      top_lp, top_ids, status);
     return cudaGetLastError();
