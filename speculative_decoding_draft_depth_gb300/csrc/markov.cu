@@ -482,6 +482,11 @@ DDT_DEVINL uint64_t warp_best_below(const uint64_t *k, uint64_t bound, int lane,
 
 constexpr int SLOTS = 4;  // frontier slots per lane: 128 >= B entries
 
+DDT_DEVINL void prefetch_l1(const void *p)
+{
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 struct TreeArgs {
     const int32_t *cand;  // [R, L, C]
     const float *tab;     // [R, L, C, C]
@@ -612,6 +617,17 @@ mk_tree_kernel(const TreeArgs a)
         ++count;
         if (count == B)
             break;
+        // the popped node's own row (its children), requested first: the
+        // sibling's scan below runs while it is in flight
+        float rv[4];
+        if (wdep < L) {
+            const float *src = tr + ((int64_t)wdep * C + wcb) * C;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int b = lane + 32 * i;
+                rv[i] = (b < C) ? src[b] : DDT_NEG_INF;
+            }
+        }
         // the next child of the same parent: the largest key of the parent's
         // row below the popped one's; it reuses the popped slot
         uint64_t sib = 0ull;
@@ -639,9 +655,18 @@ mk_tree_kernel(const TreeArgs a)
         }
         // the first child: the best of the popped node's own row (depth wdep,
         // row wcb), loaded now and kept for the node's later children
+        // a pushed entry's own row is warmed into L1 now, for when it is popped
+        if (sib != 0ull && wdep < L && lane < 4 && lane * 32 < C)
+            prefetch_l1(tr + ((int64_t)wdep * C + scol) * C + lane * 32);
         if (wdep < L) {
             uint64_t k[4];
-            load_row(tr + ((int64_t)wdep * C + wcb) * C, node, s_cand + wdep * C, k);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int b = lane + 32 * i;
+                if (b < C)
+                    s_rows[node * C + b] = rv[i];
+                k[i] = (b < C) ? child_key(rv[i], s_cand[wdep * C + b]) : 0ull;
+            }
             int ccol;
             const uint64_t chk = warp_best_below(k, ~0ull, lane, ccol);
             if (chk != 0ull) {
@@ -668,6 +693,8 @@ mk_tree_kernel(const TreeArgs a)
                             rnk[f] = 0;
                         }
                 }
+                if (wdep + 1 < L && lane < 4 && lane * 32 < C)
+                    prefetch_l1(tr + ((int64_t)(wdep + 1) * C + ccol) * C + lane * 32);
             }
         }
         __syncwarp();
