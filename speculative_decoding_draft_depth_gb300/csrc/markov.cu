@@ -61,11 +61,12 @@ DDT_DEVINL bool mk_wait(uint32_t bar, uint32_t parity, int32_t *status)
 
 // ---------------------------------------------------------------- prefilter
 // One CTA per (request, depth) row of bf16 logits. Pass 1: every thread's
-// max; the C-th largest of the 256 maxima is a value that C elements reach,
-// so no element below it is among the C best. Pass 2 re-reads the row (from
-// L2) and collects the elements at or above it, typically a few hundred; a
-// rank count sorts them by (value desc, id asc). Rows with more survivors
-// than the buffer holds (heavy ties) take an exact bitwise search instead.
+// max and the positions of its four best 8-value vectors; the C-th largest of
+// the 256 maxima is a value that C elements reach, so no element below it is
+// among the C best. Pass 2 re-reads only the vectors that reach it (a few per
+// row) and collects their elements at or above it; a rank count sorts them
+// by (value desc, id asc). Rows with more survivors than the buffer holds
+// (heavy ties) take an exact bitwise search instead.
 constexpr int PF_THREADS = 256;
 constexpr int PF_CAP = 2048;
 
@@ -103,22 +104,37 @@ DDT_DEVINL int pf_block_sum(int v, int *s_acc)
     return *s_acc;
 }
 
-__global__ void __launch_bounds__(PF_THREADS)
-mk_prefilter_kernel(const uint16_t *__restrict__ ell, int V, int C, int vec, int32_t *__restrict__ cand)
+__device__ void prefilter_row(const uint16_t *__restrict__ z, int V, int C, int vec,
+                              int32_t *__restrict__ out, uint32_t *s_tmax, uint64_t *s_key,
+                              uint32_t *s_t_, int *s_n_, int *s_acc_)
 {
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-    const uint16_t *z = ell + (int64_t)row * V;
-    __shared__ uint32_t s_tmax[PF_THREADS];
-    __shared__ uint64_t s_key[PF_CAP];
-    __shared__ uint32_t s_t;
-    __shared__ int s_n, s_acc;
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t &s_t = *s_t_;
+    int &s_n = *s_n_;
+    int &s_acc = *s_acc_;
     const int nvec = vec ? V / 8 : 0;
     const uint4 *zv = reinterpret_cast<const uint4 *>(z);
-    // pass 1: this thread's max (NaN never wins)
-    float m = DDT_NEG_INF;
+    // pass 1: this thread's max (NaN never wins), and its four best vectors
+    float tv[4] = {DDT_NEG_INF, DDT_NEG_INF, DDT_NEG_INF, DDT_NEG_INF};
+    int ti[4] = {-1, -1, -1, -1};
 #pragma unroll 4
-    for (int i = tid; i < nvec; i += PF_THREADS)
-        m = fmaxf(m, vmax8(__ldg(zv + i)));
+    for (int i = tid; i < nvec; i += PF_THREADS) {
+        float x = vmax8(__ldg(zv + i));
+        if (x > tv[3]) {
+            int xi = i;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                if (x > tv[q]) {
+                    const float t = tv[q];
+                    const int u = ti[q];
+                    tv[q] = x;
+                    ti[q] = xi;
+                    x = t;
+                    xi = u;
+                }
+        }
+    }
+    float m = tv[0];
     for (int i = nvec * 8 + tid; i < V; i += PF_THREADS)
         m = fmaxf(m, bf16_to_f32(z[i]));
     const uint32_t mk = mk_fkey(m);
@@ -136,41 +152,31 @@ mk_prefilter_kernel(const uint16_t *__restrict__ ell, int V, int C, int vec, int
         s_t = mk;
     __syncthreads();
     const float T = mk_fkey_inv(s_t);
-    // pass 2: the elements at or above T
-#pragma unroll 4
-    for (int i0 = 0; i0 < nvec; i0 += PF_THREADS) {
-        const int i = i0 + tid;
-        uint4 v = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-        if (i < nvec)
-            v = __ldg(zv + i);
-        const bool any = vmax8(v) >= T;
-        if (__any_sync(0xFFFFFFFFu, any)) {
-            uint32_t hit = 0;
-            if (any)
+    // pass 2: the elements at or above T. Only vectors whose max reaches T
+    // hold them: a thread re-reads its best vectors that do, or all of its
+    // vectors when even its fourth best does (more may)
+    auto take = [&](int i) {
+        const uint4 v = __ldg(zv + i);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    hit |= (elem8(v, e) >= T) ? (1u << e) : 0u;
-            const int cnt = __popc(hit);
-            int x = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o)
-                    x += y;
-            }
-            const int wtot = __shfl_sync(0xFFFFFFFFu, x, 31);
-            int wbase = 0;
-            if (lane == 31)
-                wbase = atomicAdd(&s_n, wtot);
-            int base = __shfl_sync(0xFFFFFFFFu, wbase, 31) + x - cnt;
-            while (hit) {
-                const int e = __ffs(hit) - 1;
-                hit &= hit - 1;
+        for (int e = 0; e < 8; ++e) {
+            const float x = elem8(v, e);
+            if (x >= T) {
+                const int base = atomicAdd(&s_n, 1);
                 if (base < PF_CAP)
-                    s_key[base] = pf_key(elem8(v, e), i * 8 + e);
-                ++base;
+                    s_key[base] = pf_key(x, i * 8 + e);
             }
         }
+    };
+    if (tv[3] >= T) {
+#pragma unroll 1
+        for (int i = tid; i < nvec; i += PF_THREADS)
+            if (vmax8(__ldg(zv + i)) >= T)
+                take(i);
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (tv[q] >= T)
+                take(ti[q]);
     }
     for (int i = nvec * 8 + tid; i < V; i += PF_THREADS) {
         const float x = bf16_to_f32(z[i]);
@@ -222,7 +228,22 @@ mk_prefilter_kernel(const uint16_t *__restrict__ ell, int V, int C, int vec, int
         rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 1);
         rk += __shfl_xor_sync(0xFFFFFFFFu, rk, 2);
         if (have && (tid & 3) == 0 && rk < C)
-            cand[(int64_t)row * C + rk] = (int)~(uint32_t)ki;
+            out[rk] = (int)~(uint32_t)ki;
+    }
+}
+
+__global__ void __launch_bounds__(PF_THREADS)
+mk_prefilter_kernel(const uint16_t *__restrict__ ell, int rows, int V, int C, int vec,
+                    int32_t *__restrict__ cand)
+{
+    __shared__ uint32_t s_tmax[PF_THREADS];
+    __shared__ uint64_t s_key[PF_CAP];
+    __shared__ uint32_t s_t;
+    __shared__ int s_n, s_acc;
+    for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+        prefilter_row(ell + (int64_t)row * V, V, C, vec, cand + (int64_t)row * C, s_tmax, s_key,
+                      &s_t, &s_n, &s_acc);
+        __syncthreads();
     }
 }
 
@@ -758,7 +779,7 @@ cudaError_t launch_markov_table(const ddt_ctx *c, const uint16_t *ell, const uin
     const int C = cfg.prefilter, L = cfg.L;
     // the prefilter: each row's C best tokens
     const int vec = (cfg.V % 8 == 0 && ((uintptr_t)ell & 15u) == 0) ? 1 : 0;
-    mk_prefilter_kernel<<<R * L, PF_THREADS, 0, s>>>(ell, cfg.V, C, vec, cand);
+    mk_prefilter_kernel<<<R * L, PF_THREADS, 0, s>>>(ell, R * L, cfg.V, C, vec, cand);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
