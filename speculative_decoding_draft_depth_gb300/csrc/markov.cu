@@ -117,39 +117,73 @@ __device__ void prefilter_row(const uint16_t *__restrict__ z, int V, int C, int 
     // pass 1: this thread's max (NaN never wins), and its four best vectors
     float tv[4] = {DDT_NEG_INF, DDT_NEG_INF, DDT_NEG_INF, DDT_NEG_INF};
     int ti[4] = {-1, -1, -1, -1};
-#pragma unroll 4
-    for (int i = tid; i < nvec; i += PF_THREADS) {
-        float x = vmax8(__ldg(zv + i));
-        if (x > tv[3]) {
-            int xi = i;
+    constexpr int PF_BATCH = 4;  // vectors in flight per thread
+    for (int i0 = tid; i0 < nvec; i0 += PF_BATCH * PF_THREADS) {
+        float vm[PF_BATCH];
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                if (x > tv[q]) {
-                    const float t = tv[q];
-                    const int u = ti[q];
-                    tv[q] = x;
-                    ti[q] = xi;
-                    x = t;
-                    xi = u;
-                }
+        for (int u = 0; u < PF_BATCH; ++u) {
+            const int i = i0 + u * PF_THREADS;
+            vm[u] = (i < nvec) ? vmax8(__ldg(zv + i)) : DDT_NEG_INF;
+        }
+#pragma unroll
+        for (int u = 0; u < PF_BATCH; ++u) {
+            float x = vm[u];
+            if (x > tv[3]) {
+                int xi = i0 + u * PF_THREADS;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (x > tv[q]) {
+                        const float t = tv[q];
+                        const int w = ti[q];
+                        tv[q] = x;
+                        ti[q] = xi;
+                        x = t;
+                        xi = w;
+                    }
+            }
         }
     }
     float m = tv[0];
     for (int i = nvec * 8 + tid; i < V; i += PF_THREADS)
         m = fmaxf(m, bf16_to_f32(z[i]));
+    // the C-th largest of the 256 maxima: each warp sorts its 32 (descending,
+    // bitonic over the lanes), then each thread's rank is its place in its
+    // own warp's list plus a binary search in each other warp's
     const uint32_t mk = mk_fkey(m);
-    s_tmax[tid] = mk;
+    uint32_t sv = mk;
+#pragma unroll
+    for (int k2 = 2; k2 <= 32; k2 <<= 1)
+#pragma unroll
+        for (int j = k2 >> 1; j > 0; j >>= 1) {
+            const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, sv, j);
+            const bool up = ((lane & k2) == 0) != ((lane & j) != 0);  // keep the larger
+            sv = up ? (sv > o ? sv : o) : (sv < o ? sv : o);
+        }
+    s_tmax[tid] = sv;  // warp w's maxima, descending, at [32 w, 32 w + 32)
     if (tid == 0)
         s_n = 0;
     __syncthreads();
-    int rank = 0;
-#pragma unroll 8
-    for (int t = 0; t < PF_THREADS; ++t) {
-        const uint32_t o = s_tmax[t];
-        rank += (o > mk || (o == mk && t < tid)) ? 1 : 0;
+    {
+        const int w0 = tid >> 5;
+        const uint32_t x = s_tmax[tid];
+        int rank = lane;  // equal values: the earlier position in the sorted lists first
+        for (int w = 0; w < PF_THREADS / 32; ++w) {
+            if (w == w0)
+                continue;
+            const uint32_t *l = s_tmax + 32 * w;
+            int lo = 0, hi = 32;  // entries of list w before x
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (l[mid] > x || (l[mid] == x && w < w0))
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            rank += lo;
+        }
+        if (rank == C - 1)
+            s_t = x;
     }
-    if (rank == C - 1)
-        s_t = mk;
     __syncthreads();
     const float T = mk_fkey_inv(s_t);
     // pass 2: the elements at or above T. Only vectors whose max reaches T
@@ -232,7 +266,7 @@ __device__ void prefilter_row(const uint16_t *__restrict__ z, int V, int C, int 
     }
 }
 
-__global__ void __launch_bounds__(PF_THREADS)
+__global__ void __launch_bounds__(PF_THREADS, 7)  // 7 CTAs per SM: every row in one wave
 mk_prefilter_kernel(const uint16_t *__restrict__ ell, int rows, int V, int C, int vec,
                     int32_t *__restrict__ cand)
 {
