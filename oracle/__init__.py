@@ -19,6 +19,9 @@ Pages cited (by title and section):
       description.
   "SparklingTree ...", "Building SparklingTree" and "Solving the candidate
       tree construction" (the prefilter and the Markov table: NEXT row 2).
+  "DSpark Speculative Decoding Explained: Block Drafting and Confidence
+      Checks", the probability rule and its toy (stochastic verification:
+      NEXT row 3).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
 against something other than itself (closed forms, brute force, library
@@ -75,6 +78,10 @@ def lib():
         L.orc_markov_tree.restype = i32
         L.orc_markov_tree_bruteforce.argtypes = [p, p, i32, i32, i32, i64, p, p, p, p, p]
         L.orc_markov_tree_bruteforce.restype = i64
+        L.orc_verify_chain.argtypes = [p, p, p, p, ctypes.c_double, i32, i64, p]
+        L.orc_verify_chain.restype = i32
+        L.orc_accept_stochastic.argtypes = [p, p, i32, p, p, p, i32, i32, i64, p, p]
+        L.orc_accept_stochastic.restype = i32
         L.orc_num_threads.argtypes = []
         L.orc_num_threads.restype = i32
         _lib = L
@@ -409,3 +416,42 @@ def markov_tree_bruteforce(cand, tab, B, max_prefixes=2_000_000):
     if n < 0:
         raise ValueError("too many prefixes for the brute force")
     return t
+
+
+# ---------------------------------------------------------------- NEXT row 3
+def verify_chain(p, q, tokens, u, r):
+    """Stochastic verification of one drafted chain ("DSpark Speculative
+    Decoding Explained ...", the probability rule): p [L+1, V] target and
+    q [L, V] draft weights, tokens [L], uniforms u [L] (guess k kept iff
+    u[k] < min(1, p/q)) and r (the replacement or bonus draw by inverse CDF
+    in index order). Returns the committed tokens."""
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    L1, V = p.shape
+    L = L1 - 1
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    out = np.full(L + 1, -1, np.int32)
+    n = lib().orc_verify_chain(_ptr(p), _ptr(q), _ptr(tokens), _ptr(u), float(r), L, V, _ptr(out))
+    if n < 0:
+        raise ValueError("bad arguments to verify_chain")
+    return [int(t) for t in out[:n]]
+
+
+def accept_stochastic(draft, target, tokens, u, r):
+    """The same rule on logits at temperature 1 for R requests: draft
+    [R, L, V], target [R, L+1, V] (same dtype), tokens [R, L], u [R, L],
+    r [R]. Returns acc_len [R] and acc_tokens [R, L+1] (-1 padded)."""
+    draft = np.ascontiguousarray(draft)
+    target = np.ascontiguousarray(target)
+    R, L, V = draft.shape
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    u = np.ascontiguousarray(u, dtype=np.float64)
+    r = np.ascontiguousarray(r, dtype=np.float64)
+    acc_len = np.empty(R, np.int32)
+    acc_tokens = np.empty((R, L + 1), np.int32)
+    rc = lib().orc_accept_stochastic(_ptr(draft), _ptr(target), _logit_dtype(draft), _ptr(tokens),
+                                     _ptr(u), _ptr(r), R, L, V, _ptr(acc_len), _ptr(acc_tokens))
+    if rc:
+        raise ValueError("bad arguments to accept_stochastic")
+    return acc_len, acc_tokens

@@ -1202,3 +1202,126 @@ int64_t orc_markov_tree_bruteforce(const int32_t *cand, const double *tab, int L
     free(order);
     return n;
 }
+
+/* ------------------------------------------------------------------------
+ * NEXT row 3: stochastic verification of a drafted chain at temperature 1
+ * ["DSpark Speculative Decoding Explained: Block Drafting and Confidence
+ * Checks", the probability rule and its toy: keep the k-th guess x_k with
+ * probability min(1, p_k(x_k) / q_k(x_k)); at the first rejected guess draw a
+ * replacement from the leftover max(0, p_k - q_k) and drop the rest; if every
+ * guess survives, draw a bonus token from the target's next distribution].
+ *
+ * The random numbers are inputs: u[k] decides guess k (kept iff
+ * u[k] < min(1, p/q)); r draws the replacement or bonus token by inverse CDF
+ * over the vocabulary in index order: the first index whose running sum of
+ * weights exceeds r times their total (the rule of a cumulative-weights
+ * bisection). Sums run left to right in fp64.
+ *
+ * orc_verify_chain: p [L+1, V] and q [L, V] as explicit probabilities (rows
+ * need not be normalised: weights), one request. Writes the committed tokens
+ * to out[0..n) and returns n (accepted guesses + 1).
+ * ---------------------------------------------------------------------- */
+static int draw_index(const double *w, int64_t V, double r)
+{
+    double total = 0.0;
+    for (int64_t v = 0; v < V; ++v)
+        total += w[v];
+    const double x = r * total;
+    double cum = 0.0;
+    int64_t last = -1;
+    for (int64_t v = 0; v < V; ++v) {
+        cum += w[v];
+        if (w[v] > 0.0)
+            last = v;
+        if (cum > x)
+            return (int)v;
+    }
+    return (int)last; /* only when rounding left x at the total */
+}
+
+int orc_verify_chain(const double *p, const double *q, const int32_t *tokens, const double *u,
+                     double r, int L, int64_t V, int32_t *out)
+{
+    if (L < 0 || V < 1)
+        return -1;
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    int n = 0;
+    for (int k = 0; k < L; ++k) {
+        const int x = tokens[k];
+        const double pk = p[(int64_t)k * V + x], qk = q[(int64_t)k * V + x];
+        const double a = (qk > 0.0) ? (pk / qk < 1.0 ? pk / qk : 1.0) : 1.0;
+        if (u[k] < a) {
+            out[n++] = x;
+            continue;
+        }
+        for (int64_t v = 0; v < V; ++v) {
+            const double d = p[(int64_t)k * V + v] - q[(int64_t)k * V + v];
+            w[v] = d > 0.0 ? d : 0.0;
+        }
+        out[n++] = draw_index(w, V, r);
+        free(w);
+        return n;
+    }
+    out[n++] = draw_index(p + (int64_t)L * V, V, r);
+    free(w);
+    return n;
+}
+
+/*
+ * The same rule on logits, for R requests: draft [R, L, V] and target
+ * [R, L+1, V] (dtype as widen), softmax at temperature 1 in fp64, tokens
+ * [R, L], u [R, L], r [R]. Outputs acc_len [R] (accepted guesses + 1) and
+ * acc_tokens [R, L+1] (-1 past acc_len).
+ */
+int orc_accept_stochastic(const void *draft, const void *target, int dtype, const int32_t *tokens,
+                          const double *u, const double *r, int R, int L, int64_t V,
+                          int32_t *acc_len, int32_t *acc_tokens)
+{
+    if (R < 1 || L < 0 || V < 1)
+        return ORC_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < R; ++i) {
+        double *p = (double *)malloc(sizeof(double) * (size_t)(L + 1) * V);
+        double *q = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1) * V);
+        for (int k = 0; k <= L; ++k) {
+            const int64_t base = ((int64_t)i * (L + 1) + k) * V;
+            double m = -INFINITY;
+            for (int64_t v = 0; v < V; ++v) {
+                const double z = widen(target, dtype, base + v);
+                if (z > m)
+                    m = z;
+            }
+            double s = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                p[(int64_t)k * V + v] = exp(widen(target, dtype, base + v) - m);
+                s += p[(int64_t)k * V + v];
+            }
+            for (int64_t v = 0; v < V; ++v)
+                p[(int64_t)k * V + v] /= s;
+        }
+        for (int k = 0; k < L; ++k) {
+            const int64_t base = ((int64_t)i * L + k) * V;
+            double m = -INFINITY;
+            for (int64_t v = 0; v < V; ++v) {
+                const double z = widen(draft, dtype, base + v);
+                if (z > m)
+                    m = z;
+            }
+            double s = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                q[(int64_t)k * V + v] = exp(widen(draft, dtype, base + v) - m);
+                s += q[(int64_t)k * V + v];
+            }
+            for (int64_t v = 0; v < V; ++v)
+                q[(int64_t)k * V + v] /= s;
+        }
+        int32_t *out = acc_tokens + (int64_t)i * (L + 1);
+        for (int k = 0; k <= L; ++k)
+            out[k] = -1;
+        acc_len[i] = orc_verify_chain(p, q, tokens + (int64_t)i * L, u + (int64_t)i * L, r[i], L, V,
+                                      out);
+        free(q);
+        free(p);
+    }
+    return 0;
+}
