@@ -191,7 +191,7 @@ def main():
                     help="skip the timing of the NEXT rows (parent-conditioned tree)")
     ap.add_argument("--stage", default="round",
                     choices=["round", "topk", "tree", "attention", "accept", "cond_tree",
-                             "markov"],
+                             "markov", "stochastic"],
                     help="time one stage alone (small profiling cases); cond_tree: the "
                          "parent-conditioned tree's workload alone")
     ap.add_argument("--requests", type=int, default=0,
@@ -215,10 +215,11 @@ def main():
 
     import torch
     torch.cuda.set_device(local_rank)
-    if args.stage in ("cond_tree", "markov"):
+    if args.stage in ("cond_tree", "markov", "stochastic"):
         from speculative_decoding_draft_depth_gb300 import ddt
         ddt.load()
-        fn = time_cond_tree if args.stage == "cond_tree" else time_markov
+        fn = {"cond_tree": time_cond_tree, "markov": time_markov,
+              "stochastic": time_stochastic}[args.stage]
         res = fn(torch.device("cuda", local_rank), reps=max(args.steps, 1),
                  cpu=not args.no_cpu_baseline)
         if rank == 0:
@@ -348,7 +349,9 @@ def main():
 
     if rank == 0 and not args.no_next:
         out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline),
-                            "markov_table_tree": time_markov(dev, cpu=not args.no_cpu_baseline)}
+                            "markov_table_tree": time_markov(dev, cpu=not args.no_cpu_baseline),
+                            "stochastic_chain": time_stochastic(dev,
+                                                                cpu=not args.no_cpu_baseline)}
     if not args.no_e2e:
         out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
                               steps=max(10, min(args.steps, 50)))
@@ -593,6 +596,69 @@ def time_markov(dev, reps=20, cpu=True):
         sec = (time.perf_counter() - t0) * R
         res["cpu_oracle_ms"] = round(sec * 1e3, 1)
         res["cpu_oracle_sample"] = "1 of 64 requests (table + tree), scaled"
+    return res
+
+
+def time_stochastic(dev, reps=20, cpu=True):
+    """Stochastic verification of drafted chains ("DSpark Speculative Decoding
+    Explained ...", the probability rule) on the batch64 shapes (R=64 chains
+    of L=15 guesses, V=151936, bf16 draft [R, L, V] and target [R, L+1, V]
+    logits): device time per ddt_accept_stochastic call over `reps` calls
+    after 3 warm-up calls (the logits, 603 MB, exceed L2, so no flush is
+    needed), with the algorithmic bytes (every logit read once); and the
+    oracle's time for the same 64 chains."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import ddt, synth
+    cfg = synth.config("batch64")
+    inp = synth.draw_chain_inputs(cfg)
+    R, L, V = cfg.R, cfg.L, cfg.V
+    K = cfg.K
+    c = ddt.make_config(R_max=R, L=L, V=V, B=K, K=K, Hq=4, Hkv=1, d=64, page_size=16,
+                        max_pages_per_req=1, num_pages=1)
+    ctx = ddt.Context(c)
+
+    def td(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    dr, tg, tok, u, r = (td(inp[k]) for k in ("draft", "target", "tokens", "u", "r"))
+    acc_len = torch.empty(R, dtype=torch.int32, device=dev)
+    acc_tok = torch.empty((R, L + 1), dtype=torch.int32, device=dev)
+
+    def call():
+        ctx.ddt_accept_stochastic(dr, tg, tok, u, r, R, acc_len, acc_tok)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        call()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set in stochastic verification")
+    al = acc_len.cpu().numpy()
+    nbytes = R * (2 * L + 1) * V * 2 + R * L * 12 + R * 4 + R * (L + 2) * 4
+    # the draw re-reads row k* of the target (and of the draft after a rejection)
+    redraw = int(sum(V * 2 * (1 + (k - 1 < L)) for k in al))
+    peak, _ = _peaks()
+    gbs = nbytes / (ms / 1e3) / 1e9
+    res = {"workload": "batch64 chains: R=64, L=15, V=151936, bf16 draft and target logits, "
+                       "target = draft + N(0, s^2), s~U[0.2,1.0], guesses sampled from the draft",
+           "ms": round(ms, 4), "chains_per_s": round(R * 1e3 / ms, 1),
+           "algorithmic_bytes": int(nbytes), "redraw_bytes": redraw,
+           "GBps": round(gbs, 1), "frac_of_hbm": round(gbs / peak, 4),
+           "mean_acc_len": float(al.mean())}
+    if cpu:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.accept_stochastic(inp["draft"], inp["target"], inp["tokens"],
+                                 inp["u"].astype(np.float64), inp["r"].astype(np.float64))
+        res["cpu_oracle_ms"] = round((time.perf_counter() - t0) * 1e3, 1)
+        res["cpu_oracle_sample"] = "all 64 chains"
     return res
 
 

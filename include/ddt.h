@@ -311,6 +311,31 @@ ddt_status ddt_build_tree_markov(ddt_ctx *ctx, const int32_t *cand_ids, const fl
 ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *args, const uint16_t *W,
                             const uint16_t *E, const int32_t *anchors, void *stream);
 
+/* Stochastic verification of a drafted chain at temperature 1 -- "DSpark
+ * Speculative Decoding Explained: Block Drafting and Confidence Checks", the
+ * probability rule (keep guess k with probability min(1, p_k(x_k) /
+ * q_k(x_k)); at the first rejection draw the replacement from max(0, p_k -
+ * q_k); when all L guesses survive draw a bonus token from p_L). p and q are
+ * the softmax of the target's and the drafter's logits (computed here).
+ *   draft_logits  [R, L, V] draft_dtype, device, rows contiguous
+ *   target_logits [R, L+1, V] target_dtype, device
+ *   draft_tokens  [R, L] i32, the guesses x_0..x_{L-1}
+ *   u             [R, L] f32 in [0, 1): guess k is kept iff u[k] < min(1, p/q)
+ *                 (q(x) = 0 counts as ratio 1)
+ *   r             [R] f32 in [0, 1): the replacement or bonus token is the
+ *                 first index (ascending) whose running sum of weights
+ *                 exceeds r times the weights' total
+ * Outputs: acc_len [R] (kept guesses + 1) and acc_tokens [R, L+1] (the kept
+ * guesses, then the drawn token, then -1). The draw is -1 only when every
+ * weight is zero (p <= q everywhere after rounding). Guesses outside [0, V)
+ * set DDT_DEV_BAD_TREE and count as rejected; NaN logits set
+ * DDT_DEV_NAN_LOGITS. Two kernels are enqueued on `stream`, the second as a
+ * programmatic dependent launch; calls on one context must not overlap. */
+ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
+                                 const void *target_logits, const int32_t *draft_tokens,
+                                 const float *u, const float *r, int32_t R, int32_t *acc_len,
+                                 int32_t *acc_tokens, void *stream);
+
 /* Wait for the context's device to finish all enqueued work, copy the
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);

@@ -67,8 +67,9 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
-        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab, total;
-    int tk_nch, am_nch, rowgroups, max_items;
+        cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
+        sv_part_d, sv_part_t, sv_cnt, sv_meta, sv_part_w, total;
+    int tk_nch, am_nch, rowgroups, max_items, sv_nch_d, sv_nch_t, sv_nch_w;
 };
 
 Layout layout_for(const ddt_config &c)
@@ -133,6 +134,18 @@ Layout layout_for(const ddt_config &c)
     const size_t C = (size_t)c.prefilter;
     L.mk_cand = take(mrows * C * sizeof(int32_t));
     L.mk_tab = take(mrows * C * C * sizeof(float));
+    // stochastic chain verification: chunk pairs of the L draft and L + 1
+    // target rows, the draw's chunk totals, two arrival counters per request
+    L.sv_nch_d = (c.V + stochastic_chunk_elems(c.draft_dtype) - 1) /
+                 stochastic_chunk_elems(c.draft_dtype);
+    L.sv_nch_t = (c.V + stochastic_chunk_elems(c.target_dtype) - 1) /
+                 stochastic_chunk_elems(c.target_dtype);
+    L.sv_nch_w = stochastic_draw_chunks(c.V);
+    L.sv_part_d = take((size_t)c.R_max * c.L * L.sv_nch_d * sizeof(float2));
+    L.sv_part_t = take((size_t)c.R_max * (c.L + 1) * L.sv_nch_t * sizeof(float2));
+    L.sv_cnt = take((size_t)2 * c.R_max * sizeof(unsigned));
+    L.sv_meta = take((size_t)c.R_max * sizeof(int4));
+    L.sv_part_w = take((size_t)c.R_max * L.sv_nch_w * sizeof(float));
     L.total = off;
     return L;
 }
@@ -295,6 +308,14 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->cg_seed_ids = (int32_t *)(w + L.cg_seed_ids);
     ctx->mk_cand = (int32_t *)(w + L.mk_cand);
     ctx->mk_tab = (float *)(w + L.mk_tab);
+    ctx->sv_nch_d = L.sv_nch_d;
+    ctx->sv_nch_t = L.sv_nch_t;
+    ctx->sv_nch_w = L.sv_nch_w;
+    ctx->sv_part_d = (float2 *)(w + L.sv_part_d);
+    ctx->sv_part_t = (float2 *)(w + L.sv_part_t);
+    ctx->sv_cnt = (unsigned *)(w + L.sv_cnt);
+    ctx->sv_meta = (int4 *)(w + L.sv_meta);
+    ctx->sv_part_w = (float *)(w + L.sv_part_w);
     ctx->att_grid = ctx->num_sms;
     ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so
@@ -535,6 +556,25 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
     DDT_TRY(launch_walk_compact(ctx, nullptr, true, argmax_out, tree_tokens, parents, n_nodes, R,
                                 acc_len, acc_nodes, acc_tokens, bonus, true, true, k_cache, v_cache,
                                 block_table, ctx_lens, k_tree, v_tree, s));
+    return DDT_OK;
+}
+
+ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
+                                 const void *target_logits, const int32_t *draft_tokens,
+                                 const float *u, const float *r, int32_t R, int32_t *acc_len,
+                                 int32_t *acc_tokens, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!draft_logits || !target_logits || !draft_tokens || !u || !r || !acc_len || !acc_tokens)
+        return DDT_EINVAL;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_accept_stochastic(ctx, draft_logits, target_logits, draft_tokens, u, r, R,
+                                     acc_len, acc_tokens, (cudaStream_t)stream));
     return DDT_OK;
 }
 

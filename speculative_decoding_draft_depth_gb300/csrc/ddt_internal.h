@@ -77,6 +77,13 @@ struct ddt_ctx {
     // SparklingTree table tree (prefilter > 0)
     int32_t *mk_cand;        // [R_max, L, C] kept tokens (ddt_round_markov)
     float *mk_tab;           // [R_max, L, C, C] the table (ddt_round_markov)
+    // stochastic chain verification
+    int sv_nch_d, sv_nch_t, sv_nch_w;  // chunks per draft row, target row, drawn row
+    float2 *sv_part_d;       // [R_max * L, sv_nch_d] (max, sum of exp)
+    float2 *sv_part_t;       // [R_max * (L + 1), sv_nch_t]
+    unsigned *sv_cnt;        // [2 * R_max] arrival counters of the two kernels (self-resetting)
+    int4 *sv_meta;           // [R_max] (k*, log Z of target row k*, of draft row k*, 0)
+    float *sv_part_w;        // [R_max, sv_nch_w] chunk totals of the draw's weights
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };
@@ -132,6 +139,13 @@ cudaError_t launch_markov_table(const ddt_ctx *c, const uint16_t *ell, const uin
 cudaError_t launch_markov_tree(const ddt_ctx *c, const int32_t *cand, const float *tab, int R,
                                int32_t *tree_tokens, int32_t *parents, int32_t *depths,
                                int32_t *n_nodes, uint32_t *mask, cudaStream_t s);
+
+// stochastic verification of a chain (stochastic.cu)
+int stochastic_chunk_elems(int dtype);
+int stochastic_draw_chunks(int V);
+cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const void *target,
+                                     const int32_t *tokens, const float *u, const float *r, int R,
+                                     int32_t *acc_len, int32_t *acc_tokens, cudaStream_t s);
 
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,

@@ -1,0 +1,545 @@
+// stochastic.cu -- stochastic verification of a drafted chain at temperature
+// 1 ("DSpark Speculative Decoding Explained: Block Drafting and Confidence
+// Checks", the probability rule): guess x_k is kept with probability
+// min(1, p_k(x_k) / q_k(x_k)); the first rejected guess is replaced by a draw
+// from max(0, p_k - q_k) and the guesses after it are dropped; when every
+// guess survives, a bonus token is drawn from p_L. The uniforms are inputs:
+// u[k] decides guess k (kept iff u[k] < min(1, p/q)); r draws by inverse CDF
+// over the vocabulary in index order (the first index whose running sum of
+// weights exceeds r times their total).
+//
+// Design (HBM-bound: every logit is read once, the drawn row once more):
+//  * sv_rows_kernel: one CTA per (request, row, chunk of 16 KB-32 KB); each
+//    thread keeps 8 vectors of 16 bytes in registers and the CTA reduces
+//    them to the chunk's (max, sum of exp). CTAs run request by request; the
+//    last CTA of a request to finish (an arrival counter) merges its rows'
+//    pairs into log-partitions, reads the 2L logits of the guesses, runs the
+//    L decisions in one warp (a ballot finds the first rejection k*) and
+//    writes the accepted prefix, the length and (k*, the two
+//    log-partitions of row k*) for the draw.
+//  * sv_draw_kernel (a dependent launch): one CTA per (request, chunk of
+//    8192 weights) sums the draw's weights of its chunk; the last CTA of a
+//    request adds the chunk totals in index order, finds the chunk that holds
+//    r * total, re-reads that chunk in index order (32 consecutive weights per
+//    thread, a block scan) and picks the first index whose running sum
+//    exceeds it.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "ddt_device.cuh"
+#include "ddt_internal.h"
+#include "logit_vec.cuh"
+
+namespace {
+
+constexpr int SV_THREADS = 256;
+constexpr int SV_NV = 8;                   // 16-byte vectors per thread in the row pass
+constexpr int SV_WPT = 32;                 // weights per thread in the draw
+constexpr int SV_WCH = SV_THREADS * SV_WPT;  // weights per CTA of the draw (8192)
+
+// ---------------------------------------------------------------- row pass
+// (max, sum of exp(x - max)) of one chunk of a row, for the whole CTA; the
+// result is valid in thread 0
+template <typename T, bool ALIGNED>
+DDT_DEVINL void chunk_ms(const T *__restrict__ zrow, int c0, int cn, float &M, float &S,
+                         float *s_m, float *s_s)
+{
+    constexpr int VE = Elem<T>::VE;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint4 raw[SV_NV];
+#pragma unroll
+    for (int j = 0; j < SV_NV; ++j) {
+        const int e0 = (j * SV_THREADS + tid) * VE;
+        if (ALIGNED) {
+            if (e0 < cn)
+                raw[j] = ldg_stream(zrow + c0 + e0);
+            else
+                raw[j] = make_uint4(Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL,
+                                    Elem<T>::NEG_INF_FILL, Elem<T>::NEG_INF_FILL);
+        } else {
+            raw[j] = load_scalar<T>(zrow + c0 + e0, e0 < cn ? min(VE, cn - e0) : 0);
+        }
+    }
+    float m = DDT_NEG_INF;
+#pragma unroll
+    for (int j = 0; j < SV_NV; ++j)
+        m = fmaxf(m, vec_max<T>(raw[j]));
+    float s = 0.f;
+    if (m != DDT_NEG_INF) {
+        const float nb = -m * DDT_LOG2E;
+        if constexpr (sizeof(T) == 2) {
+            const uint64_t c2 = f2pack(DDT_LOG2E, DDT_LOG2E), b2 = f2pack(nb, nb);
+            uint64_t acc0 = f2pack(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+            for (int j = 0; j < SV_NV; ++j) {
+                acc0 = f2add(acc0, exp_pair(raw[j].x, c2, b2));
+                acc1 = f2add(acc1, exp_pair(raw[j].y, c2, b2));
+                acc0 = f2add(acc0, exp_pair(raw[j].z, c2, b2));
+                acc1 = f2add(acc1, exp_pair(raw[j].w, c2, b2));
+            }
+            float a0, a1, a2, a3;
+            f2unpack(acc0, a0, a1);
+            f2unpack(acc1, a2, a3);
+            s = (a0 + a1) + (a2 + a3);
+        } else {
+#pragma unroll
+            for (int j = 0; j < SV_NV; ++j)
+#pragma unroll
+                for (int e = 0; e < VE; ++e)
+                    s += ex2(fmaf(Elem<T>::get(raw[j], e), DDT_LOG2E, nb));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+        const float so = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+        ms_combine(m, s, mo, so);
+    }
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_s[warp] = s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        M = s_m[0];
+        S = s_s[0];
+        for (int w = 1; w < SV_THREADS / 32; ++w)
+            ms_combine(M, S, s_m[w], s_s[w]);
+    }
+}
+
+// one logit of a row (the guess's), as fp32
+template <typename T>
+DDT_DEVINL float logit_at(const T *row, int x)
+{
+    if constexpr (sizeof(T) == 2)
+        return bf16_to_f32(row[x]);
+    else
+        return row[x];
+}
+
+struct RowsArgs {
+    const void *draft;        // [R, L, V] draft logits
+    const void *target;       // [R, L + 1, V] target logits
+    const int32_t *tokens;    // [R, L] the guesses
+    const float *u;           // [R, L] acceptance uniforms
+    float2 *part_d, *part_t;  // chunk (max, sum) pairs of the draft / target rows
+    unsigned *cnt;            // [R] arrivals (self-resetting)
+    int4 *meta;               // [R] (k*, log Z_t of row k*, log Z_d of row k*, 0)
+    int32_t *acc_len;         // [R]
+    int32_t *acc_tokens;      // [R, L + 1]
+    int32_t *status;
+    int L, V, nch_d, nch_t;
+    bool al_d, al_t;          // 16-byte aligned rows
+};
+
+// grid: R * (L * nch_d + (L + 1) * nch_t) CTAs, request-major, so requests
+// finish (and decide) one after another while the rest stream in
+template <typename TD, typename TT>
+__global__ void __launch_bounds__(SV_THREADS)
+sv_rows_kernel(RowsArgs a)
+{
+    const int L = a.L, V = a.V;
+    const int per = L * a.nch_d + (L + 1) * a.nch_t;
+    const int i = blockIdx.x / per, j = blockIdx.x % per;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
+    __shared__ float s_lse[2 * DDT_MAX_L + 1], s_lz[2 * DDT_MAX_L + 1];
+    __shared__ int s_last;
+    pdl_trigger();
+
+    float M = 0.f, S = 0.f;
+    float2 *slot;
+    if (j < L * a.nch_d) {  // a draft row
+        const int row = i * L + j / a.nch_d, c = j % a.nch_d;
+        constexpr int CH = SV_THREADS * SV_NV * Elem<TD>::VE;
+        const TD *z = static_cast<const TD *>(a.draft) + (int64_t)row * V;
+        if (a.al_d)
+            chunk_ms<TD, true>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
+        else
+            chunk_ms<TD, false>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
+        slot = a.part_d + (int64_t)row * a.nch_d + c;
+    } else {  // a target row
+        const int jt = j - L * a.nch_d;
+        const int row = i * (L + 1) + jt / a.nch_t, c = jt % a.nch_t;
+        constexpr int CH = SV_THREADS * SV_NV * Elem<TT>::VE;
+        const TT *z = static_cast<const TT *>(a.target) + (int64_t)row * V;
+        if (a.al_t)
+            chunk_ms<TT, true>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
+        else
+            chunk_ms<TT, false>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
+        slot = a.part_t + (int64_t)row * a.nch_t + c;
+    }
+    if (tid == 0) {
+        if (M != M || S != S)
+            set_status(a.status, DDT_DEV_NAN_LOGITS);
+        *slot = make_float2(M, S);
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.cnt[i], 1u);
+        s_last = (prev == (unsigned)per - 1u);
+        if (s_last)
+            a.cnt[i] = 0u;  // every arrival of this call is in: ready for the next
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+
+    // ---- the request's last CTA: log-partitions of its 2L + 1 rows (draft
+    // rows 0..L-1, then target rows 0..L) and the guesses' log-probs
+    const TD *zd = static_cast<const TD *>(a.draft) + (int64_t)i * L * V;
+    const TT *zt = static_cast<const TT *>(a.target) + (int64_t)i * (L + 1) * V;
+    for (int t = warp; t < 2 * L + 1; t += SV_THREADS / 32) {
+        const bool isd = t < L;
+        const int k = isd ? t : t - L;
+        const int nch = isd ? a.nch_d : a.nch_t;
+        const float2 *part = isd ? a.part_d + ((int64_t)i * L + k) * nch
+                                 : a.part_t + ((int64_t)i * (L + 1) + k) * nch;
+        float m = DDT_NEG_INF, s = 0.f;
+        for (int c = lane; c < nch; c += 32) {
+            const float2 p = __ldcg(part + c);
+            ms_combine(m, s, p.x, p.y);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+            const float so = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            ms_combine(m, s, mo, so);
+        }
+        if (lane == 0) {
+            const float lse = m + logf(s);
+            s_lse[t] = lse;
+            float lz = 0.f;
+            if (k < L) {
+                const int x = a.tokens[(int64_t)i * L + k];
+                if (x >= 0 && x < V)
+                    lz = (isd ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x)) -
+                         lse;
+            }
+            s_lz[t] = lz;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        bool keep = false;
+        if (lane < L) {
+            const int x = a.tokens[(int64_t)i * L + lane];
+            const bool ok = x >= 0 && x < V;
+            if (!ok)
+                set_status(a.status, DDT_DEV_BAD_TREE);
+            // min(1, p/q) from the two log-probs; q = 0 gives +inf (or NaN
+            // when p = 0 too), which fminf takes to 1
+            const float ratio = fminf(1.f, expf(s_lz[L + lane] - s_lz[lane]));
+            keep = ok && a.u[(int64_t)i * L + lane] < ratio;
+        }
+        const unsigned kept = __ballot_sync(0xFFFFFFFFu, keep);
+        const int ks = __ffs(~kept) - 1;  // lanes >= L never keep: ks <= L
+        if (lane == 0) {
+            a.meta[i] = make_int4(ks, __float_as_int(s_lse[L + ks]),
+                                  __float_as_int(ks < L ? s_lse[ks] : 0.f), 0);
+            a.acc_len[i] = ks + 1;
+        }
+        for (int t = lane; t <= L; t += 32)
+            if (t != ks)
+                a.acc_tokens[(int64_t)i * (L + 1) + t] =
+                    t < ks ? a.tokens[(int64_t)i * L + t] : -1;
+    }
+}
+
+// ---------------------------------------------------------------- the draw
+struct DrawArgs {
+    const void *draft, *target;
+    const float *r;        // [R] draw uniforms
+    const int4 *meta;      // [R] from sv_rows_kernel
+    float *part_w;         // [R, nchw] chunk totals of the weights
+    unsigned *cnt;         // [R] arrivals (self-resetting)
+    int32_t *acc_tokens;   // [R, L + 1]
+    int L, V, nchw;
+    bool al_d, al_t;
+};
+
+// 8 consecutive logits starting at v0 (a multiple of 8) as fp32; -inf past V
+template <typename T, bool ALIGNED>
+DDT_DEVINL void load8(const T *__restrict__ row, int v0, int V, float (&z)[8])
+{
+    if (ALIGNED && v0 + 8 <= V) {
+        if constexpr (sizeof(T) == 2) {
+            const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(row + v0));
+            z[0] = bf16lo(w.x); z[1] = bf16hi(w.x); z[2] = bf16lo(w.y); z[3] = bf16hi(w.y);
+            z[4] = bf16lo(w.z); z[5] = bf16hi(w.z); z[6] = bf16lo(w.w); z[7] = bf16hi(w.w);
+        } else {
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + v0));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + v0 + 4));
+            z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
+            z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            z[e] = (v0 + e < V) ? logit_at(row, v0 + e) : DDT_NEG_INF;
+    }
+}
+
+// the draw's weights of 8 consecutive tokens: p - q clipped at 0 after a
+// rejection (zd != nullptr), p alone for the bonus draw; p = 2^(z log2 e -
+// log Z log2 e) on the MUFU unit
+template <typename TD, typename TT, bool AD, bool AT>
+DDT_DEVINL void weights8(const TD *zd, const TT *zt, int v0, int V, float bd, float bt,
+                         float (&w)[8])
+{
+    float z[8];
+    load8<TT, AT>(zt, v0, V, z);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        w[e] = ex2(fmaf(z[e], DDT_LOG2E, bt));
+    if (zd != nullptr) {
+        load8<TD, AD>(zd, v0, V, z);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float q = ex2(fmaf(z[e], DDT_LOG2E, bd));
+            w[e] = w[e] > q ? w[e] - q : 0.f;
+        }
+    }
+}
+
+template <typename TD, typename TT, bool AD, bool AT>
+DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
+{
+    const int L = a.L, V = a.V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ float s_w[SV_THREADS / 32];
+    __shared__ int s_last, s_chunk, s_pick;
+    __shared__ float s_x;
+
+    const int4 mt = __ldcg(a.meta + i);
+    const int ks = mt.x;
+    const float bt = -__int_as_float(mt.y) * DDT_LOG2E;
+    const float bd = -__int_as_float(mt.z) * DDT_LOG2E;
+    const TT *zt = static_cast<const TT *>(a.target) + ((int64_t)i * (L + 1) + ks) * V;
+    const TD *zd = ks < L ? static_cast<const TD *>(a.draft) + ((int64_t)i * L + ks) * V : nullptr;
+
+    // ---- this chunk's total (coalesced: groups of 8 tokens, thread-interleaved)
+    float t = 0.f;
+#pragma unroll
+    for (int g = 0; g < SV_WPT / 8; ++g) {
+        float w[8];
+        weights8<TD, TT, AD, AT>(zd, zt, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, bd, bt, w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            t += w[e];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+    if (lane == 0)
+        s_w[warp] = t;
+    __syncthreads();
+    if (tid == 0) {
+        float ct = 0.f;
+        for (int w = 0; w < SV_THREADS / 32; ++w)
+            ct += s_w[w];
+        a.part_w[(int64_t)i * a.nchw + c] = ct;
+        __threadfence();
+        const unsigned prev = atomicAdd(&a.cnt[i], 1u);
+        s_last = (prev == (unsigned)a.nchw - 1u);
+        if (s_last)
+            a.cnt[i] = 0u;
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+
+    // ---- the request's last CTA: the chunk that holds r * total (fp64 sums
+    // in index order)
+    if (tid == 0) {
+        double W = 0.0;
+        for (int k = 0; k < a.nchw; ++k)
+            W += (double)__ldcg(a.part_w + (int64_t)i * a.nchw + k);
+        const double x = (double)a.r[i] * W;
+        double run = 0.0;
+        int k = 0, last = -1;
+        for (; k < a.nchw; ++k) {
+            const float tk = __ldcg(a.part_w + (int64_t)i * a.nchw + k);
+            if (tk > 0.f)
+                last = k;
+            if (run + (double)tk > x)
+                break;
+            run += (double)tk;
+        }
+        if (k == a.nchw) {  // x at the total (rounding, or no weight at all)
+            k = last;
+            s_x = __builtin_huge_valf();
+        } else {
+            s_x = (float)(x - run);
+        }
+        s_chunk = k;
+        s_pick = 0x7FFFFFFF;
+    }
+    __syncthreads();
+    const int ch = s_chunk;
+    int tok = -1;
+    if (ch >= 0) {
+        // 32 consecutive weights per thread, an exclusive scan over threads
+        const float xin = s_x;
+        const int v0 = ch * SV_WCH + tid * SV_WPT;
+        float w[SV_WPT], st = 0.f;
+#pragma unroll
+        for (int g = 0; g < SV_WPT / 8; ++g) {
+            float w8[8];
+            weights8<TD, TT, AD, AT>(zd, zt, v0 + g * 8, V, bd, bt, w8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                w[g * 8 + e] = w8[e];
+                st += w8[e];
+            }
+        }
+        float incl = st;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        __syncthreads();  // s_w reuse
+        if (lane == 31)
+            s_w[warp] = incl;
+        __syncthreads();
+        float cum = incl - st;
+        for (int q = 0; q < warp; ++q)
+            cum += s_w[q];
+        int first = 0x7FFFFFFF, lastpos = -1;
+#pragma unroll
+        for (int e = 0; e < SV_WPT; ++e) {
+            cum += w[e];
+            if (w[e] > 0.f) {
+                lastpos = v0 + e;
+                if (first == 0x7FFFFFFF && cum > xin)
+                    first = v0 + e;
+            }
+        }
+        if (first != 0x7FFFFFFF)
+            atomicMin(&s_pick, first);
+        __syncthreads();
+        if (s_pick == 0x7FFFFFFF) {  // rounding left x past the chunk's sum
+            __syncthreads();
+            if (tid == 0)
+                s_pick = -1;
+            __syncthreads();
+            if (lastpos >= 0)
+                atomicMax(&s_pick, lastpos);
+            __syncthreads();
+        }
+        tok = s_pick;
+    }
+    if (tid == 0)
+        a.acc_tokens[(int64_t)i * (L + 1) + ks] = tok;
+}
+
+// grid (nchw, R): one CTA per (chunk of the drawn row, request)
+template <typename TD, typename TT>
+__global__ void __launch_bounds__(SV_THREADS)
+sv_draw_kernel(DrawArgs a)
+{
+    pdl_wait();  // k* and the log-partitions come from sv_rows_kernel
+    const int c = blockIdx.x, i = blockIdx.y;
+    if (a.al_d) {
+        if (a.al_t)
+            draw_body<TD, TT, true, true>(a, i, c);
+        else
+            draw_body<TD, TT, true, false>(a, i, c);
+    } else {
+        if (a.al_t)
+            draw_body<TD, TT, false, true>(a, i, c);
+        else
+            draw_body<TD, TT, false, false>(a, i, c);
+    }
+}
+
+}  // namespace
+
+int stochastic_chunk_elems(int dtype)
+{
+    return SV_THREADS * SV_NV * (dtype == DDT_BF16 ? 8 : 4);
+}
+
+int stochastic_draw_chunks(int V)
+{
+    return (V + SV_WCH - 1) / SV_WCH;
+}
+
+cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const void *target,
+                                     const int32_t *tokens, const float *u, const float *r, int R,
+                                     int32_t *acc_len, int32_t *acc_tokens, cudaStream_t s)
+{
+    const ddt_config &cfg = c->cfg;
+    const int L = cfg.L, V = cfg.V;
+    const int esd = cfg.draft_dtype == DDT_BF16 ? 2 : 4, est = cfg.target_dtype == DDT_BF16 ? 2 : 4;
+    RowsArgs ra;
+    ra.draft = draft;
+    ra.target = target;
+    ra.tokens = tokens;
+    ra.u = u;
+    ra.part_d = c->sv_part_d;
+    ra.part_t = c->sv_part_t;
+    ra.cnt = c->sv_cnt;
+    ra.meta = c->sv_meta;
+    ra.acc_len = acc_len;
+    ra.acc_tokens = acc_tokens;
+    ra.status = c->status;
+    ra.L = L;
+    ra.V = V;
+    ra.nch_d = c->sv_nch_d;
+    ra.nch_t = c->sv_nch_t;
+    ra.al_d = ((int64_t)V * esd) % 16 == 0 && ((uintptr_t)draft % 16) == 0;
+    ra.al_t = ((int64_t)V * est) % 16 == 0 && ((uintptr_t)target % 16) == 0;
+    const int64_t nrows = (int64_t)R * (L * ra.nch_d + (L + 1) * ra.nch_t);
+    if (nrows > 0x7FFFFFFF)
+        return cudaErrorInvalidConfiguration;
+    const bool bd = cfg.draft_dtype == DDT_BF16, bt = cfg.target_dtype == DDT_BF16;
+    if (bd && bt)
+        sv_rows_kernel<uint16_t, uint16_t><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);
+    else if (bd)
+        sv_rows_kernel<uint16_t, float><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);
+    else if (bt)
+        sv_rows_kernel<float, uint16_t><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);
+    else
+        sv_rows_kernel<float, float><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+
+    DrawArgs da;
+    da.draft = draft;
+    da.target = target;
+    da.r = r;
+    da.meta = c->sv_meta;
+    da.part_w = c->sv_part_w;
+    da.cnt = c->sv_cnt + c->cfg.R_max;
+    da.acc_tokens = acc_tokens;
+    da.L = L;
+    da.V = V;
+    da.nchw = c->sv_nch_w;
+    da.al_d = ra.al_d;
+    da.al_t = ra.al_t;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)da.nchw, (unsigned)R);
+    lc.blockDim = dim3(SV_THREADS);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (bd && bt)
+        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, uint16_t>, da);
+    else if (bd)
+        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, float>, da);
+    else if (bt)
+        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<float, uint16_t>, da);
+    else
+        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<float, float>, da);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}

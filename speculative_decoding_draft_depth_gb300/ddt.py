@@ -21,8 +21,8 @@ DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
 EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
            "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
            "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_round_conditioned",
-           "ddt_markov_table", "ddt_build_tree_markov", "ddt_round_markov", "ddt_device_status",
-           "ddt_strerror", "ddt_last_cuda_error")
+           "ddt_markov_table", "ddt_build_tree_markov", "ddt_round_markov",
+           "ddt_accept_stochastic", "ddt_device_status", "ddt_strerror", "ddt_last_cuda_error")
 
 
 class DdtError(RuntimeError):
@@ -88,6 +88,7 @@ def load(path=LIB_PATH):
         "ddt_markov_table": ([_P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
         "ddt_build_tree_markov": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
         "ddt_round_markov": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
+        "ddt_accept_stochastic": ([_P, _P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
         "ddt_last_cuda_error": ([], i32),
@@ -208,6 +209,13 @@ class Context:
                                _ptr(acc_tokens), _ptr(bonus), _ptr(k_cache), _ptr(v_cache),
                                _ptr(block_table), _ptr(k_tree), _ptr(v_tree), _ptr(ctx_lens),
                                _stream(stream)), "ddt_accept")
+
+    def ddt_accept_stochastic(self, draft_logits, target_logits, draft_tokens, u, r, R, acc_len,
+                              acc_tokens, stream=None):
+        _check(_lib.ddt_accept_stochastic(self._h, _ptr(draft_logits), _ptr(target_logits),
+                                          _ptr(draft_tokens), _ptr(u), _ptr(r), R, _ptr(acc_len),
+                                          _ptr(acc_tokens), _stream(stream)),
+               "ddt_accept_stochastic")
 
     def ddt_round(self, R, bufs, stream=None, att_events=None):
         """bufs: dict of tensors named like the fields of ddt_round_args.

@@ -28,6 +28,13 @@ draws stand in for them):
   sparkling R=64, L=15, V=151936, the SparklingTree table tree: top-C=128
            prefilter per depth, Markov head W, E bf16 N(0, 0.02) [V, 256],
            budget B=64; logits, contexts and agreement as batch64  (seed 5)
+
+Chains for stochastic verification (draw_chain_inputs): the draft logits of
+the chosen workload; target rows 0..L-1 are the draft row plus N(0, s_r^2)
+noise with s_r ~ U[0.2, 1.0] per request, row L is a fresh draw like a draft
+row; the guesses are sampled from the draft rows at temperature 1 (Gumbel-max
+on the stored logits, a data-construction step); u [R, L] and r [R] are
+float32 uniforms in [0, 1).
 """
 from dataclasses import dataclass, field, replace
 
@@ -246,6 +253,35 @@ def draw_next_round(cfg, k, seed=None):
     agree = draw_agreement(cfg, rng)
     return dict(draft=draft, draft_logits=draft.z, q=q, k_tree=k_tree, v_tree=v_tree,
                 agree=agree)
+
+
+def draw_chain_inputs(cfg, seed=None, noise=(0.2, 1.0)):
+    """One batch of drafted chains for stochastic verification: draft
+    [R, L, V] and target [R, L+1, V] logits (cfg.logit_dtype), guesses
+    tokens [R, L] int32, u [R, L] and r [R] float32 in [0, 1), and the
+    per-request noise scale s [R]."""
+    rng = np.random.default_rng([cfg.seed if seed is None else seed, 23])
+    R, L, V = cfg.R, cfg.L, cfg.V
+    draft = draw_draft_logits(cfg, rng).z
+    bf16 = cfg.logit_dtype == "bf16"
+    target = np.empty((R, L + 1, V), np.uint16 if bf16 else np.float32)
+    tokens = np.empty((R, L), np.int32)
+    sig = rng.uniform(noise[0], noise[1], size=R).astype(np.float32)
+    one = replace(cfg, R=1, L=1)
+    for i in range(R):
+        zd = bf16_bits_to_f32(draft[i]) if bf16 else draft[i]
+        zt = zd + sig[i] * rng.standard_normal((L, V), dtype=np.float32)
+        last = draw_draft_logits(one, rng).z[0]
+        target[i, :L] = to_bf16_bits(zt) if bf16 else zt
+        target[i, L] = last[0]
+        # Gumbel-max: -log of a unit exponential is a standard Gumbel draw
+        e = rng.standard_exponential((L, V), dtype=np.float32)
+        np.maximum(e, np.float32(1e-30), out=e)
+        np.log(e, out=e)
+        tokens[i] = np.argmax(zd - e, axis=-1)
+    u = rng.random((R, L), dtype=np.float32)
+    r = rng.random(R, dtype=np.float32)
+    return dict(draft=draft, target=target, tokens=tokens, u=u, r=r, noise=sig)
 
 
 # ---------------------------------------------------------------- target
