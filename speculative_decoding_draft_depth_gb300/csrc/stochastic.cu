@@ -9,14 +9,14 @@
 // weights exceeds r times their total).
 //
 // Design (HBM-bound: every logit is read once, the drawn row once more):
-//  * sv_rows_kernel: one CTA per (request, row, chunk of 16 KB-32 KB); each
+//  * sv_rows_kernel: one CTA per (request, row, chunk of 32 KB); each
 //    thread keeps 8 vectors of 16 bytes in registers and the CTA reduces
 //    them to the chunk's (max, sum of exp). CTAs run request by request; the
 //    last CTA of a request to finish (an arrival counter) merges its rows'
-//    pairs into log-partitions, reads the 2L logits of the guesses, runs the
-//    L decisions in one warp (a ballot finds the first rejection k*) and
-//    writes the accepted prefix, the length and (k*, the two
-//    log-partitions of row k*) for the draw.
+//    pairs into log-partitions (a warp per row), reads the 2L logits of the
+//    guesses, runs the L decisions in one warp (a ballot finds the first
+//    rejection k*) and writes the accepted prefix, the length and (k*, the
+//    two log-partitions of row k*) for the draw.
 //  * sv_draw_kernel (a dependent launch): one CTA per (request, chunk of
 //    8192 weights) sums the draw's weights of its chunk; the last CTA of a
 //    request adds the chunk totals in index order, finds the chunk that holds
@@ -256,51 +256,97 @@ struct DrawArgs {
     unsigned *cnt;         // [R] arrivals (self-resetting)
     int32_t *acc_tokens;   // [R, L + 1]
     int L, V, nchw;
-    bool al_d, al_t;
+    bool al_d, al_t;  // (host side: selects the kernel)
 };
 
-// 8 consecutive logits starting at v0 (a multiple of 8) as fp32; -inf past V
-template <typename T, bool ALIGNED>
-DDT_DEVINL void load8(const T *__restrict__ row, int v0, int V, float (&z)[8])
+// one group of 8 consecutive logits (v0 a multiple of 8) as raw 16-byte
+// vectors: one for bf16, two for fp32; -inf past V
+template <typename T> struct Grp {
+    static constexpr int NU = sizeof(T) / 2;  // 16-byte vectors per group
+    static constexpr int VE = Elem<T>::VE;
+    uint4 u[NU];
+    DDT_DEVINL float at(int e) const { return Elem<T>::get(u[e / VE], e % VE); }
+};
+
+template <typename T, bool AL>
+DDT_DEVINL void ld_group(const T *__restrict__ row, int v0, int V, Grp<T> &g)
 {
-    if (ALIGNED && v0 + 8 <= V) {
-        if constexpr (sizeof(T) == 2) {
-            const uint4 w = __ldcg(reinterpret_cast<const uint4 *>(row + v0));
-            z[0] = bf16lo(w.x); z[1] = bf16hi(w.x); z[2] = bf16lo(w.y); z[3] = bf16hi(w.y);
-            z[4] = bf16lo(w.z); z[5] = bf16hi(w.z); z[6] = bf16lo(w.w); z[7] = bf16hi(w.w);
-        } else {
-            const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + v0));
-            const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + v0 + 4));
-            z[0] = a.x; z[1] = a.y; z[2] = a.z; z[3] = a.w;
-            z[4] = b.x; z[5] = b.y; z[6] = b.z; z[7] = b.w;
-        }
+    constexpr int NU = Grp<T>::NU, VE = Grp<T>::VE;
+    if (AL && v0 + 8 <= V) {
+#pragma unroll
+        for (int k = 0; k < NU; ++k)
+            g.u[k] = __ldcg(reinterpret_cast<const uint4 *>(row + v0) + k);
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            z[e] = (v0 + e < V) ? logit_at(row, v0 + e) : DDT_NEG_INF;
+        for (int k = 0; k < NU; ++k) {
+            const int n = V - (v0 + k * VE);
+            g.u[k] = load_scalar<T>(row + v0 + k * VE, n <= 0 ? 0 : (n < VE ? n : VE));
+        }
     }
 }
 
-// the draw's weights of 8 consecutive tokens: p - q clipped at 0 after a
-// rejection (zd != nullptr), p alone for the bonus draw; p = 2^(z log2 e -
-// log Z log2 e) on the MUFU unit
-template <typename TD, typename TT, bool AD, bool AT>
-DDT_DEVINL void weights8(const TD *zd, const TT *zt, int v0, int V, float bd, float bt,
-                         float (&w)[8])
+// the draw's weight of one token: p - q clipped at 0 after a rejection,
+// p alone for the bonus draw; p = 2^(z log2 e - log Z log2 e) on the MUFU unit
+DDT_DEVINL float draw_weight(float zt, float zd, float bt, float bd, bool leftover)
 {
-    float z[8];
-    load8<TT, AT>(zt, v0, V, z);
+    const float p = ex2(fmaf(zt, DDT_LOG2E, bt));
+    if (!leftover)
+        return p;
+    const float q = ex2(fmaf(zd, DDT_LOG2E, bd));
+    return p > q ? p - q : 0.f;
+}
+
+constexpr int SV_G = SV_WPT / 8;  // groups of 8 weights per thread
+
+// sum of the draw's weights of tokens v0 .. v0 + 31 (in index order)
+template <typename TD, typename TT, bool AD, bool AT>
+DDT_DEVINL float thread_sum(const TT *zt, const TD *zd, int v0, int V, float bt, float bd,
+                            bool leftover)
+{
+    Grp<TT> gt[SV_G];
+    Grp<TD> gd[SV_G];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-        w[e] = ex2(fmaf(z[e], DDT_LOG2E, bt));
-    if (zd != nullptr) {
-        load8<TD, AD>(zd, v0, V, z);
+    for (int g = 0; g < SV_G; ++g)
+        ld_group<TT, AT>(zt, v0 + g * 8, V, gt[g]);
+    if (leftover) {
+#pragma unroll
+        for (int g = 0; g < SV_G; ++g)
+            ld_group<TD, AD>(zd, v0 + g * 8, V, gd[g]);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int g = 0; g < SV_G; ++g)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            s += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
+    return s;
+}
+
+// tokens v0 .. v0 + 31 with running sum `cum` before them: the first positive
+// weight whose running sum exceeds x, else (x = +inf) the last positive one
+template <typename TD, typename TT, bool AD, bool AT>
+__device__ __noinline__ int fine_search(const TT *zt, const TD *zd, int v0, int V, float bt,
+                                        float bd, bool leftover, float cum, float x)
+{
+    int last = -1;
+    for (int g = 0; g < SV_G; ++g) {
+        Grp<TT> gt;
+        Grp<TD> gd;
+        ld_group<TT, AT>(zt, v0 + g * 8, V, gt);
+        if (leftover)
+            ld_group<TD, AD>(zd, v0 + g * 8, V, gd);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float q = ex2(fmaf(z[e], DDT_LOG2E, bd));
-            w[e] = w[e] > q ? w[e] - q : 0.f;
+            const float w = draw_weight(gt.at(e), leftover ? gd.at(e) : 0.f, bt, bd, leftover);
+            cum += w;
+            if (w > 0.f) {
+                last = v0 + g * 8 + e;
+                if (cum > x)
+                    return last;
+            }
         }
     }
+    return last;
 }
 
 template <typename TD, typename TT, bool AD, bool AT>
@@ -314,21 +360,30 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
 
     const int4 mt = __ldcg(a.meta + i);
     const int ks = mt.x;
+    const bool leftover = ks < L;
     const float bt = -__int_as_float(mt.y) * DDT_LOG2E;
     const float bd = -__int_as_float(mt.z) * DDT_LOG2E;
     const TT *zt = static_cast<const TT *>(a.target) + ((int64_t)i * (L + 1) + ks) * V;
-    const TD *zd = ks < L ? static_cast<const TD *>(a.draft) + ((int64_t)i * L + ks) * V : nullptr;
+    const TD *zd = static_cast<const TD *>(a.draft) + ((int64_t)i * L + (leftover ? ks : 0)) * V;
 
-    // ---- this chunk's total (coalesced: groups of 8 tokens, thread-interleaved)
+    // ---- this chunk's total: every load issued before any arithmetic;
+    // groups of 8 tokens interleaved across threads (coalesced)
+    Grp<TT> gt[SV_G];
+    Grp<TD> gd[SV_G];
+#pragma unroll
+    for (int g = 0; g < SV_G; ++g)
+        ld_group<TT, AT>(zt, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, gt[g]);
+    if (leftover) {
+#pragma unroll
+        for (int g = 0; g < SV_G; ++g)
+            ld_group<TD, AD>(zd, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, gd[g]);
+    }
     float t = 0.f;
 #pragma unroll
-    for (int g = 0; g < SV_WPT / 8; ++g) {
-        float w[8];
-        weights8<TD, TT, AD, AT>(zd, zt, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, bd, bt, w);
+    for (int g = 0; g < SV_G; ++g)
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-            t += w[e];
-    }
+            t += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
@@ -351,50 +406,66 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
         return;
     __threadfence();
 
-    // ---- the request's last CTA: the chunk that holds r * total (fp64 sums
-    // in index order)
-    if (tid == 0) {
+    // ---- the request's last CTA. Warp 0: the weights' total W (fp64), then
+    // the first chunk whose running total (fp64, index order) exceeds r * W
+    if (warp == 0) {
+        const float *pw = a.part_w + (int64_t)i * a.nchw;
         double W = 0.0;
-        for (int k = 0; k < a.nchw; ++k)
-            W += (double)__ldcg(a.part_w + (int64_t)i * a.nchw + k);
+        int lastpos = -1;
+        for (int b = 0; b < a.nchw; b += 32) {
+            const float tk = (b + lane < a.nchw) ? __ldcg(pw + b + lane) : 0.f;
+            double s = tk;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            W += s;
+            const unsigned pos = __ballot_sync(0xFFFFFFFFu, tk > 0.f);
+            if (pos)
+                lastpos = b + 31 - __clz(pos);
+        }
         const double x = (double)a.r[i] * W;
         double run = 0.0;
-        int k = 0, last = -1;
-        for (; k < a.nchw; ++k) {
-            const float tk = __ldcg(a.part_w + (int64_t)i * a.nchw + k);
-            if (tk > 0.f)
-                last = k;
-            if (run + (double)tk > x)
-                break;
-            run += (double)tk;
+        int found = -1;
+        float xin = 0.f;
+        for (int b = 0; b < a.nchw && found < 0; b += 32) {
+            const float tk = (b + lane < a.nchw) ? __ldcg(pw + b + lane) : 0.f;
+            double incl = tk;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const double y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o)
+                    incl += y;
+            }
+            incl += run;
+            const unsigned hit = __ballot_sync(0xFFFFFFFFu, incl > x);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                found = b + l;
+                xin = (float)(x - __shfl_sync(0xFFFFFFFFu, incl - (double)tk, l));
+            }
+            run = __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        if (k == a.nchw) {  // x at the total (rounding, or no weight at all)
-            k = last;
-            s_x = __builtin_huge_valf();
-        } else {
-            s_x = (float)(x - run);
+        if (lane == 0) {
+            if (found < 0) {  // x at the total (rounding, or no weight at all)
+                s_chunk = lastpos;
+                s_x = __builtin_huge_valf();
+            } else {
+                s_chunk = found;
+                s_x = xin;
+            }
+            s_pick = 0x7FFFFFFF;
         }
-        s_chunk = k;
-        s_pick = 0x7FFFFFFF;
     }
     __syncthreads();
     const int ch = s_chunk;
     int tok = -1;
     if (ch >= 0) {
-        // 32 consecutive weights per thread, an exclusive scan over threads
+        // 32 consecutive weights per thread (index order): each thread's sum,
+        // an exclusive scan over threads, then the first thread whose range
+        // reaches x re-reads its 32 tokens and finds the crossing one
         const float xin = s_x;
         const int v0 = ch * SV_WCH + tid * SV_WPT;
-        float w[SV_WPT], st = 0.f;
-#pragma unroll
-        for (int g = 0; g < SV_WPT / 8; ++g) {
-            float w8[8];
-            weights8<TD, TT, AD, AT>(zd, zt, v0 + g * 8, V, bd, bt, w8);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                w[g * 8 + e] = w8[e];
-                st += w8[e];
-            }
-        }
+        const float st = thread_sum<TD, TT, AD, AT>(zt, zd, v0, V, bt, bd, leftover);
         float incl = st;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -402,59 +473,46 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
             if (lane >= o)
                 incl += y;
         }
-        __syncthreads();  // s_w reuse
         if (lane == 31)
             s_w[warp] = incl;
         __syncthreads();
         float cum = incl - st;
         for (int q = 0; q < warp; ++q)
             cum += s_w[q];
-        int first = 0x7FFFFFFF, lastpos = -1;
-#pragma unroll
-        for (int e = 0; e < SV_WPT; ++e) {
-            cum += w[e];
-            if (w[e] > 0.f) {
-                lastpos = v0 + e;
-                if (first == 0x7FFFFFFF && cum > xin)
-                    first = v0 + e;
-            }
-        }
-        if (first != 0x7FFFFFFF)
-            atomicMin(&s_pick, first);
+        if (st > 0.f && cum + st > xin)
+            atomicMin(&s_pick, tid);
         __syncthreads();
-        if (s_pick == 0x7FFFFFFF) {  // rounding left x past the chunk's sum
+        int who = s_pick;
+        const bool crossed = who != 0x7FFFFFFF;
+        if (!crossed) {  // rounding left x past the chunk's sum: its last weight
             __syncthreads();
             if (tid == 0)
                 s_pick = -1;
             __syncthreads();
-            if (lastpos >= 0)
-                atomicMax(&s_pick, lastpos);
+            if (st > 0.f)
+                atomicMax(&s_pick, tid);
             __syncthreads();
+            who = s_pick;
         }
-        tok = s_pick;
+        __syncthreads();
+        if (tid == who)
+            s_pick = fine_search<TD, TT, AD, AT>(zt, zd, v0, V, bt, bd, leftover, cum,
+                                                crossed ? xin : __builtin_huge_valf());
+        __syncthreads();
+        tok = who >= 0 ? s_pick : -1;
     }
     if (tid == 0)
         a.acc_tokens[(int64_t)i * (L + 1) + ks] = tok;
 }
 
-// grid (nchw, R): one CTA per (chunk of the drawn row, request)
-template <typename TD, typename TT>
-__global__ void __launch_bounds__(SV_THREADS)
+// grid (nchw, R): one CTA per (chunk of the drawn row, request); AL: both
+// logit tensors have 16-byte aligned rows
+template <typename TD, typename TT, bool AL>
+__global__ void __launch_bounds__(SV_THREADS, sizeof(TD) + sizeof(TT) == 8 ? 3 : 4)
 sv_draw_kernel(DrawArgs a)
 {
     pdl_wait();  // k* and the log-partitions come from sv_rows_kernel
-    const int c = blockIdx.x, i = blockIdx.y;
-    if (a.al_d) {
-        if (a.al_t)
-            draw_body<TD, TT, true, true>(a, i, c);
-        else
-            draw_body<TD, TT, true, false>(a, i, c);
-    } else {
-        if (a.al_t)
-            draw_body<TD, TT, false, true>(a, i, c);
-        else
-            draw_body<TD, TT, false, false>(a, i, c);
-    }
+    draw_body<TD, TT, AL, AL>(a, blockIdx.y, blockIdx.x);
 }
 
 }  // namespace
@@ -533,13 +591,18 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     lc.stream = s;
     lc.attrs = attr;
     lc.numAttrs = 1;
+    const bool al = da.al_d && da.al_t;
     if (bd && bt)
-        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, uint16_t>, da);
+        e = al ? cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, uint16_t, true>, da)
+               : cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, uint16_t, false>, da);
     else if (bd)
-        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, float>, da);
+        e = al ? cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, float, true>, da)
+               : cudaLaunchKernelEx(&lc, sv_draw_kernel<uint16_t, float, false>, da);
     else if (bt)
-        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<float, uint16_t>, da);
+        e = al ? cudaLaunchKernelEx(&lc, sv_draw_kernel<float, uint16_t, true>, da)
+               : cudaLaunchKernelEx(&lc, sv_draw_kernel<float, uint16_t, false>, da);
     else
-        e = cudaLaunchKernelEx(&lc, sv_draw_kernel<float, float>, da);
+        e = al ? cudaLaunchKernelEx(&lc, sv_draw_kernel<float, float, true>, da)
+               : cudaLaunchKernelEx(&lc, sv_draw_kernel<float, float, false>, da);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
