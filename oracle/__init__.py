@@ -21,7 +21,8 @@ Pages cited (by title and section):
       tree construction" (the prefilter and the Markov table: NEXT row 2).
   "DSpark Speculative Decoding Explained: Block Drafting and Confidence
       Checks", the probability rule and its toy (stochastic verification:
-      NEXT row 3).
+      NEXT row 3), and "Survival probability" / "Picking the budget" with the
+      DSpark post's "Hardware aware prefix scheduler" (NEXT row 4).
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test
 against something other than itself (closed forms, brute force, library
@@ -82,6 +83,10 @@ def lib():
         L.orc_verify_chain.restype = i32
         L.orc_accept_stochastic.argtypes = [p, p, i32, p, p, p, i32, i32, i64, p, p]
         L.orc_accept_stochastic.restype = i32
+        L.orc_schedule_prefix.argtypes = [p, i32, i32, p, p, p, p]
+        L.orc_schedule_prefix.restype = i32
+        L.orc_schedule_bruteforce.argtypes = [p, i32, i32, p]
+        L.orc_schedule_bruteforce.restype = ctypes.c_double
         L.orc_num_threads.argtypes = []
         L.orc_num_threads.restype = i32
         _lib = L
@@ -455,3 +460,32 @@ def accept_stochastic(draft, target, tokens, u, r):
     if rc:
         raise ValueError("bad arguments to accept_stochastic")
     return acc_len, acc_tokens
+
+
+def schedule_prefix(conf, cost):
+    """The hardware-aware prefix scheduler ("DSpark Speculative Decoding
+    Explained ...", "Survival probability" and "Picking the budget"):
+    conf [R, L] conditional survival chances, cost [R*L + 1] step costs in
+    ms indexed by the number of verified guesses. Returns n_keep [R],
+    n_total, tokens per ms, expected tokens and the status bits."""
+    conf = np.ascontiguousarray(conf, dtype=np.float64)
+    R, L = conf.shape
+    cost = np.ascontiguousarray(cost, dtype=np.float64)
+    if cost.shape != (R * L + 1,):
+        raise ValueError("cost must have R*L + 1 entries")
+    n_keep = np.empty(R, np.int32)
+    n_total = np.zeros(1, np.int32)
+    stats = np.zeros(2, np.float64)
+    rc = lib().orc_schedule_prefix(_ptr(conf), R, L, _ptr(cost), _ptr(n_keep), _ptr(n_total),
+                                   _ptr(stats))
+    if rc & BAD_ARG:
+        raise ValueError("bad arguments to schedule_prefix")
+    return n_keep, int(n_total[0]), float(stats[0]), float(stats[1]), int(rc)
+
+
+def schedule_bruteforce(conf, cost):
+    """Best tokens per ms over every subset of the slots (R*L <= 20)."""
+    conf = np.ascontiguousarray(conf, dtype=np.float64)
+    R, L = conf.shape
+    cost = np.ascontiguousarray(cost, dtype=np.float64)
+    return float(lib().orc_schedule_bruteforce(_ptr(conf), R, L, _ptr(cost)))

@@ -1325,3 +1325,130 @@ int orc_accept_stochastic(const void *draft, const void *target, int dtype, cons
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------
+ * The hardware-aware prefix scheduler ["DSpark Speculative Decoding
+ * Explained: Block Drafting and Confidence Checks", sections "Survival
+ * probability" and "Picking the budget"; the DSpark speculative-decoder
+ * post, "Hardware aware prefix scheduler"] (NEXT row 4).
+ *
+ * conf [R, L]: the chance that guess k of request r survives, given that the
+ * guesses before it did. Values outside [0, 1] are clamped; NaN counts as 0
+ * and is reported. The survival of slot (r, k) is the product conf[r][0] *
+ * ... * conf[r][k], taken in that order in fp64; it cannot rise along a
+ * block. Slots are ranked by survival, descending; equal survivals go by
+ * position, then request, ascending.
+ *
+ * Verifying the n best slots (n = 0 .. R*L) is expected to commit R + (their
+ * survivals' sum) tokens -- one guaranteed token per request -- at a step
+ * cost of cost[n] milliseconds. The chosen n maximises tokens per
+ * millisecond; the smallest such n wins a tie, and an n whose cost is not
+ * positive (or NaN) is never chosen (n = 0 when none is valid).
+ *
+ * Outputs: n_keep [R] (request r keeps its first n_keep[r] guesses; the
+ * ranking makes the chosen slots a prefix of every block), *n_total, and
+ * stats [2] = (the best tokens per ms, the expected tokens); stats may be
+ * NULL. Returns ORC_NAN_SEEN when a confidence was NaN.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    double s;
+    int k, r;
+} sched_slot;
+
+static int sched_cmp(const void *pa, const void *pb)
+{
+    const sched_slot *a = (const sched_slot *)pa, *b = (const sched_slot *)pb;
+    if (a->s != b->s)
+        return a->s > b->s ? -1 : 1;
+    if (a->k != b->k)
+        return a->k < b->k ? -1 : 1;
+    return a->r < b->r ? -1 : (a->r > b->r ? 1 : 0);
+}
+
+static double sched_conf(double c, int *nan_seen)
+{
+    if (c != c) {
+        *nan_seen = 1;
+        return 0.0;
+    }
+    return c < 0.0 ? 0.0 : (c > 1.0 ? 1.0 : c);
+}
+
+static int sched_cost_ok(double c) { return c == c && c > 0.0; }
+
+int orc_schedule_prefix(const double *conf, int R, int L, const double *cost, int32_t *n_keep,
+                        int32_t *n_total, double *stats)
+{
+    if (R < 0 || L < 1)
+        return ORC_BAD_ARG;
+    const int N = R * L;
+    int nan_seen = 0;
+    sched_slot *slots = (sched_slot *)malloc(sizeof(sched_slot) * (size_t)(N > 0 ? N : 1));
+    for (int r = 0; r < R; ++r) {
+        double s = 1.0;
+        for (int k = 0; k < L; ++k) {
+            s = s * sched_conf(conf[(int64_t)r * L + k], &nan_seen);
+            slots[r * L + k].s = s;
+            slots[r * L + k].k = k;
+            slots[r * L + k].r = r;
+        }
+    }
+    qsort(slots, (size_t)N, sizeof(sched_slot), sched_cmp);
+    /* tokens per ms for every n, the sum growing one slot at a time */
+    int best_n = 0;
+    double best = -INFINITY, best_tokens = (double)R, sum = 0.0;
+    for (int n = 0; n <= N; ++n) {
+        if (n > 0)
+            sum += slots[n - 1].s;
+        if (!sched_cost_ok(cost[n]))
+            continue;
+        const double theta = ((double)R + sum) / cost[n];
+        if (theta > best) {
+            best = theta;
+            best_n = n;
+            best_tokens = (double)R + sum;
+        }
+    }
+    for (int r = 0; r < R; ++r)
+        n_keep[r] = 0;
+    for (int j = 0; j < best_n; ++j)
+        n_keep[slots[j].r] += 1;
+    *n_total = best_n;
+    if (stats) {
+        stats[0] = best == -INFINITY ? 0.0 : best;
+        stats[1] = best_tokens;
+    }
+    free(slots);
+    return nan_seen ? ORC_NAN_SEEN : 0;
+}
+
+/* Brute force for the pins: the best tokens per ms over EVERY subset of the
+ * R*L slots (not only prefixes, no ranking), for R*L <= 20. */
+double orc_schedule_bruteforce(const double *conf, int R, int L, const double *cost)
+{
+    const int N = R * L;
+    if (N > 20 || N < 0)
+        return NAN;
+    double s[20];
+    int nan_seen = 0;
+    for (int r = 0; r < R; ++r) {
+        double p = 1.0;
+        for (int k = 0; k < L; ++k) {
+            p = p * sched_conf(conf[r * L + k], &nan_seen);
+            s[r * L + k] = p;
+        }
+    }
+    double best = -INFINITY;
+    for (uint32_t m = 0; m < (1u << N); ++m) {
+        double tokens = (double)R;
+        int n = 0;
+        for (int j = 0; j < N; ++j)
+            if (m & (1u << j)) {
+                tokens += s[j];
+                ++n;
+            }
+        if (sched_cost_ok(cost[n]) && tokens / cost[n] > best)
+            best = tokens / cost[n];
+    }
+    return best == -INFINITY ? 0.0 : best;
+}
