@@ -336,6 +336,32 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
                                  const float *u, const float *r, int32_t R, int32_t *acc_len,
                                  int32_t *acc_tokens, void *stream);
 
+/* The hardware-aware prefix scheduler -- "DSpark Speculative Decoding
+ * Explained: Block Drafting and Confidence Checks", sections "Survival
+ * probability" and "Picking the budget"; the DSpark post, "Hardware aware
+ * prefix scheduler". Decides how many drafted guesses of each request to
+ * verify in the next step.
+ *   conf    [R, L] f32, device: conf[r][k] is the chance that guess k of
+ *           request r survives given that guesses 0..k-1 did. Values are
+ *           clamped to [0, 1]; NaN counts as 0 and sets DDT_DEV_NAN_LOGITS.
+ *   cost_ms [R*L + 1] f32, device: the step's cost in ms when n guesses are
+ *           verified besides the R guaranteed tokens, n = 0..R*L (a table
+ *           measured beforehand). An n whose cost is not positive (or NaN)
+ *           is never chosen.
+ * The survival of slot (r, k) is conf[r][0] * ... * conf[r][k] (fp64). The
+ * slots of all requests are ranked by survival, descending (ties: lower k,
+ * then lower r first), and n is chosen to maximise (R + the n best
+ * survivals' sum) / cost_ms[n] -- expected committed tokens per ms; the
+ * smallest n wins a tie, and n = 0 when no cost is valid.
+ * Outputs (device): n_keep [R] i32, the guesses request r verifies (always
+ * a prefix of its block); n_total [1] i32 (may be NULL), the chosen n;
+ * stats [2] f64 (may be NULL): the best tokens per ms and the expected
+ * committed tokens. Requires R * L <= DDT_SCHED_MAX_SLOTS (else
+ * DDT_EUNSUPPORTED). One CTA is enqueued on `stream`. */
+#define DDT_SCHED_MAX_SLOTS 8192
+ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const float *cost_ms,
+                               int32_t *n_keep, int32_t *n_total, double *stats, void *stream);
+
 /* Wait for the context's device to finish all enqueued work, copy the
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);

@@ -578,6 +578,25 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
     return DDT_OK;
 }
 
+ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const float *cost_ms,
+                               int32_t *n_keep, int32_t *n_total, double *stats, void *stream)
+{
+    ddt_status st = check_R(ctx, R);
+    if (st != DDT_OK)
+        return st;
+    if (R == 0)
+        return DDT_OK;
+    if (!conf || !cost_ms || !n_keep)
+        return DDT_EINVAL;
+    if ((int64_t)R * ctx->cfg.L > DDT_SCHED_MAX_SLOTS)
+        return DDT_EUNSUPPORTED;
+    if ((st = set_device(ctx)) != DDT_OK)
+        return st;
+    DDT_TRY(launch_schedule_prefix(ctx, conf, R, cost_ms, n_keep, n_total, stats,
+                                   (cudaStream_t)stream));
+    return DDT_OK;
+}
+
 // a4 once the tree (ev_tree) and a5 (ev_join) are done, then a6/a7, on `s`
 static ddt_status round_verify(ddt_ctx *ctx, const ddt_round_args *a, cudaStream_t s)
 {

@@ -147,6 +147,12 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
                                      const int32_t *tokens, const float *u, const float *r, int R,
                                      int32_t *acc_len, int32_t *acc_tokens, cudaStream_t s);
 
+// the hardware-aware prefix scheduler (sched.cu)
+int schedule_smem_bytes(int R, int L);
+cudaError_t launch_schedule_prefix(const ddt_ctx *c, const float *conf, int R, const float *cost,
+                                   int32_t *n_keep, int32_t *n_total, double *stats,
+                                   cudaStream_t s);
+
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,
                                 float *part_val, int32_t *part_idx, float2 *part_ms,

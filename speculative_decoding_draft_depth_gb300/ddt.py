@@ -22,7 +22,8 @@ EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprob
            "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
            "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_round_conditioned",
            "ddt_markov_table", "ddt_build_tree_markov", "ddt_round_markov",
-           "ddt_accept_stochastic", "ddt_device_status", "ddt_strerror", "ddt_last_cuda_error")
+           "ddt_accept_stochastic", "ddt_schedule_prefix", "ddt_device_status", "ddt_strerror",
+           "ddt_last_cuda_error")
 
 
 class DdtError(RuntimeError):
@@ -89,6 +90,7 @@ def load(path=LIB_PATH):
         "ddt_build_tree_markov": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
         "ddt_round_markov": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
         "ddt_accept_stochastic": ([_P, _P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
+        "ddt_schedule_prefix": ([_P, _P, i32, _P, _P, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
         "ddt_last_cuda_error": ([], i32),
@@ -216,6 +218,12 @@ class Context:
                                           _ptr(draft_tokens), _ptr(u), _ptr(r), R, _ptr(acc_len),
                                           _ptr(acc_tokens), _stream(stream)),
                "ddt_accept_stochastic")
+
+    def ddt_schedule_prefix(self, conf, R, cost_ms, n_keep, n_total=None, stats=None,
+                            stream=None):
+        _check(_lib.ddt_schedule_prefix(self._h, _ptr(conf), R, _ptr(cost_ms), _ptr(n_keep),
+                                        _ptr(n_total), _ptr(stats), _stream(stream)),
+               "ddt_schedule_prefix")
 
     def ddt_round(self, R, bufs, stream=None, att_events=None):
         """bufs: dict of tensors named like the fields of ddt_round_args.

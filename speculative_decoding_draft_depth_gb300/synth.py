@@ -35,6 +35,10 @@ noise with s_r ~ U[0.2, 1.0] per request, row L is a fresh draw like a draft
 row; the guesses are sampled from the draft rows at temperature 1 (Gumbel-max
 on the stored logits, a data-construction step); u [R, L] and r [R] are
 float32 uniforms in [0, 1).
+
+Confidences for the prefix scheduler (draw_confidences): per request a base
+chance b_r ~ U[0.5, 0.95]; guess k survives its predecessors with chance
+sigmoid(logit(b_r) - 0.15 k + 0.5 e), e ~ N(0, 1), stored as float32.
 """
 from dataclasses import dataclass, field, replace
 
@@ -282,6 +286,15 @@ def draw_chain_inputs(cfg, seed=None, noise=(0.2, 1.0)):
     u = rng.random((R, L), dtype=np.float32)
     r = rng.random(R, dtype=np.float32)
     return dict(draft=draft, target=target, tokens=tokens, u=u, r=r, noise=sig)
+
+
+def draw_confidences(R, L, seed=0):
+    """[R, L] float32 chances that each drafted guess survives given that
+    the ones before it did (see the module docstring)."""
+    rng = np.random.default_rng([seed, 29])
+    b = rng.uniform(0.5, 0.95, size=(R, 1))
+    z = np.log(b / (1.0 - b)) - 0.15 * np.arange(L) + 0.5 * rng.standard_normal((R, L))
+    return (1.0 / (1.0 + np.exp(-z))).astype(np.float32)
 
 
 # ---------------------------------------------------------------- target
