@@ -191,7 +191,7 @@ def main():
                     help="skip the timing of the NEXT rows (parent-conditioned tree)")
     ap.add_argument("--stage", default="round",
                     choices=["round", "topk", "tree", "attention", "accept", "cond_tree",
-                             "markov", "stochastic"],
+                             "markov", "stochastic", "scheduler"],
                     help="time one stage alone (small profiling cases); cond_tree: the "
                          "parent-conditioned tree's workload alone")
     ap.add_argument("--requests", type=int, default=0,
@@ -215,11 +215,11 @@ def main():
 
     import torch
     torch.cuda.set_device(local_rank)
-    if args.stage in ("cond_tree", "markov", "stochastic"):
+    if args.stage in ("cond_tree", "markov", "stochastic", "scheduler"):
         from speculative_decoding_draft_depth_gb300 import ddt
         ddt.load()
         fn = {"cond_tree": time_cond_tree, "markov": time_markov,
-              "stochastic": time_stochastic}[args.stage]
+              "stochastic": time_stochastic, "scheduler": time_scheduler}[args.stage]
         res = fn(torch.device("cuda", local_rank), reps=max(args.steps, 1),
                  cpu=not args.no_cpu_baseline)
         if rank == 0:
@@ -351,7 +351,9 @@ def main():
         out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline),
                             "markov_table_tree": time_markov(dev, cpu=not args.no_cpu_baseline),
                             "stochastic_chain": time_stochastic(dev,
-                                                                cpu=not args.no_cpu_baseline)}
+                                                                cpu=not args.no_cpu_baseline),
+                            "prefix_scheduler": time_scheduler(dev,
+                                                               cpu=not args.no_cpu_baseline)}
     if not args.no_e2e:
         out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
                               steps=max(10, min(args.steps, 50)))
@@ -660,6 +662,103 @@ def time_stochastic(dev, reps=20, cpu=True):
         res["cpu_oracle_ms"] = round((time.perf_counter() - t0) * 1e3, 1)
         res["cpu_oracle_sample"] = "all 64 chains"
     return res
+
+
+def time_scheduler(dev, reps=200, cpu=True):
+    """The hardware-aware prefix scheduler ("DSpark Speculative Decoding
+    Explained ...", "Picking the budget") on two workloads:
+      toy:      128 requests x 5 guesses with the page's toy cost, 25 ms plus
+                0.1 ms per token checked (R + n tokens);
+      measured: 64 requests x 15 guesses (the batch64 chains) with a cost
+                table measured here from this library's own verification
+                (ddt_accept_stochastic on 64 chains of 1, 2, 4, 8 and 15
+                guesses, interpolated in the number of guesses).
+    Confidences come from synth.draw_confidences. Reports the device time
+    per ddt_schedule_prefix call (CUDA events over `reps` calls after 3
+    warm-up calls), the chosen budget, its tokens per ms against verifying
+    every guess, and the oracle's time for the same decision."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import ddt, synth
+
+    def td(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(dev)
+
+    def events_ms(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    # the cost table: our chain verification at a few lengths
+    cfg = synth.config("batch64")
+    R, L, V = cfg.R, cfg.L, cfg.V
+    inp = synth.draw_chain_inputs(cfg)
+    dr, tg, tok, u, r = (td(inp[k]) for k in ("draft", "target", "tokens", "u", "r"))
+    points = []
+    for Lp in (1, 2, 4, 8, 15):
+        c = ddt.make_config(R_max=R, L=Lp, V=V, B=8, K=8, Hq=4, Hkv=1, d=64, page_size=16,
+                            max_pages_per_req=1, num_pages=1)
+        cx = ddt.Context(c)
+        d_p = dr[:, :Lp].contiguous()
+        t_p = tg[:, :Lp + 1].contiguous()
+        k_p, u_p = tok[:, :Lp].contiguous(), u[:, :Lp].contiguous()
+        al = torch.empty(R, dtype=torch.int32, device=dev)
+        at = torch.empty((R, Lp + 1), dtype=torch.int32, device=dev)
+        ms = events_ms(lambda: cx.ddt_accept_stochastic(d_p, t_p, k_p, u_p, r, R, al, at), 10)
+        points.append((R * Lp, ms))
+        del cx, d_p, t_p
+    xs = np.array([p[0] for p in points], np.float64)
+    ys = np.array([p[1] for p in points], np.float64)
+    n_all = np.arange(R * L + 1, dtype=np.float64)
+    slope0 = (ys[1] - ys[0]) / (xs[1] - xs[0])
+    measured = np.where(n_all < xs[0], ys[0] - slope0 * (xs[0] - n_all), np.interp(n_all, xs, ys))
+    measured = np.maximum(measured, 1e-3).astype(np.float32)
+
+    out = {}
+    for name, Rw, Lw, cost in (
+            ("toy", 128, 5, (25.0 + 0.1 * (128 + np.arange(128 * 5 + 1))).astype(np.float32)),
+            ("measured", R, L, measured)):
+        conf = synth.draw_confidences(Rw, Lw, seed=1)
+        c = ddt.make_config(R_max=Rw, L=Lw, V=64, B=8, K=8, Hq=4, Hkv=1, d=64, page_size=16,
+                            max_pages_per_req=1, num_pages=1)
+        cx = ddt.Context(c)
+        conf_d, cost_d = td(conf), td(cost)
+        n_keep = torch.empty(Rw, dtype=torch.int32, device=dev)
+        n_tot = torch.empty(1, dtype=torch.int32, device=dev)
+        stats = torch.empty(2, dtype=torch.float64, device=dev)
+        ms = events_ms(lambda: cx.ddt_schedule_prefix(conf_d, Rw, cost_d, n_keep, n_tot, stats),
+                       reps)
+        if cx.ddt_device_status() != 0:
+            raise RuntimeError("device status flags set in the scheduler")
+        keep = n_keep.cpu().numpy()
+        st = stats.cpu().numpy()
+        surv = np.cumprod(conf.astype(np.float64), axis=1)
+        theta_all = (Rw + surv.sum()) / float(cost[-1])
+        row = {"requests": Rw, "guesses_per_request": Lw, "us_per_call": round(ms * 1e3, 2),
+               "kept": int(n_tot.cpu().numpy()[0]), "of": Rw * Lw,
+               "tokens_per_ms": round(float(st[0]), 4),
+               "tokens_per_ms_all_verified": round(theta_all, 4),
+               "expected_tokens": round(float(st[1]), 3),
+               "kept_per_request_histogram": np.bincount(keep, minlength=Lw + 1).tolist()}
+        if cpu:
+            import oracle
+            t0 = time.perf_counter()
+            for _ in range(20):
+                oracle.schedule_prefix(conf, cost)
+            row["cpu_oracle_us"] = round((time.perf_counter() - t0) / 20 * 1e6, 1)
+        out[name] = row
+    out["measured"]["cost_table_points_ms"] = [[int(x), round(y, 4)] for x, y in points]
+    out["workload"] = ("toy: 128 x 5, cost 25 ms + 0.1 ms per token checked; measured: 64 x 15 "
+                       "(batch64 chains), cost = this library's ddt_accept_stochastic time")
+    out["bound"] = "latency (one CTA; a few thousand slots)"
+    return out
 
 
 def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps, n_copy=4):

@@ -84,6 +84,10 @@ struct ddt_ctx {
     unsigned *sv_cnt;        // [2 * R_max] arrival counters of the two kernels (self-resetting)
     int4 *sv_meta;           // [R_max] (k*, log Z of target row k*, of draft row k*, 0)
     float *sv_part_w;        // [R_max, sv_nch_w] chunk totals of the draw's weights
+    // prefix scheduler (rank-counting grid)
+    uint64_t *ps_rk;         // [DDT_SCHED_MAX_SLOTS] survival bits in ranking order
+    int32_t *ps_rid;         // [DDT_SCHED_MAX_SLOTS] their tie ids
+    unsigned *ps_arrive;     // arrival counter (self-resetting)
     int att_grid;            // persistent CTAs
     bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };

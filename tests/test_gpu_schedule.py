@@ -70,7 +70,8 @@ def check(conf, cost, g_keep, g_n, g_stats):
     return "tie"
 
 
-SHAPES = [(1, 1), (3, 5), (16, 5), (128, 5), (64, 15), (100, 7), (512, 16), (2048, 4)]
+SHAPES = [(1, 1), (3, 5), (16, 5), (128, 5), (64, 15), (100, 7), (1500, 1), (1024, 3), (512, 16),
+          (2048, 4)]  # both kernels: the rank-counting grid, and the bitonic sort (2048 x 4)
 KINDS = ["toy", "flat", "steep", "convex", "random", "holes"]
 
 
