@@ -68,7 +68,7 @@ struct Layout {
     size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
         cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
-        sv_part_d, sv_part_t, sv_cnt, sv_meta, sv_part_w, ps_rk, ps_rid, ps_arrive, total;
+        sv_part_d, sv_part_t, sv_cnt, sv_part_w, ps_rk, ps_rid, ps_arrive, total;
     int tk_nch, am_nch, rowgroups, max_items, sv_nch_d, sv_nch_t, sv_nch_w;
 };
 
@@ -135,7 +135,7 @@ Layout layout_for(const ddt_config &c)
     L.mk_cand = take(mrows * C * sizeof(int32_t));
     L.mk_tab = take(mrows * C * C * sizeof(float));
     // stochastic chain verification: chunk pairs of the L draft and L + 1
-    // target rows, the draw's chunk totals, two arrival counters per request
+    // target rows, the draw's chunk totals, an arrival counter per request
     L.sv_nch_d = (c.V + stochastic_chunk_elems(c.draft_dtype) - 1) /
                  stochastic_chunk_elems(c.draft_dtype);
     L.sv_nch_t = (c.V + stochastic_chunk_elems(c.target_dtype) - 1) /
@@ -143,8 +143,7 @@ Layout layout_for(const ddt_config &c)
     L.sv_nch_w = stochastic_draw_chunks(c.V);
     L.sv_part_d = take((size_t)c.R_max * c.L * L.sv_nch_d * sizeof(float2));
     L.sv_part_t = take((size_t)c.R_max * (c.L + 1) * L.sv_nch_t * sizeof(float2));
-    L.sv_cnt = take((size_t)2 * c.R_max * sizeof(unsigned));
-    L.sv_meta = take((size_t)c.R_max * sizeof(int4));
+    L.sv_cnt = take((size_t)c.R_max * sizeof(unsigned));
     L.sv_part_w = take((size_t)c.R_max * L.sv_nch_w * sizeof(float));
     // prefix scheduler: the ranking of up to DDT_SCHED_MAX_SLOTS slots
     L.ps_rk = take((size_t)DDT_SCHED_MAX_SLOTS * sizeof(uint64_t));
@@ -318,7 +317,6 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->sv_part_d = (float2 *)(w + L.sv_part_d);
     ctx->sv_part_t = (float2 *)(w + L.sv_part_t);
     ctx->sv_cnt = (unsigned *)(w + L.sv_cnt);
-    ctx->sv_meta = (int4 *)(w + L.sv_meta);
     ctx->sv_part_w = (float *)(w + L.sv_part_w);
     ctx->ps_rk = (uint64_t *)(w + L.ps_rk);
     ctx->ps_rid = (int32_t *)(w + L.ps_rid);

@@ -81,8 +81,7 @@ struct ddt_ctx {
     int sv_nch_d, sv_nch_t, sv_nch_w;  // chunks per draft row, target row, drawn row
     float2 *sv_part_d;       // [R_max * L, sv_nch_d] (max, sum of exp)
     float2 *sv_part_t;       // [R_max * (L + 1), sv_nch_t]
-    unsigned *sv_cnt;        // [2 * R_max] arrival counters of the two kernels (self-resetting)
-    int4 *sv_meta;           // [R_max] (k*, log Z of target row k*, of draft row k*, 0)
+    unsigned *sv_cnt;        // [R_max] arrival counters of the draw (self-resetting)
     float *sv_part_w;        // [R_max, sv_nch_w] chunk totals of the draw's weights
     // prefix scheduler (rank-counting grid)
     uint64_t *ps_rk;         // [DDT_SCHED_MAX_SLOTS] survival bits in ranking order

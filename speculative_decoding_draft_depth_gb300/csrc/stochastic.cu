@@ -11,18 +11,18 @@
 // Design (HBM-bound: every logit is read once, the drawn row once more):
 //  * sv_rows_kernel: one CTA per (request, row, chunk of 32 KB); each
 //    thread keeps 8 vectors of 16 bytes in registers and the CTA reduces
-//    them to the chunk's (max, sum of exp). CTAs run request by request; the
-//    last CTA of a request to finish (an arrival counter) merges its rows'
-//    pairs into log-partitions (a warp per row), reads the 2L logits of the
-//    guesses, runs the L decisions in one warp (a ballot finds the first
-//    rejection k*) and writes the accepted prefix, the length and (k*, the
-//    two log-partitions of row k*) for the draw.
-//  * sv_draw_kernel (a dependent launch): one CTA per (request, chunk of
-//    8192 weights) sums the draw's weights of its chunk; the last CTA of a
-//    request adds the chunk totals in index order, finds the chunk that holds
-//    r * total, re-reads that chunk in index order (32 consecutive weights per
-//    thread, a block scan) and picks the first index whose running sum
-//    exceeds it.
+//    them to the chunk's (max, sum of exp), stores the pair and exits.
+//  * sv_draw_kernel (a dependent launch): one CTA per (request, 8192 tokens
+//    of the drawn row). Every CTA of a request first takes the request's
+//    decisions itself -- the log-partitions of its 2L + 1 rows from the
+//    pairs (a warp per row), the guesses' log-probs, the L decisions in one
+//    warp (a ballot finds the first rejection k*) -- the same loads in the
+//    same order, so all agree; the request's first CTA writes the committed
+//    prefix and the length. Then each sums the draw's weights of its chunk
+//    of row k*; the last CTA of the request (an arrival counter) adds the
+//    chunk totals in index order, finds the chunk that holds r * total,
+//    re-reads that chunk in index order (32 consecutive weights per thread,
+//    a block scan) and picks the first index whose running sum exceeds it.
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -37,6 +37,7 @@ constexpr int SV_THREADS = 256;
 constexpr int SV_NV = 8;                   // 16-byte vectors per thread in the row pass
 constexpr int SV_WPT = 32;                 // weights per thread in the draw
 constexpr int SV_WCH = SV_THREADS * SV_WPT;  // weights per CTA of the draw (8192)
+constexpr int SV_DEC_PAIRS = 1024;           // chunk pairs a request's decision stages in smem
 
 // ---------------------------------------------------------------- row pass
 // (max, sum of exp(x - max)) of one chunk of a row, for the whole CTA; the
@@ -122,20 +123,15 @@ DDT_DEVINL float logit_at(const T *row, int x)
 struct RowsArgs {
     const void *draft;        // [R, L, V] draft logits
     const void *target;       // [R, L + 1, V] target logits
-    const int32_t *tokens;    // [R, L] the guesses
-    const float *u;           // [R, L] acceptance uniforms
     float2 *part_d, *part_t;  // chunk (max, sum) pairs of the draft / target rows
-    unsigned *cnt;            // [R] arrivals (self-resetting)
-    int4 *meta;               // [R] (k*, log Z_t of row k*, log Z_d of row k*, 0)
-    int32_t *acc_len;         // [R]
-    int32_t *acc_tokens;      // [R, L + 1]
     int32_t *status;
     int L, V, nch_d, nch_t;
     bool al_d, al_t;          // 16-byte aligned rows
 };
 
-// grid: R * (L * nch_d + (L + 1) * nch_t) CTAs, request-major, so requests
-// finish (and decide) one after another while the rest stream in
+// grid: R * (L * nch_d + (L + 1) * nch_t) CTAs, request-major; each stores
+// its chunk's (max, sum) pair and exits (the decisions are taken by the
+// draw kernel, which waits for this whole grid)
 template <typename TD, typename TT>
 __global__ void __launch_bounds__(SV_THREADS)
 sv_rows_kernel(RowsArgs a)
@@ -143,10 +139,7 @@ sv_rows_kernel(RowsArgs a)
     const int L = a.L, V = a.V;
     const int per = L * a.nch_d + (L + 1) * a.nch_t;
     const int i = blockIdx.x / per, j = blockIdx.x % per;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
-    __shared__ float s_lse[2 * DDT_MAX_L + 1], s_lz[2 * DDT_MAX_L + 1];
-    __shared__ int s_last;
     pdl_trigger();
 
     float M = 0.f, S = 0.f;
@@ -171,53 +164,102 @@ sv_rows_kernel(RowsArgs a)
             chunk_ms<TT, false>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
         slot = a.part_t + (int64_t)row * a.nch_t + c;
     }
-    if (tid == 0) {
+    if (threadIdx.x == 0) {
         if (M != M || S != S)
             set_status(a.status, DDT_DEV_NAN_LOGITS);
         *slot = make_float2(M, S);
-        __threadfence();
-        const unsigned prev = atomicAdd(&a.cnt[i], 1u);
-        s_last = (prev == (unsigned)per - 1u);
-        if (s_last)
-            a.cnt[i] = 0u;  // every arrival of this call is in: ready for the next
     }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
+}
 
-    // ---- the request's last CTA: log-partitions of its 2L + 1 rows (draft
-    // rows 0..L-1, then target rows 0..L) and the guesses' log-probs
+// ---------------------------------------------------------------- the draw
+struct DrawArgs {
+    const void *draft, *target;
+    const int32_t *tokens;          // [R, L] the guesses
+    const float *u;                 // [R, L] acceptance uniforms
+    const float *r;                 // [R] draw uniforms
+    const float2 *part_d, *part_t;  // from sv_rows_kernel
+    float *part_w;                  // [R, nchw] chunk totals of the weights
+    unsigned *cnt;                  // [R] arrivals (self-resetting)
+    int32_t *acc_len;               // [R]
+    int32_t *acc_tokens;            // [R, L + 1]
+    int32_t *status;
+    int L, V, nchw, nch_d, nch_t;
+    bool al_d, al_t;  // (host side: selects the kernel)
+};
+
+// Request i's decisions, taken by every CTA of the draw that works on it (the
+// same loads in the same order, so each gets the same answer): the
+// log-partitions of its 2L + 1 rows from the chunk pairs (a warp per row,
+// lanes over chunks), the guesses' log-probs, then the L decisions in warp 0
+// (kept iff u < min(1, p/q); a ballot finds the first rejection k*). The CTA
+// with `writer` set also stores the length and every committed token but the
+// drawn one. Returns k*; s_lse[t] holds the log-partition of row t (draft rows
+// 0..L-1, then target rows 0..L).
+template <typename TD, typename TT>
+__device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float *s_lse,
+                                   float *s_lz, int *s_ks, float2 *s_pairs)
+{
+    const int L = a.L, V = a.V;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const TD *zd = static_cast<const TD *>(a.draft) + (int64_t)i * L * V;
     const TT *zt = static_cast<const TT *>(a.target) + (int64_t)i * (L + 1) * V;
-    for (int t = warp; t < 2 * L + 1; t += SV_THREADS / 32) {
-        const bool isd = t < L;
-        const int k = isd ? t : t - L;
-        const int nch = isd ? a.nch_d : a.nch_t;
-        const float2 *part = isd ? a.part_d + ((int64_t)i * L + k) * nch
-                                 : a.part_t + ((int64_t)i * (L + 1) + k) * nch;
-        float m = DDT_NEG_INF, s = 0.f;
-        for (int c = lane; c < nch; c += 32) {
-            const float2 p = __ldcg(part + c);
-            ms_combine(m, s, p.x, p.y);
+    const int nd = L * a.nch_d, nt = (L + 1) * a.nch_t;
+    if (nd + nt <= SV_DEC_PAIRS) {
+        // every pair of the request and the 2L guess logits at once (one round
+        // trip), then a thread per row merges its pairs from shared memory
+        const float2 *pd = a.part_d + (int64_t)i * nd, *pt = a.part_t + (int64_t)i * nt;
+        for (int q = tid; q < nd + nt; q += SV_THREADS)
+            s_pairs[q] = q < nd ? __ldcg(pd + q) : __ldcg(pt + (q - nd));
+        for (int q = tid; q < 2 * L; q += SV_THREADS) {
+            const int k = q < L ? q : q - L;
+            const int x = a.tokens[(int64_t)i * L + k];
+            float zx = 0.f;
+            if (x >= 0 && x < V)
+                zx = q < L ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x);
+            s_lz[q] = zx;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
-            const float so = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            ms_combine(m, s, mo, so);
-        }
-        if (lane == 0) {
-            const float lse = m + logf(s);
+        __syncthreads();
+        if (tid < 2 * L + 1) {
+            const int t = tid;
+            const float2 *pp = t < L ? s_pairs + t * a.nch_d : s_pairs + nd + (t - L) * a.nch_t;
+            const int nch = t < L ? a.nch_d : a.nch_t;
+            float m = DDT_NEG_INF, sm = 0.f;
+            for (int c = 0; c < nch; ++c)
+                ms_combine(m, sm, pp[c].x, pp[c].y);
+            const float lse = m + logf(sm);
             s_lse[t] = lse;
-            float lz = 0.f;
-            if (k < L) {
+            if (t < 2 * L)
+                s_lz[t] -= lse;
+        }
+    } else {
+        for (int t = warp; t < 2 * L + 1; t += SV_THREADS / 32) {
+            const bool isd = t < L;
+            const int k = isd ? t : t - L;
+            const int nch = isd ? a.nch_d : a.nch_t;
+            const float2 *part = isd ? a.part_d + ((int64_t)i * L + k) * nch
+                                     : a.part_t + ((int64_t)i * (L + 1) + k) * nch;
+            float zx = 0.f;  // the guess's logit, loaded beside the pairs
+            if (lane == 0 && k < L) {
                 const int x = a.tokens[(int64_t)i * L + k];
                 if (x >= 0 && x < V)
-                    lz = (isd ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x)) -
-                         lse;
+                    zx = isd ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x);
             }
-            s_lz[t] = lz;
+            float m = DDT_NEG_INF, sm = 0.f;
+            for (int c = lane; c < nch; c += 32) {
+                const float2 p = __ldcg(part + c);
+                ms_combine(m, sm, p.x, p.y);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float mo = __shfl_xor_sync(0xFFFFFFFFu, m, o);
+                const float so = __shfl_xor_sync(0xFFFFFFFFu, sm, o);
+                ms_combine(m, sm, mo, so);
+            }
+            if (lane == 0) {
+                const float lse = m + logf(sm);
+                s_lse[t] = lse;
+                s_lz[t] = zx - lse;
+            }
         }
     }
     __syncthreads();
@@ -226,7 +268,7 @@ sv_rows_kernel(RowsArgs a)
         if (lane < L) {
             const int x = a.tokens[(int64_t)i * L + lane];
             const bool ok = x >= 0 && x < V;
-            if (!ok)
+            if (!ok && writer)
                 set_status(a.status, DDT_DEV_BAD_TREE);
             // min(1, p/q) from the two log-probs; q = 0 gives +inf (or NaN
             // when p = 0 too), which fminf takes to 1
@@ -235,29 +277,20 @@ sv_rows_kernel(RowsArgs a)
         }
         const unsigned kept = __ballot_sync(0xFFFFFFFFu, keep);
         const int ks = __ffs(~kept) - 1;  // lanes >= L never keep: ks <= L
-        if (lane == 0) {
-            a.meta[i] = make_int4(ks, __float_as_int(s_lse[L + ks]),
-                                  __float_as_int(ks < L ? s_lse[ks] : 0.f), 0);
-            a.acc_len[i] = ks + 1;
+        if (lane == 0)
+            *s_ks = ks;
+        if (writer) {
+            if (lane == 0)
+                a.acc_len[i] = ks + 1;
+            for (int t = lane; t <= L; t += 32)
+                if (t != ks)
+                    a.acc_tokens[(int64_t)i * (L + 1) + t] =
+                        t < ks ? a.tokens[(int64_t)i * L + t] : -1;
         }
-        for (int t = lane; t <= L; t += 32)
-            if (t != ks)
-                a.acc_tokens[(int64_t)i * (L + 1) + t] =
-                    t < ks ? a.tokens[(int64_t)i * L + t] : -1;
     }
+    __syncthreads();
+    return *s_ks;
 }
-
-// ---------------------------------------------------------------- the draw
-struct DrawArgs {
-    const void *draft, *target;
-    const float *r;        // [R] draw uniforms
-    const int4 *meta;      // [R] from sv_rows_kernel
-    float *part_w;         // [R, nchw] chunk totals of the weights
-    unsigned *cnt;         // [R] arrivals (self-resetting)
-    int32_t *acc_tokens;   // [R, L + 1]
-    int L, V, nchw;
-    bool al_d, al_t;  // (host side: selects the kernel)
-};
 
 // one group of 8 consecutive logits (v0 a multiple of 8) as raw 16-byte
 // vectors: one for bf16, two for fp32; -inf past V
@@ -297,32 +330,36 @@ DDT_DEVINL float draw_weight(float zt, float zd, float bt, float bd, bool leftov
 }
 
 constexpr int SV_G = SV_WPT / 8;  // groups of 8 weights per thread
+constexpr int SV_GH = 4;          // groups loaded at once (registers)
 
-// sum of the draw's weights of tokens v0 .. v0 + 31 (in index order)
+// sum of the draw's weights of tokens v0 .. v0 + SV_WPT - 1 (in index order)
 template <typename TD, typename TT, bool AD, bool AT>
 DDT_DEVINL float thread_sum(const TT *zt, const TD *zd, int v0, int V, float bt, float bd,
                             bool leftover)
 {
-    Grp<TT> gt[SV_G];
-    Grp<TD> gd[SV_G];
-#pragma unroll
-    for (int g = 0; g < SV_G; ++g)
-        ld_group<TT, AT>(zt, v0 + g * 8, V, gt[g]);
-    if (leftover) {
-#pragma unroll
-        for (int g = 0; g < SV_G; ++g)
-            ld_group<TD, AD>(zd, v0 + g * 8, V, gd[g]);
-    }
     float s = 0.f;
 #pragma unroll
-    for (int g = 0; g < SV_G; ++g)
+    for (int h = 0; h < SV_G; h += SV_GH) {
+        Grp<TT> gt[SV_GH];
+        Grp<TD> gd[SV_GH];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            s += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
+        for (int g = 0; g < SV_GH; ++g)
+            ld_group<TT, AT>(zt, v0 + (h + g) * 8, V, gt[g]);
+        if (leftover) {
+#pragma unroll
+            for (int g = 0; g < SV_GH; ++g)
+                ld_group<TD, AD>(zd, v0 + (h + g) * 8, V, gd[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < SV_GH; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                s += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
+    }
     return s;
 }
 
-// tokens v0 .. v0 + 31 with running sum `cum` before them: the first positive
+// tokens v0 .. v0 + SV_WPT - 1 with running sum `cum` before them: the first positive
 // weight whose running sum exceeds x, else (x = +inf) the last positive one
 template <typename TD, typename TT, bool AD, bool AT>
 __device__ __noinline__ int fine_search(const TT *zt, const TD *zd, int v0, int V, float bt,
@@ -355,35 +392,39 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
     const int L = a.L, V = a.V;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ float s_w[SV_THREADS / 32];
-    __shared__ int s_last, s_chunk, s_pick;
+    __shared__ int s_last, s_chunk, s_pick, s_ks;
     __shared__ float s_x;
+    __shared__ float s_lse[2 * DDT_MAX_L + 1], s_lz[2 * DDT_MAX_L + 1];
+    __shared__ float2 s_pairs[SV_DEC_PAIRS];
 
-    const int4 mt = __ldcg(a.meta + i);
-    const int ks = mt.x;
+    const int ks = decide<TD, TT>(a, i, c == 0, s_lse, s_lz, &s_ks, s_pairs);
     const bool leftover = ks < L;
-    const float bt = -__int_as_float(mt.y) * DDT_LOG2E;
-    const float bd = -__int_as_float(mt.z) * DDT_LOG2E;
+    const float bt = -s_lse[L + ks] * DDT_LOG2E;
+    const float bd = leftover ? -s_lse[ks] * DDT_LOG2E : 0.f;
     const TT *zt = static_cast<const TT *>(a.target) + ((int64_t)i * (L + 1) + ks) * V;
     const TD *zd = static_cast<const TD *>(a.draft) + ((int64_t)i * L + (leftover ? ks : 0)) * V;
 
-    // ---- this chunk's total: every load issued before any arithmetic;
-    // groups of 8 tokens interleaved across threads (coalesced)
-    Grp<TT> gt[SV_G];
-    Grp<TD> gd[SV_G];
-#pragma unroll
-    for (int g = 0; g < SV_G; ++g)
-        ld_group<TT, AT>(zt, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, gt[g]);
-    if (leftover) {
-#pragma unroll
-        for (int g = 0; g < SV_G; ++g)
-            ld_group<TD, AD>(zd, c * SV_WCH + (g * SV_THREADS + tid) * 8, V, gd[g]);
-    }
+    // ---- this chunk's total: the loads of SV_GH groups issued before their
+    // arithmetic; groups of 8 tokens interleaved across threads (coalesced)
     float t = 0.f;
 #pragma unroll
-    for (int g = 0; g < SV_G; ++g)
+    for (int h = 0; h < SV_G; h += SV_GH) {
+        Grp<TT> gt[SV_GH];
+        Grp<TD> gd[SV_GH];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            t += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
+        for (int g = 0; g < SV_GH; ++g)
+            ld_group<TT, AT>(zt, c * SV_WCH + ((h + g) * SV_THREADS + tid) * 8, V, gt[g]);
+        if (leftover) {
+#pragma unroll
+            for (int g = 0; g < SV_GH; ++g)
+                ld_group<TD, AD>(zd, c * SV_WCH + ((h + g) * SV_THREADS + tid) * 8, V, gd[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < SV_GH; ++g)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                t += draw_weight(gt[g].at(e), leftover ? gd[g].at(e) : 0.f, bt, bd, leftover);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
@@ -460,9 +501,9 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
     const int ch = s_chunk;
     int tok = -1;
     if (ch >= 0) {
-        // 32 consecutive weights per thread (index order): each thread's sum,
+        // SV_WPT consecutive weights per thread (index order): each thread's sum,
         // an exclusive scan over threads, then the first thread whose range
-        // reaches x re-reads its 32 tokens and finds the crossing one
+        // reaches x re-reads its SV_WPT tokens and finds the crossing one
         const float xin = s_x;
         const int v0 = ch * SV_WCH + tid * SV_WPT;
         const float st = thread_sum<TD, TT, AD, AT>(zt, zd, v0, V, bt, bd, leftover);
@@ -511,7 +552,7 @@ template <typename TD, typename TT, bool AL>
 __global__ void __launch_bounds__(SV_THREADS, sizeof(TD) + sizeof(TT) == 8 ? 3 : 4)
 sv_draw_kernel(DrawArgs a)
 {
-    pdl_wait();  // k* and the log-partitions come from sv_rows_kernel
+    pdl_wait();  // the chunk pairs come from sv_rows_kernel
     draw_body<TD, TT, AL, AL>(a, blockIdx.y, blockIdx.x);
 }
 
@@ -537,14 +578,8 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     RowsArgs ra;
     ra.draft = draft;
     ra.target = target;
-    ra.tokens = tokens;
-    ra.u = u;
     ra.part_d = c->sv_part_d;
     ra.part_t = c->sv_part_t;
-    ra.cnt = c->sv_cnt;
-    ra.meta = c->sv_meta;
-    ra.acc_len = acc_len;
-    ra.acc_tokens = acc_tokens;
     ra.status = c->status;
     ra.L = L;
     ra.V = V;
@@ -571,14 +606,21 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     DrawArgs da;
     da.draft = draft;
     da.target = target;
+    da.tokens = tokens;
+    da.u = u;
     da.r = r;
-    da.meta = c->sv_meta;
+    da.part_d = c->sv_part_d;
+    da.part_t = c->sv_part_t;
     da.part_w = c->sv_part_w;
-    da.cnt = c->sv_cnt + c->cfg.R_max;
+    da.cnt = c->sv_cnt;
+    da.acc_len = acc_len;
     da.acc_tokens = acc_tokens;
+    da.status = c->status;
     da.L = L;
     da.V = V;
     da.nchw = c->sv_nch_w;
+    da.nch_d = c->sv_nch_d;
+    da.nch_t = c->sv_nch_t;
     da.al_d = ra.al_d;
     da.al_t = ra.al_t;
     cudaLaunchAttribute attr[1];
