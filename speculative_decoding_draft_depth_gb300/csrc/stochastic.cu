@@ -133,7 +133,7 @@ struct RowsArgs {
 // its chunk's (max, sum) pair and exits (the decisions are taken by the
 // draw kernel, which waits for this whole grid)
 template <typename TD, typename TT>
-__global__ void __launch_bounds__(SV_THREADS)
+__global__ void __launch_bounds__(SV_THREADS, 5)  // 48 registers: five CTAs per SM
 sv_rows_kernel(RowsArgs a)
 {
     const int L = a.L, V = a.V;
