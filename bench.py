@@ -46,6 +46,30 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+# ---------------------------------------------------------------- replicas
+def rank_seed(base, rank):
+    """Each rank's replica draws its own inputs: the workload's seed plus the
+    rank."""
+    return base + rank
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's time; every rank gets it (a single process keeps
+    its own)."""
+    if not dist:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, steps, ms):
+    """Units per second of the whole job: every rank ran `steps` units in the
+    slowest rank's `ms`."""
+    return world * steps / (ms / 1e3)
+
+
 def _workload_desc(cfg):
     return ("%s: R=%d,L=%d,V=%d,B=%d,K=%d,P=%d,Hq=%d,Hkv=%d,d=%d,page=%d,ctx~U[%d,%d],bf16"
             % (cfg.name, cfg.R, cfg.L, cfg.V, cfg.B, cfg.K, cfg.P, cfg.Hq, cfg.Hkv, cfg.d, cfg.page,
@@ -203,7 +227,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     from speculative_decoding_draft_depth_gb300 import synth
-    cfg = synth.config(WORKLOAD, seed=synth.config(WORKLOAD).seed + rank)
+    cfg = synth.config(WORKLOAD, seed=rank_seed(synth.config(WORKLOAD).seed, rank))
     if args.requests:
         cfg = synth.config(WORKLOAD, R=args.requests, seed=cfg.seed)
 
@@ -305,13 +329,9 @@ def main():
     if dist:
         dist.barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     ms_per_step = ms_total / args.steps
-    value = world * args.steps / (ms_total / 1e3)
+    value = job_throughput(world, args.steps, ms_total)
 
     # ---------------- per-stage durations (same stream, CUDA events)
     stage_ms = time_stages(ctx, cfg, bufs, d, ctx0, stream, reps=max(20, args.steps // 10))
@@ -825,13 +845,9 @@ def time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist, steps, n_co
         step(i, first)
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(a.elapsed_time(b), dist, dev)
     d["ctx_lens"].copy_(ctx0)
-    return {"value": round(world * steps / (ms / 1e3), 2), "unit": UNIT,
+    return {"value": round(job_throughput(world, steps, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "copy_streams": n_copy}
 
