@@ -72,7 +72,7 @@ struct ddt_ctx {
     double *cg_c_S;          // [R_max, Cmax] candidate scores
     int32_t *cg_c_meta;      // [R_max, Cmax, 3] depth, parent candidate, token
     uint32_t *cg_thr;        // [L, CG_NP_MAX] per-parent lower bounds of the k-th child (value keys)
-    float *cg_seed_lp;       // [R_max, L, K] log-probs of the draft's own top-K (unused)
+    float *cg_seed_lp;       // [R_max, L, K] the seeds' log-probs (written by top-K, not read)
     int32_t *cg_seed_ids;    // [R_max, L, K] the draft's top-K columns per depth: bound seeds
     // SparklingTree table tree (prefilter > 0)
     int32_t *mk_cand;        // [R_max, L, C] kept tokens (ddt_round_markov)

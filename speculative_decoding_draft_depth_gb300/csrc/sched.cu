@@ -13,19 +13,19 @@
 // kept). Survival cannot rise along a block, so the kept slots are a prefix
 // of every request's block.
 //
-// Up to 8192 slots. Two kernels, by size (GB300's fp64 pipe is narrow, so
-// fp64 does only the products and the sums):
-//  * up to 2^23 slot-request pairs, a grid counts every slot's rank by
-//    binary searches (ps_rank_kernel, below);
-//  * beyond that, one CTA of 1024 threads sorts:
+// Up to 8192 slots. GB300's fp64 pipe is narrow, so fp64 does only the
+// products, the running sums and the budget comparisons. The steps:
 //  * survivals as fp64 products in position order (the same products, bit
 //    for bit, as a sequential reference);
-//  * a bitonic sort of (survival bits as an integer, position * R + request)
-//    pairs, in registers, shuffles and shared memory by stride;
-//  * expected tokens for every n: each thread sums a contiguous run of the
-//    ranked survivals and a block scan gives the runs' offsets; budgets are
-//    compared by cross-multiplying tokens and costs, and a block reduction
-//    finds the best n;
+//  * the ranking, one of two ways by size: up to 2^23 slot-request pairs, a
+//    grid counts every slot's rank by binary searches (ps_rank_kernel);
+//    beyond that, one CTA of 1024 threads runs a bitonic sort of (survival
+//    bits as an integer, position * R + request) pairs, in registers,
+//    shuffles and shared memory by stride (ps_schedule_kernel);
+//  * expected tokens for every n: each of 256 threads sums a contiguous run
+//    of the ranked survivals and a block scan gives the runs' offsets;
+//    budgets are compared by cross-multiplying tokens and costs, and a
+//    reduction finds the best n;
 //  * kept slots counted per request with shared-memory atomics.
 #include <cuda_runtime.h>
 #include <stdint.h>
