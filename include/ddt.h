@@ -13,6 +13,19 @@
  * and ddt_round chains a1..a7 (ddt_accept chains a5..a7) on one stream
  * with no host synchronisation.
  *
+ * Further entry points (declared after the round's):
+ *   ddt_build_tree_conditioned / ddt_round_conditioned
+ *       TreeSpark's parent-conditioned tree (Markov bias per parent,
+ *       per-parent top-k, frontier pruning, top-N packing), and its round
+ *   ddt_markov_table / ddt_build_tree_markov / ddt_round_markov
+ *       SparklingTree's top-C prefilter, Markov table and the heap over it
+ *   ddt_accept_stochastic
+ *       stochastic verification of drafted chains at temperature 1
+ *   ddt_schedule_prefix
+ *       the hardware-aware prefix scheduler (guesses to verify per request)
+ *   ddt_topk_logprobs_noalloc
+ *       a1 without a context
+ *
  * Pages the operations follow (title and section):
  *   "SparklingTree: 30-40% faster speculative decoding over DSpark",
  *       "How is the tree actually created?", Steps 1-4.
@@ -20,7 +33,14 @@
  *       for Speculative Decoding", sections 3 (Prop. 1, Prop. 2, Lemma 1),
  *       4 (Algorithm 1) and 5 (implementation highlights).
  *   "Robot2050/TreeSpark", item 4 and the continuous-batching engine
- *       (device-side masks, vectorised acceptance, ragged-batch KV).
+ *       (device-side masks, vectorised acceptance, ragged-batch KV); items
+ *       1 and 2 for the parent-conditioned tree.
+ *   "SparklingTree ...", "First order markov model conditioning",
+ *       "Building SparklingTree" and "Solving the candidate tree
+ *       construction" for the table tree.
+ *   "DSpark Speculative Decoding Explained: Block Drafting and Confidence
+ *       Checks", the probability rule (stochastic verification), "Survival
+ *       probability" and "Picking the budget" (the scheduler).
  *
  * Conventions shared by every call
  *   - Pointers are DEVICE pointers unless stated. The caller owns every
