@@ -71,9 +71,15 @@ def job_throughput(world, steps, ms):
 
 
 def _workload_desc(cfg):
-    return ("%s: R=%d,L=%d,V=%d,B=%d,K=%d,P=%d,Hq=%d,Hkv=%d,d=%d,page=%d,ctx~U[%d,%d],bf16"
+    if cfg.ctx_kind == "uniform":
+        ctx = "ctx~U[%d,%d]" % cfg.ctx_args[:2]
+    elif cfg.ctx_kind == "fixed":
+        ctx = "ctx=%d" % cfg.ctx_args[0]
+    else:
+        ctx = "ctx~%s%s" % (cfg.ctx_kind, tuple(cfg.ctx_args))
+    return ("%s: R=%d,L=%d,V=%d,B=%d,K=%d,P=%d,Hq=%d,Hkv=%d,d=%d,page=%d,%s,%s"
             % (cfg.name, cfg.R, cfg.L, cfg.V, cfg.B, cfg.K, cfg.P, cfg.Hq, cfg.Hkv, cfg.d, cfg.page,
-               cfg.ctx_args[0], cfg.ctx_args[1]))
+               ctx, cfg.logit_dtype))
 
 
 def round_bytes(cfg, ctx_lens, acc_len=None):
