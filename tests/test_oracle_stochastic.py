@@ -10,7 +10,10 @@ guess by a draw from max(0, p - q), a bonus draw from p when all survive).
     the target within Monte-Carlo error;
   * with a constant acceptance rate a and g guesses, the mean tokens per
     pass is the page's (1 - a^(g+1)) / (1 - a);
-  * the logits form equals the probability form after a softmax.
+  * the logits form equals the probability form after a softmax, also for
+    logits far from zero;
+  * the rule's edges: p(x) = 0 is never kept, a zero weight is never drawn,
+    q(x) = 0 counts as ratio 1.
 """
 import os
 import random
@@ -171,3 +174,46 @@ def test_logits_form_matches_probabilities():
         [draft, draft[:, :1]], 1), tokens, np.full((R, L), 0.999999), r)
     assert (acc_len == L + 1).all()
     assert (acc_tokens[:, :L] == tokens).all()
+
+
+def test_boundaries_the_rule_fixes():
+    """Cases the rule decides at its edges: a guess the target gives
+    probability 0 is kept with probability 0 (so never, even at u = 0); a
+    token whose weight is 0 is never drawn (even at r = 0); a guess the draft
+    gives probability 0 counts as ratio 1 (the stated reading: such a guess
+    cannot come from the draft, and the rule would divide by zero)."""
+    p = np.array([[0.0, 0.5, 0.5], [0.2, 0.3, 0.5]])
+    q = np.array([[0.5, 0.25, 0.25]])
+    # p(x) = 0: rejected at u = 0; the leftover max(0, p - q) = (0, .25, .25)
+    # gives token 0 no weight, so r = 0 draws token 1
+    assert oracle.verify_chain(p, q, [0], [0.0], 0.0) == [1]
+    # q(x) = 0 with p(x) > 0: kept whatever u, then the bonus from p's last row
+    q0 = np.array([[0.0, 0.5, 0.5]])
+    p0 = np.array([[0.4, 0.3, 0.3], [0.2, 0.3, 0.5]])
+    assert oracle.verify_chain(p0, q0, [0], [0.999], 0.0) == [0, 0]
+    # bonus at r = 0 skips a zero-weight first token
+    pz = np.array([[0.5, 0.5, 0.0], [0.0, 0.4, 0.6]])
+    qz = np.array([[0.5, 0.5, 0.0]])
+    assert oracle.verify_chain(pz, qz, [1], [0.0], 0.0) == [1, 1]
+
+
+def test_large_logits():
+    """Logits far from zero (+900 on the draft, -900 on the target: a softmax
+    must shift by the row max, or exp overflows or underflows) give the same
+    answers as the probability form of the same logits."""
+    rng = np.random.default_rng(5)
+    R, L, V = 2, 3, 40
+    dfar = ((rng.standard_normal((R, L, V)) * 2) + 900.0).astype(np.float32)
+    tfar = ((rng.standard_normal((R, L + 1, V)) * 2) - 900.0).astype(np.float32)
+    tokens = rng.integers(0, V, size=(R, L)).astype(np.int32)
+    u, r = rng.random((R, L)), rng.random(R)
+    acc_len, acc_tokens = oracle.accept_stochastic(dfar, tfar, tokens, u, r)
+
+    def sm(z):
+        z = z.astype(np.float64)
+        e = np.exp(z - z.max(-1, keepdims=True))
+        return e / e.sum(-1, keepdims=True)
+
+    for i in range(R):
+        want = oracle.verify_chain(sm(tfar[i]), sm(dfar[i]), tokens[i], u[i], r[i])
+        assert acc_len[i] == len(want) and list(acc_tokens[i, :acc_len[i]]) == want
