@@ -133,3 +133,41 @@ def test_parent_lists_match_the_tree_lists():
     lp, ids = oracle.cond_parent_lists(ell, W, E, req, dep, tok, 4)
     np.testing.assert_array_equal(ids, np.array(want_ids))
     np.testing.assert_array_equal(lp, np.array(want_lp))
+
+
+def test_tied_logits_list_the_lower_token_first():
+    """Equal logits (integers, many ties) with no bias: each parent's list is
+    numpy's stable descending order, lower token id first among equals."""
+    rng = np.random.default_rng(11)
+    R, D, V, H, k = 2, 2, 24, 4, 6
+    ell = rng.integers(-2, 3, size=(R, D, V)).astype(np.float32)
+    W = np.zeros((V, H), np.float32)
+    E = rng.standard_normal((V, H)).astype(np.float32)
+    anchors = rng.integers(0, V, size=R).astype(np.int32)
+    t = oracle.cond_tree(ell, W, E, anchors, k=k, F=2, N=8)
+    for r in range(R):
+        z = ell[r, 0].astype(np.float64)
+        np.testing.assert_array_equal(t.cand_ids[r, 0, 0], np.argsort(-z, kind="stable")[:k])
+
+
+def test_score_ties_pack_the_parent_first():
+    """A depth whose only likely token has log-prob 0 (the others 1000 below:
+    exp underflows, log-partition exactly the max) gives each child the same
+    score as its parent. Packing by (score desc, depth asc) keeps the tree
+    prefix-closed: every node's parent comes before it."""
+    R, D, V, H, k, N = 2, 3, 12, 4, 3, 10
+    rng = np.random.default_rng(12)
+    ell = (rng.standard_normal((R, D, V)) * 2).astype(np.float32)
+    ell[:, 1, :] = -1000.0
+    ell[:, 1, 5] = 0.0  # depth 2 is certain: token 5 with log-prob 0
+    W = np.zeros((V, H), np.float32)
+    E = rng.standard_normal((V, H)).astype(np.float32)
+    anchors = rng.integers(0, V, size=R).astype(np.int32)
+    t = oracle.cond_tree(ell, W, E, anchors, k=k, F=k, N=N)
+    for r in range(R):
+        n = int(t.n_nodes[r])
+        for i in range(1, n + 1):
+            p = int(t.parents[r, i])
+            assert 0 <= p < i, (r, i, p)
+            if t.depths[r, i] == 2:  # the certain child ties with its parent
+                assert t.S[r, i] == t.S[r, p]
