@@ -33,13 +33,23 @@ CASES = {
     "ragged_v": dict(name="treespark", R=3, L=4, V=3001, B=16, K=3, frontier=3, seed=25),
     # more requests than l stages hold, and seed rows that do not fit
     "many_requests": dict(name="treespark", R=60, L=3, V=4096, B=10, K=2, frontier=2, seed=26),
+    # depth 2 is certain (one token at 0, the rest 60 below: their exp is
+    # below one ulp of 1 in fp32 and fp64, so its log-prob is exactly 0):
+    # each child's score ties with its parent's, and packing must keep
+    # parents first
+    "certain_depth": dict(name="treespark", R=3, L=4, V=2000, B=16, K=3, frontier=3, seed=27,
+                          certain_depth=1),
 }
 
 
 class CondCase:
-    def __init__(self, cfg, head_scale=0.02):
+    def __init__(self, cfg, head_scale=0.02, certain_depth=None):
         self.cfg = cfg
         self.inp = inp = synth.draw_round_inputs(cfg)
+        if certain_depth is not None:
+            z = inp["draft_logits"]  # bf16 bits
+            z[:, certain_depth, :] = synth.to_bf16_bits(np.array([-60.0], np.float32))[0]
+            z[:, certain_depth, 5] = 0
         self.W, self.E, self.anchors = synth.draw_markov_head(cfg, scale=head_scale)
         ctx = self.ctx = make_ctx(cfg, inp)
         R, L, F, K, N = cfg.R, cfg.L, cfg.frontier, cfg.K, cfg.B
@@ -64,7 +74,8 @@ class CondCase:
 def case(request):
     kw = dict(CASES[request.param])
     scale = kw.pop("head_scale", 0.02)
-    return CondCase(synth.config(kw.pop("name"), **kw), head_scale=scale)
+    certain = kw.pop("certain_depth", None)
+    return CondCase(synth.config(kw.pop("name"), **kw), head_scale=scale, certain_depth=certain)
 
 
 def test_status_clean(case):
