@@ -81,7 +81,7 @@ def lib():
         L.orc_markov_tree_bruteforce.restype = i64
         L.orc_verify_chain.argtypes = [p, p, p, p, ctypes.c_double, i32, i64, p]
         L.orc_verify_chain.restype = i32
-        L.orc_accept_stochastic.argtypes = [p, p, i32, p, p, p, i32, i32, i64, p, p]
+        L.orc_accept_stochastic.argtypes = [p, p, i32, p, p, p, i32, i32, i64, p, p, p]
         L.orc_accept_stochastic.restype = i32
         L.orc_schedule_prefix.argtypes = [p, i32, i32, p, p, p, p]
         L.orc_schedule_prefix.restype = i32
@@ -443,20 +443,25 @@ def verify_chain(p, q, tokens, u, r):
     return [int(t) for t in out[:n]]
 
 
-def accept_stochastic(draft, target, tokens, u, r):
+def accept_stochastic(draft, target, tokens, u, r, n_guess=None):
     """The same rule on logits at temperature 1 for R requests: draft
     [R, L, V], target [R, L+1, V] (same dtype), tokens [R, L], u [R, L],
-    r [R]. Returns acc_len [R] and acc_tokens [R, L+1] (-1 padded)."""
+    r [R]. n_guess [R] (optional): request i verifies only its first
+    n_guess[i] guesses. Returns acc_len [R] and acc_tokens [R, L+1] (-1
+    padded)."""
     draft = np.ascontiguousarray(draft)
     target = np.ascontiguousarray(target)
     R, L, V = draft.shape
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     u = np.ascontiguousarray(u, dtype=np.float64)
     r = np.ascontiguousarray(r, dtype=np.float64)
+    ng = None if n_guess is None else np.ascontiguousarray(n_guess, dtype=np.int32)
     acc_len = np.empty(R, np.int32)
     acc_tokens = np.empty((R, L + 1), np.int32)
     rc = lib().orc_accept_stochastic(_ptr(draft), _ptr(target), _logit_dtype(draft), _ptr(tokens),
-                                     _ptr(u), _ptr(r), R, L, V, _ptr(acc_len), _ptr(acc_tokens))
+                                     _ptr(u), _ptr(r), R, L, V,
+                                     None if ng is None else _ptr(ng), _ptr(acc_len),
+                                     _ptr(acc_tokens))
     if rc:
         raise ValueError("bad arguments to accept_stochastic")
     return acc_len, acc_tokens

@@ -1272,10 +1272,13 @@ int orc_verify_chain(const double *p, const double *q, const int32_t *tokens, co
  * [R, L+1, V] (dtype as widen), softmax at temperature 1 in fp64, tokens
  * [R, L], u [R, L], r [R]. Outputs acc_len [R] (accepted guesses + 1) and
  * acc_tokens [R, L+1] (-1 past acc_len).
+ * n_guess [R] (may be NULL: L each): request i verifies only its first
+ * n_guess[i] guesses (clamped to [0, L]; the prefix a scheduler kept), so
+ * when all of those survive the bonus comes from target row n_guess[i].
  */
 int orc_accept_stochastic(const void *draft, const void *target, int dtype, const int32_t *tokens,
                           const double *u, const double *r, int R, int L, int64_t V,
-                          int32_t *acc_len, int32_t *acc_tokens)
+                          const int32_t *n_guess, int32_t *acc_len, int32_t *acc_tokens)
 {
     if (R < 1 || L < 0 || V < 1)
         return ORC_BAD_ARG;
@@ -1318,7 +1321,10 @@ int orc_accept_stochastic(const void *draft, const void *target, int dtype, cons
         int32_t *out = acc_tokens + (int64_t)i * (L + 1);
         for (int k = 0; k <= L; ++k)
             out[k] = -1;
-        acc_len[i] = orc_verify_chain(p, q, tokens + (int64_t)i * L, u + (int64_t)i * L, r[i], L, V,
+        int n = n_guess ? n_guess[i] : L;
+        n = n < 0 ? 0 : (n > L ? L : n);
+        /* the first n guesses: target rows 0..n, draft rows 0..n-1 */
+        acc_len[i] = orc_verify_chain(p, q, tokens + (int64_t)i * L, u + (int64_t)i * L, r[i], n, V,
                                       out);
         free(q);
         free(p);

@@ -217,3 +217,32 @@ def test_large_logits():
     for i in range(R):
         want = oracle.verify_chain(sm(tfar[i]), sm(dfar[i]), tokens[i], u[i], r[i])
         assert acc_len[i] == len(want) and list(acc_tokens[i, :acc_len[i]]) == want
+
+
+def test_scheduled_prefix_lengths():
+    """Verifying only the first n guesses of a request (the prefix a
+    scheduler kept) is the rule on the chain cut to n guesses: the bonus then
+    comes from target row n. n = 0 draws the bonus from row 0 at once."""
+    rng = np.random.default_rng(9)
+    R, L, V = 6, 5, 30
+    draft = (rng.standard_normal((R, L, V)) * 2).astype(np.float32)
+    target = (rng.standard_normal((R, L + 1, V)) * 2).astype(np.float32)
+    target[:, :L] = draft + (0.3 * rng.standard_normal((R, L, V))).astype(np.float32)
+    tokens = rng.integers(0, V, size=(R, L)).astype(np.int32)
+    u, r = rng.random((R, L)), rng.random(R)
+    n = np.array([0, 1, 2, 3, 5, 9], np.int32)  # 9 is clamped to L
+    acc_len, acc_tokens = oracle.accept_stochastic(draft, target, tokens, u, r, n_guess=n)
+    for i in range(R):
+        m = min(int(n[i]), L)
+        cut_len, cut_tok = oracle.accept_stochastic(
+            draft[i:i + 1, :m] if m > 0 else np.zeros((1, 0, V), np.float32),
+            np.concatenate([target[i:i + 1, :m], target[i:i + 1, m:m + 1]], axis=1),
+            tokens[i:i + 1, :m], u[i:i + 1, :m], r[i:i + 1])
+        assert acc_len[i] == cut_len[0] and acc_len[i] <= m + 1
+        np.testing.assert_array_equal(acc_tokens[i, :acc_len[i]], cut_tok[0, :cut_len[0]])
+        assert (acc_tokens[i, acc_len[i]:] == -1).all()
+    # no n_guess is n = L everywhere
+    full = oracle.accept_stochastic(draft, target, tokens, u, r)
+    same = oracle.accept_stochastic(draft, target, tokens, u, r, n_guess=np.full(R, L, np.int32))
+    np.testing.assert_array_equal(full[0], same[0])
+    np.testing.assert_array_equal(full[1], same[1])
