@@ -697,12 +697,18 @@ def time_scheduler(dev, reps=200, cpu=True):
                 0.1 ms per token checked (R + n tokens);
       measured: 64 requests x 15 guesses (the batch64 chains) with a cost
                 table measured here from this library's own verification
-                (ddt_accept_stochastic on 64 chains of 1, 2, 4, 8 and 15
-                guesses, interpolated in the number of guesses).
+                (ddt_accept_stochastic of the first 1, 2, 4, 8 and 15
+                guesses of each chain, interpolated in the number of
+                guesses).
     Confidences come from synth.draw_confidences. Reports the device time
-    per ddt_schedule_prefix call (CUDA events over `reps` calls after 3
-    warm-up calls), the chosen budget, its tokens per ms against verifying
-    every guess, and the oracle's time for the same decision."""
+    per ddt_schedule_prefix call (CUDA events around one replay of a CUDA
+    graph of `reps` calls, after 3 warm-up calls; beside it the same over an
+    eager loop of calls, where the host's launch rate can be the bound), the
+    chosen budget, its tokens per ms against verifying
+    every guess, and the oracle's time for the same decision; for the
+    measured workload also the scheduled step (the budget, then verification
+    of the kept prefixes with n_keep left on the device) beside verifying
+    every guess."""
     import torch
     from speculative_decoding_draft_depth_gb300 import ddt, synth
 
@@ -722,24 +728,46 @@ def time_scheduler(dev, reps=200, cpu=True):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / n
 
-    # the cost table: our chain verification at a few lengths
+    def graph_ms(fn, n):
+        # n calls captured in one CUDA graph and replayed: device time per
+        # call without the host's launch rate (a call is one kernel)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(n):
+                fn()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    # the cost table: our chain verification of the first Lp guesses of every
+    # chain (per-request guess counts on one 15-guess context, as a scheduled
+    # step runs it)
     cfg = synth.config("batch64")
     R, L, V = cfg.R, cfg.L, cfg.V
     inp = synth.draw_chain_inputs(cfg)
     dr, tg, tok, u, r = (td(inp[k]) for k in ("draft", "target", "tokens", "u", "r"))
+    cv = ddt.Context(ddt.make_config(R_max=R, L=L, V=V, B=8, K=8, Hq=4, Hkv=1, d=64,
+                                     page_size=16, max_pages_per_req=1, num_pages=1))
+    al = torch.empty(R, dtype=torch.int32, device=dev)
+    at = torch.empty((R, L + 1), dtype=torch.int32, device=dev)
     points = []
     for Lp in (1, 2, 4, 8, 15):
-        c = ddt.make_config(R_max=R, L=Lp, V=V, B=8, K=8, Hq=4, Hkv=1, d=64, page_size=16,
-                            max_pages_per_req=1, num_pages=1)
-        cx = ddt.Context(c)
-        d_p = dr[:, :Lp].contiguous()
-        t_p = tg[:, :Lp + 1].contiguous()
-        k_p, u_p = tok[:, :Lp].contiguous(), u[:, :Lp].contiguous()
-        al = torch.empty(R, dtype=torch.int32, device=dev)
-        at = torch.empty((R, Lp + 1), dtype=torch.int32, device=dev)
-        ms = events_ms(lambda: cx.ddt_accept_stochastic(d_p, t_p, k_p, u_p, r, R, al, at), 10)
+        ng = torch.full((R,), Lp, dtype=torch.int32, device=dev)
+        ms = events_ms(lambda: cv.ddt_accept_stochastic(dr, tg, tok, u, r, R, al, at,
+                                                        n_guess=ng), 10)
         points.append((R * Lp, ms))
-        del cx, d_p, t_p
     xs = np.array([p[0] for p in points], np.float64)
     ys = np.array([p[1] for p in points], np.float64)
     n_all = np.arange(R * L + 1, dtype=np.float64)
@@ -759,8 +787,9 @@ def time_scheduler(dev, reps=200, cpu=True):
         n_keep = torch.empty(Rw, dtype=torch.int32, device=dev)
         n_tot = torch.empty(1, dtype=torch.int32, device=dev)
         stats = torch.empty(2, dtype=torch.float64, device=dev)
-        ms = events_ms(lambda: cx.ddt_schedule_prefix(conf_d, Rw, cost_d, n_keep, n_tot, stats),
-                       reps)
+        call = lambda: cx.ddt_schedule_prefix(conf_d, Rw, cost_d, n_keep, n_tot, stats)  # noqa: E731
+        ms_eager = events_ms(call, reps)
+        ms = graph_ms(call, reps)
         if cx.ddt_device_status() != 0:
             raise RuntimeError("device status flags set in the scheduler")
         keep = n_keep.cpu().numpy()
@@ -768,6 +797,7 @@ def time_scheduler(dev, reps=200, cpu=True):
         surv = np.cumprod(conf.astype(np.float64), axis=1)
         theta_all = (Rw + surv.sum()) / float(cost[-1])
         row = {"requests": Rw, "guesses_per_request": Lw, "us_per_call": round(ms * 1e3, 2),
+               "us_per_call_eager": round(ms_eager * 1e3, 2),
                "kept": int(n_tot.cpu().numpy()[0]), "of": Rw * Lw,
                "tokens_per_ms": round(float(st[0]), 4),
                "tokens_per_ms_all_verified": round(theta_all, 4),
@@ -780,9 +810,26 @@ def time_scheduler(dev, reps=200, cpu=True):
                 oracle.schedule_prefix(conf, cost)
             row["cpu_oracle_us"] = round((time.perf_counter() - t0) / 20 * 1e6, 1)
         out[name] = row
+        if name == "measured":
+            # the scheduled step: the budget, then verification of the kept
+            # prefixes (n_keep stays on the device), against verifying all
+            n_kv = torch.empty(R, dtype=torch.int32, device=dev)
+
+            def scheduled():
+                cv.ddt_schedule_prefix(conf_d, R, cost_d, n_kv)
+                cv.ddt_accept_stochastic(dr, tg, tok, u, r, R, al, at, n_guess=n_kv)
+
+            row["scheduled_step_us"] = round(events_ms(scheduled, 20) * 1e3, 2)
+            row["verify_all_us"] = round(
+                events_ms(lambda: cv.ddt_accept_stochastic(dr, tg, tok, u, r, R, al, at), 20)
+                * 1e3, 2)
+            if cv.ddt_device_status() != 0:
+                raise RuntimeError("device status flags set in the scheduled step")
     out["measured"]["cost_table_points_ms"] = [[int(x), round(y, 4)] for x, y in points]
     out["workload"] = ("toy: 128 x 5, cost 25 ms + 0.1 ms per token checked; measured: 64 x 15 "
-                       "(batch64 chains), cost = this library's ddt_accept_stochastic time")
+                       "(batch64 chains), cost = this library's ddt_accept_stochastic time; "
+                       "scheduled_step_us = ddt_schedule_prefix then ddt_accept_stochastic of "
+                       "the kept prefixes")
     out["bound"] = "latency (one CTA; a few thousand slots)"
     return out
 

@@ -345,6 +345,12 @@ ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *args, const uint
  *   r             [R] f32 in [0, 1): the replacement or bonus token is the
  *                 first index (ascending) whose running sum of weights
  *                 exceeds r times the weights' total
+ *   n_guess       [R] i32, device, or NULL (L for every request): request i
+ *                 verifies only its first n = n_guess[i] guesses (the prefix
+ *                 ddt_schedule_prefix kept), so when all n survive the bonus
+ *                 comes from target row n. Draft rows k >= n and target rows
+ *                 k > n are not read. A value outside [0, L] is clamped into
+ *                 it and sets DDT_DEV_BAD_TREE.
  * Outputs: acc_len [R] (kept guesses + 1) and acc_tokens [R, L+1] (the kept
  * guesses, then the drawn token, then -1). The draw is -1 only when every
  * weight is zero (p <= q everywhere after rounding). Guesses outside [0, V)
@@ -354,7 +360,7 @@ ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *args, const uint
 ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
                                  const void *target_logits, const int32_t *draft_tokens,
                                  const float *u, const float *r, int32_t R, int32_t *acc_len,
-                                 int32_t *acc_tokens, void *stream);
+                                 int32_t *acc_tokens, const int32_t *n_guess, void *stream);
 
 /* The hardware-aware prefix scheduler -- "DSpark Speculative Decoding
  * Explained: Block Drafting and Confidence Checks", sections "Survival

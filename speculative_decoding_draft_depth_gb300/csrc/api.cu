@@ -567,7 +567,7 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
 ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
                                  const void *target_logits, const int32_t *draft_tokens,
                                  const float *u, const float *r, int32_t R, int32_t *acc_len,
-                                 int32_t *acc_tokens, void *stream)
+                                 int32_t *acc_tokens, const int32_t *n_guess, void *stream)
 {
     ddt_status st = check_R(ctx, R);
     if (st != DDT_OK)
@@ -579,7 +579,7 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
     if ((st = set_device(ctx)) != DDT_OK)
         return st;
     DDT_TRY(launch_accept_stochastic(ctx, draft_logits, target_logits, draft_tokens, u, r, R,
-                                     acc_len, acc_tokens, (cudaStream_t)stream));
+                                     n_guess, acc_len, acc_tokens, (cudaStream_t)stream));
     return DDT_OK;
 }
 

@@ -148,7 +148,8 @@ int stochastic_chunk_elems(int dtype);
 int stochastic_draw_chunks(int V);
 cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const void *target,
                                      const int32_t *tokens, const float *u, const float *r, int R,
-                                     int32_t *acc_len, int32_t *acc_tokens, cudaStream_t s);
+                                     const int32_t *n_guess, int32_t *acc_len, int32_t *acc_tokens,
+                                     cudaStream_t s);
 
 // the hardware-aware prefix scheduler (sched.cu)
 int schedule_smem_bytes(int R, int L);

@@ -110,6 +110,15 @@ DDT_DEVINL void chunk_ms(const T *__restrict__ zrow, int c0, int cn, float &M, f
     }
 }
 
+// the guesses request i verifies: n_guess[i] clamped to [0, L], or L
+DDT_DEVINL int guesses_of(const int32_t *n_guess, int i, int L)
+{
+    if (n_guess == nullptr)
+        return L;
+    const int n = n_guess[i];
+    return n < 0 ? 0 : (n > L ? L : n);
+}
+
 // one logit of a row (the guess's), as fp32
 template <typename T>
 DDT_DEVINL float logit_at(const T *row, int x)
@@ -124,6 +133,7 @@ struct RowsArgs {
     const void *draft;        // [R, L, V] draft logits
     const void *target;       // [R, L + 1, V] target logits
     float2 *part_d, *part_t;  // chunk (max, sum) pairs of the draft / target rows
+    const int32_t *n_guess;   // [R] guesses verified per request, or nullptr (L)
     int32_t *status;
     int L, V, nch_d, nch_t;
     bool al_d, al_t;          // 16-byte aligned rows
@@ -142,10 +152,18 @@ sv_rows_kernel(RowsArgs a)
     __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
     pdl_trigger();
 
+    // which row (k) and chunk (c); rows past the request's verified guesses
+    // are never read, so their CTAs do nothing
+    const bool isd = j < L * a.nch_d;
+    const int jj = isd ? j : j - L * a.nch_d, nch = isd ? a.nch_d : a.nch_t;
+    const int k = jj / nch, c = jj - k * nch;
+    const int n = guesses_of(a.n_guess, i, L);
+    if (isd ? k >= n : k > n)
+        return;
     float M = 0.f, S = 0.f;
     float2 *slot;
-    if (j < L * a.nch_d) {  // a draft row
-        const int row = i * L + j / a.nch_d, c = j % a.nch_d;
+    if (isd) {  // a draft row
+        const int row = i * L + k;
         constexpr int CH = SV_THREADS * SV_NV * Elem<TD>::VE;
         const TD *z = static_cast<const TD *>(a.draft) + (int64_t)row * V;
         if (a.al_d)
@@ -154,8 +172,7 @@ sv_rows_kernel(RowsArgs a)
             chunk_ms<TD, false>(z, c * CH, min(CH, V - c * CH), M, S, s_m, s_s);
         slot = a.part_d + (int64_t)row * a.nch_d + c;
     } else {  // a target row
-        const int jt = j - L * a.nch_d;
-        const int row = i * (L + 1) + jt / a.nch_t, c = jt % a.nch_t;
+        const int row = i * (L + 1) + k;
         constexpr int CH = SV_THREADS * SV_NV * Elem<TT>::VE;
         const TT *z = static_cast<const TT *>(a.target) + (int64_t)row * V;
         if (a.al_t)
@@ -178,6 +195,7 @@ struct DrawArgs {
     const float *u;                 // [R, L] acceptance uniforms
     const float *r;                 // [R] draw uniforms
     const float2 *part_d, *part_t;  // from sv_rows_kernel
+    const int32_t *n_guess;         // [R] guesses verified per request, or nullptr (L)
     float *part_w;                  // [R, nchw] chunk totals of the weights
     unsigned *cnt;                  // [R] arrivals (self-resetting)
     int32_t *acc_len;               // [R]
@@ -194,7 +212,8 @@ struct DrawArgs {
 // (kept iff u < min(1, p/q); a ballot finds the first rejection k*). The CTA
 // with `writer` set also stores the length and every committed token but the
 // drawn one. Returns k*; s_lse[t] holds the log-partition of row t (draft rows
-// 0..L-1, then target rows 0..L).
+// 0..L-1, then target rows 0..L). Only the rows the request verifies are
+// touched: draft rows k < n and target rows k <= n, n = its guess count.
 template <typename TD, typename TT>
 __device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float *s_lse,
                                    float *s_lz, int *s_ks, float2 *s_pairs)
@@ -204,22 +223,30 @@ __device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float 
     const TD *zd = static_cast<const TD *>(a.draft) + (int64_t)i * L * V;
     const TT *zt = static_cast<const TT *>(a.target) + (int64_t)i * (L + 1) * V;
     const int nd = L * a.nch_d, nt = (L + 1) * a.nch_t;
+    const int n = guesses_of(a.n_guess, i, L);
+    // row t (as in s_lse) is one the request verifies
+    auto used = [&](int t) { return t < L ? t < n : t - L <= n; };
     if (nd + nt <= SV_DEC_PAIRS) {
-        // every pair of the request and the 2L guess logits at once (one round
+        // every pair of the request and the guess logits at once (one round
         // trip), then a thread per row merges its pairs from shared memory
         const float2 *pd = a.part_d + (int64_t)i * nd, *pt = a.part_t + (int64_t)i * nt;
+        const int ud = n * a.nch_d, ut = (n + 1) * a.nch_t;  // pairs of the used rows
         for (int q = tid; q < nd + nt; q += SV_THREADS)
-            s_pairs[q] = q < nd ? __ldcg(pd + q) : __ldcg(pt + (q - nd));
+            if (q < nd ? q < ud : q - nd < ut)
+                s_pairs[q] = q < nd ? __ldcg(pd + q) : __ldcg(pt + (q - nd));
         for (int q = tid; q < 2 * L; q += SV_THREADS) {
             const int k = q < L ? q : q - L;
-            const int x = a.tokens[(int64_t)i * L + k];
             float zx = 0.f;
-            if (x >= 0 && x < V)
-                zx = q < L ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x);
+            if (k < n) {
+                const int x = a.tokens[(int64_t)i * L + k];
+                if (x >= 0 && x < V)
+                    zx = q < L ? logit_at(zd + (int64_t)k * V, x)
+                               : logit_at(zt + (int64_t)k * V, x);
+            }
             s_lz[q] = zx;
         }
         __syncthreads();
-        if (tid < 2 * L + 1) {
+        if (tid < 2 * L + 1 && used(tid)) {
             const int t = tid;
             const float2 *pp = t < L ? s_pairs + t * a.nch_d : s_pairs + nd + (t - L) * a.nch_t;
             const int nch = t < L ? a.nch_d : a.nch_t;
@@ -233,13 +260,15 @@ __device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float 
         }
     } else {
         for (int t = warp; t < 2 * L + 1; t += SV_THREADS / 32) {
+            if (!used(t))
+                continue;
             const bool isd = t < L;
             const int k = isd ? t : t - L;
             const int nch = isd ? a.nch_d : a.nch_t;
             const float2 *part = isd ? a.part_d + ((int64_t)i * L + k) * nch
                                      : a.part_t + ((int64_t)i * (L + 1) + k) * nch;
             float zx = 0.f;  // the guess's logit, loaded beside the pairs
-            if (lane == 0 && k < L) {
+            if (lane == 0 && k < n) {
                 const int x = a.tokens[(int64_t)i * L + k];
                 if (x >= 0 && x < V)
                     zx = isd ? logit_at(zd + (int64_t)k * V, x) : logit_at(zt + (int64_t)k * V, x);
@@ -264,8 +293,10 @@ __device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float 
     }
     __syncthreads();
     if (warp == 0) {
+        if (writer && lane == 0 && a.n_guess != nullptr && n != a.n_guess[i])
+            set_status(a.status, DDT_DEV_BAD_TREE);
         bool keep = false;
-        if (lane < L) {
+        if (lane < n) {
             const int x = a.tokens[(int64_t)i * L + lane];
             const bool ok = x >= 0 && x < V;
             if (!ok && writer)
@@ -276,7 +307,7 @@ __device__ __noinline__ int decide(const DrawArgs &a, int i, bool writer, float 
             keep = ok && a.u[(int64_t)i * L + lane] < ratio;
         }
         const unsigned kept = __ballot_sync(0xFFFFFFFFu, keep);
-        const int ks = __ffs(~kept) - 1;  // lanes >= L never keep: ks <= L
+        const int ks = __ffs(~kept) - 1;  // lanes >= n never keep: ks <= n
         if (lane == 0)
             *s_ks = ks;
         if (writer) {
@@ -398,7 +429,9 @@ DDT_DEVINL void draw_body(const DrawArgs &a, int i, int c)
     __shared__ float2 s_pairs[SV_DEC_PAIRS];
 
     const int ks = decide<TD, TT>(a, i, c == 0, s_lse, s_lz, &s_ks, s_pairs);
-    const bool leftover = ks < L;
+    // a rejection draws from the leftover; all verified guesses kept, the
+    // bonus from target row ks
+    const bool leftover = ks < guesses_of(a.n_guess, i, L);
     const float bt = -s_lse[L + ks] * DDT_LOG2E;
     const float bd = leftover ? -s_lse[ks] * DDT_LOG2E : 0.f;
     const TT *zt = static_cast<const TT *>(a.target) + ((int64_t)i * (L + 1) + ks) * V;
@@ -570,7 +603,8 @@ int stochastic_draw_chunks(int V)
 
 cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const void *target,
                                      const int32_t *tokens, const float *u, const float *r, int R,
-                                     int32_t *acc_len, int32_t *acc_tokens, cudaStream_t s)
+                                     const int32_t *n_guess, int32_t *acc_len, int32_t *acc_tokens,
+                                     cudaStream_t s)
 {
     const ddt_config &cfg = c->cfg;
     const int L = cfg.L, V = cfg.V;
@@ -580,6 +614,7 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     ra.target = target;
     ra.part_d = c->sv_part_d;
     ra.part_t = c->sv_part_t;
+    ra.n_guess = n_guess;
     ra.status = c->status;
     ra.L = L;
     ra.V = V;
@@ -611,6 +646,7 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     da.r = r;
     da.part_d = c->sv_part_d;
     da.part_t = c->sv_part_t;
+    da.n_guess = n_guess;
     da.part_w = c->sv_part_w;
     da.cnt = c->sv_cnt;
     da.acc_len = acc_len;

@@ -89,7 +89,7 @@ def load(path=LIB_PATH):
         "ddt_markov_table": ([_P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
         "ddt_build_tree_markov": ([_P, _P, _P, i32, _P, _P, _P, _P, _P, _P], i32),
         "ddt_round_markov": ([_P, ctypes.POINTER(RoundArgs), _P, _P, _P, _P], i32),
-        "ddt_accept_stochastic": ([_P, _P, _P, _P, _P, _P, i32, _P, _P, _P], i32),
+        "ddt_accept_stochastic": ([_P, _P, _P, _P, _P, _P, i32, _P, _P, _P, _P], i32),
         "ddt_schedule_prefix": ([_P, _P, i32, _P, _P, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
@@ -213,10 +213,10 @@ class Context:
                                _stream(stream)), "ddt_accept")
 
     def ddt_accept_stochastic(self, draft_logits, target_logits, draft_tokens, u, r, R, acc_len,
-                              acc_tokens, stream=None):
+                              acc_tokens, n_guess=None, stream=None):
         _check(_lib.ddt_accept_stochastic(self._h, _ptr(draft_logits), _ptr(target_logits),
                                           _ptr(draft_tokens), _ptr(u), _ptr(r), R, _ptr(acc_len),
-                                          _ptr(acc_tokens), _stream(stream)),
+                                          _ptr(acc_tokens), _ptr(n_guess), _stream(stream)),
                "ddt_accept_stochastic")
 
     def ddt_schedule_prefix(self, conf, R, cost_ms, n_keep, n_total=None, stats=None,

@@ -45,31 +45,33 @@ def softmax64(z):
     return e / e.sum(-1, keepdims=True)
 
 
-def run_gpu(ctx, draft, target, tokens, u, r, R=None, stream=None):
+def run_gpu(ctx, draft, target, tokens, u, r, R=None, stream=None, n_guess=None):
     R = draft.shape[0] if R is None else R
     L = tokens.shape[1]
     acc_len = torch.full((max(R, 1),), -7, dtype=torch.int32, device="cuda")
     acc_tok = torch.full((max(R, 1), L + 1), -7, dtype=torch.int32, device="cuda")
+    ng = None if n_guess is None else (n_guess if torch.is_tensor(n_guess) else dev(n_guess))
     ctx.ddt_accept_stochastic(dev(draft), dev(target), dev(tokens), dev(u), dev(r), R, acc_len,
-                              acc_tok, stream=stream)
+                              acc_tok, n_guess=ng, stream=stream)
     torch.cuda.synchronize()
     return host(acc_len), host(acc_tok), ctx.ddt_device_status()
 
 
-def run_oracle(draft, target, tokens, u, r):
+def run_oracle(draft, target, tokens, u, r, n_guess=None):
     # the oracle takes one logit dtype: widen bf16 (exactly) when the two differ
     if draft.dtype != target.dtype:
         draft, target = widen(draft), widen(target)
     return oracle.accept_stochastic(draft, target, tokens, u.astype(np.float64),
-                                    r.astype(np.float64))
+                                    r.astype(np.float64), n_guess=n_guess)
 
 
-def check_request(i, g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r):
+def check_request(i, g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, n_guess=None):
     """Exact agreement, or a disagreement explained by a tie (see above)."""
     L = tokens.shape[1]
     if g_len == o_len and np.array_equal(g_tok, o_tok):
         return "exact"
-    assert 1 <= g_len <= L + 1, (i, g_len)
+    n = L if n_guess is None else int(np.clip(n_guess[i], 0, L))  # guesses verified
+    assert 1 <= g_len <= n + 1, (i, g_len)
     assert np.array_equal(g_tok[:g_len - 1], tokens[i, :g_len - 1]), i
     assert (g_tok[g_len:] == -1).all(), i
     p = softmax64(target[i])
@@ -80,7 +82,7 @@ def check_request(i, g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r):
         a = 1.0 if q[k, x] == 0 else min(1.0, p[k, x] / q[k, x])
         assert abs(float(u[i, k]) - a) <= U_TIE, (i, k, float(u[i, k]), a)
     ks = g_len - 1
-    w = np.maximum(p[ks] - q[ks], 0.0) if ks < L else p[L]
+    w = np.maximum(p[ks] - q[ks], 0.0) if ks < n else p[n]
     W = w.sum()
     t = int(g_tok[ks])
     if W <= CDF_TIE:  # (almost) no weight: any in-range token or -1
@@ -93,9 +95,9 @@ def check_request(i, g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r):
     return "tie"
 
 
-def compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r):
+def compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, n_guess=None):
     kinds = [check_request(i, g_len[i], g_tok[i], o_len[i], o_tok[i], draft, target, tokens, u,
-                           r) for i in range(len(o_len))]
+                           r, n_guess) for i in range(len(o_len))]
     # ties are rare: a run where most requests need the band has a real bug
     assert kinds.count("tie") <= max(1, len(kinds) // 16), kinds
     return kinds
@@ -261,3 +263,83 @@ def test_side_stream():
     assert st == 0
     o_len, o_tok = run_oracle(draft, target, tokens, u, r)
     compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r)
+
+
+# ------------------------------------------ a scheduled prefix (guesses per request)
+def test_random_guess_counts_match_oracle():
+    """Request i verifies only its first n_i guesses, n_i drawn from [0, L]
+    (0 and L both present): kept prefixes, draws and bonus rows (target row
+    n_i) against the oracle, on a ragged vocabulary."""
+    draft, target, tokens, u, r = case_inputs("ragged_bf16")
+    R, L = tokens.shape
+    ng = np.array([0, L, 2, 1, 4], dtype=np.int32)[:R]
+    ctx = chain_ctx(R, L, draft.shape[-1], True, True)
+    g_len, g_tok, st = run_gpu(ctx, draft, target, tokens, u, r, n_guess=ng)
+    assert st == 0
+    o_len, o_tok = run_oracle(draft, target, tokens, u, r, n_guess=ng)
+    compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, ng)
+    assert (g_len <= ng + 1).all()
+    assert g_len[0] == 1  # nothing verified: only the bonus from target row 0
+
+
+def test_guess_counts_with_every_guess_kept_take_the_bonus_from_row_n():
+    draft, target, tokens, u, r = base_case(R=6, L=5, seed=78)
+    target[:, :-1] = draft  # ratio exactly 1 on every guessed row
+    ng = np.arange(6, dtype=np.int32) % 6  # 0..5
+    u0 = np.zeros_like(u)
+    ctx = chain_ctx(6, 5, draft.shape[-1], True, True)
+    g_len, g_tok, st = run_gpu(ctx, draft, target, tokens, u0, r, n_guess=ng)
+    assert st == 0
+    o_len, o_tok = run_oracle(draft, target, tokens, u0, r, n_guess=ng)
+    np.testing.assert_array_equal(o_len, ng + 1)
+    compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u0, r, ng)
+
+
+def test_rows_past_the_guess_count_are_not_read():
+    """NaNs planted in draft rows k >= n_i and target rows k > n_i are never
+    seen: no NaN status, and the result is that of clean rows."""
+    draft, target, tokens, u, r = base_case(R=4, L=6, seed=79)
+    ng = np.array([2, 0, 6, 3], dtype=np.int32)
+    o_len, o_tok = run_oracle(draft, target, tokens, u, r, n_guess=ng)
+    d2, t2 = draft.copy(), target.copy()
+    for i, n in enumerate(ng):
+        d2[i, n:, :] = np.uint16(0x7FC0)
+        t2[i, n + 1:, :] = np.uint16(0x7FC0)
+    ctx = chain_ctx(4, 6, draft.shape[-1], True, True)
+    g_len, g_tok, st = run_gpu(ctx, d2, t2, tokens, u, r, n_guess=ng)
+    assert st == 0
+    compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, ng)
+
+
+def test_out_of_range_guess_count_is_clamped_and_sets_status():
+    draft, target, tokens, u, r = base_case(R=3, L=5, seed=80)
+    ng = np.array([-1, 7, 3], dtype=np.int32)
+    ctx = chain_ctx(3, 5, draft.shape[-1], True, True)
+    g_len, g_tok, st = run_gpu(ctx, draft, target, tokens, u, r, n_guess=ng)
+    assert st & ddt.DEV_BAD_TREE
+    o_len, o_tok = run_oracle(draft, target, tokens, u, r, n_guess=np.clip(ng, 0, 5))
+    compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, np.clip(ng, 0, 5))
+
+
+def test_scheduler_output_feeds_verification_on_the_device():
+    """ddt_schedule_prefix's n_keep, left on the device, is the guess count
+    of ddt_accept_stochastic: the two calls chained against the oracle's
+    schedule_prefix then accept_stochastic, on the 64-chain workload."""
+    cfg = synth.config("batch64")
+    d = synth.draw_chain_inputs(cfg)
+    R, L = cfg.R, cfg.L
+    conf = synth.draw_confidences(R, L, seed=81)
+    cost = (25.0 + 0.1 * (R + np.arange(R * L + 1))).astype(np.float32)
+    ctx = chain_ctx(R, L, cfg.V, True, True)
+    keep = torch.full((R,), -7, dtype=torch.int32, device="cuda")
+    ctx.ddt_schedule_prefix(dev(conf), R, dev(cost), keep)
+    g_len, g_tok, st = run_gpu(ctx, d["draft"], d["target"], d["tokens"], d["u"], d["r"],
+                               n_guess=keep)
+    assert st == 0
+    o_keep = oracle.schedule_prefix(conf, cost.astype(np.float64))[0]
+    np.testing.assert_array_equal(host(keep), o_keep)
+    assert 0 < o_keep.sum() < R * L  # the budget cuts some chains, not all
+    o_len, o_tok = run_oracle(d["draft"], d["target"], d["tokens"], d["u"], d["r"],
+                              n_guess=o_keep)
+    compare(g_len, g_tok, o_len, o_tok, d["draft"], d["target"], d["tokens"], d["u"], d["r"],
+            o_keep)
