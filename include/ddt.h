@@ -94,7 +94,7 @@ typedef enum ddt_dtype { DDT_BF16 = 0, DDT_F32 = 1 } ddt_dtype;
 #define DDT_DEV_TIMEOUT 0x8    /* a bounded on-device wait gave up (the kernel wound down) */
 
 typedef struct ddt_config {
-    int32_t R_max;             /* most requests a call may carry */
+    int32_t R_max;             /* most requests a call may carry (1..2048) */
     int32_t L;                 /* draft depths per request (1..18) */
     int32_t V;                 /* vocabulary size */
     int32_t B;                 /* non-root tree nodes (1..127) */

@@ -24,6 +24,7 @@
 //    re-reads that chunk in index order (32 consecutive weights per thread,
 //    a block scan) and picks the first index whose running sum exceeds it.
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 
@@ -38,6 +39,7 @@ constexpr int SV_NV = 8;                   // 16-byte vectors per thread in the 
 constexpr int SV_WPT = 32;                 // weights per thread in the draw
 constexpr int SV_WCH = SV_THREADS * SV_WPT;  // weights per CTA of the draw (8192)
 constexpr int SV_DEC_PAIRS = 1024;           // chunk pairs a request's decision stages in smem
+constexpr int SV_ROW_WAVES = 2;  // counted row pass: CTAs = SMs x 5 resident x this
 
 // ---------------------------------------------------------------- row pass
 // (max, sum of exp(x - max)) of one chunk of a row, for the whole CTA; the
@@ -139,27 +141,13 @@ struct RowsArgs {
     bool al_d, al_t;          // 16-byte aligned rows
 };
 
-// grid: R * (L * nch_d + (L + 1) * nch_t) CTAs, request-major; each stores
-// its chunk's (max, sum) pair and exits (the decisions are taken by the
-// draw kernel, which waits for this whole grid)
+// one item of the row pass: chunk c of draft row k (isd) or target row k of
+// request i; thread 0 stores the chunk's (max, sum) pair
 template <typename TD, typename TT>
-__global__ void __launch_bounds__(SV_THREADS, 5)  // 48 registers: five CTAs per SM
-sv_rows_kernel(RowsArgs a)
+DDT_DEVINL void row_item(const RowsArgs &a, int i, bool isd, int k, int c, float *s_m,
+                         float *s_s)
 {
     const int L = a.L, V = a.V;
-    const int per = L * a.nch_d + (L + 1) * a.nch_t;
-    const int i = blockIdx.x / per, j = blockIdx.x % per;
-    __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
-    pdl_trigger();
-
-    // which row (k) and chunk (c); rows past the request's verified guesses
-    // are never read, so their CTAs do nothing
-    const bool isd = j < L * a.nch_d;
-    const int jj = isd ? j : j - L * a.nch_d, nch = isd ? a.nch_d : a.nch_t;
-    const int k = jj / nch, c = jj - k * nch;
-    const int n = guesses_of(a.n_guess, i, L);
-    if (isd ? k >= n : k > n)
-        return;
     float M = 0.f, S = 0.f;
     float2 *slot;
     if (isd) {  // a draft row
@@ -185,6 +173,111 @@ sv_rows_kernel(RowsArgs a)
         if (M != M || S != S)
             set_status(a.status, DDT_DEV_NAN_LOGITS);
         *slot = make_float2(M, S);
+    }
+}
+
+// grid: R * (L * nch_d + (L + 1) * nch_t) CTAs, request-major; each stores
+// its chunk's (max, sum) pair and exits (the decisions are taken by the
+// draw kernel, which waits for this whole grid)
+template <typename TD, typename TT>
+__global__ void __launch_bounds__(SV_THREADS, 5)  // 48 registers: five CTAs per SM
+sv_rows_kernel(RowsArgs a)
+{
+    const int L = a.L;
+    const int per = L * a.nch_d + (L + 1) * a.nch_t;
+    const int i = blockIdx.x / per, j = blockIdx.x % per;
+    __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
+    pdl_trigger();
+
+    // which row (k) and chunk (c); rows past the request's verified guesses
+    // are never read, so their CTAs do nothing
+    const bool isd = j < L * a.nch_d;
+    const int jj = isd ? j : j - L * a.nch_d, nch = isd ? a.nch_d : a.nch_t;
+    const int k = jj / nch;
+    const int n = guesses_of(a.n_guess, i, L);
+    if (isd ? k >= n : k > n)
+        return;
+    row_item<TD, TT>(a, i, isd, k, jj - k * nch, s_m, s_s);
+}
+
+// The row pass for given guess counts: only the items of the rows the
+// requests verify (n_i * nch_d + (n_i + 1) * nch_t for request i), numbered
+// request-major, draft rows before target rows. Each CTA first turns the
+// counts into every request's first item (in shared memory: s_first [R + 1],
+// then s_n [R]), then takes a contiguous range of the items: a binary search
+// finds its first item's request, and the rest follow in order. No CTA is launched only to find its row unused.
+template <typename TD, typename TT>
+__global__ void __launch_bounds__(SV_THREADS, 5)
+sv_rows_counted_kernel(RowsArgs a, int R)
+{
+    extern __shared__ int s_dyn[];
+    int *s_first = s_dyn, *s_n = s_dyn + R + 1;
+    __shared__ float s_m[SV_THREADS / 32], s_s[SV_THREADS / 32];
+    __shared__ int s_wsum[SV_THREADS / 32];
+    pdl_trigger();
+    const int L = a.L, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // each thread sums a contiguous run of requests, then a block scan
+    const int run = (R + SV_THREADS - 1) / SV_THREADS;
+    const int r0 = min(R, tid * run), r1 = min(R, r0 + run);
+    int own = 0;
+    for (int i = r0; i < r1; ++i) {
+        const int n = guesses_of(a.n_guess, i, L);
+        s_n[i] = n;
+        own += n * a.nch_d + (n + 1) * a.nch_t;
+    }
+    int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o)
+            incl += v;
+    }
+    if (lane == 31)
+        s_wsum[warp] = incl;
+    __syncthreads();
+    int first = incl - own;
+    for (int w = 0; w < warp; ++w)
+        first += s_wsum[w];
+    for (int i = r0; i < r1; ++i) {
+        s_first[i] = first;
+        first += s_n[i] * a.nch_d + (s_n[i] + 1) * a.nch_t;
+    }
+    if (tid == SV_THREADS - 1)  // its run ends at R: first is the total
+        s_first[R] = first;
+    __syncthreads();
+
+    const int total = s_first[R];
+    const int span = (total + gridDim.x - 1) / gridDim.x;
+    int q = blockIdx.x * span;
+    const int qe = min(total, q + span);
+    if (q >= qe)
+        return;
+    // the first item's request: the last i with s_first[i] <= q (every
+    // request has at least one item, target row 0)
+    int i = 0, hi = R - 1;
+    while (i < hi) {
+        const int mid = (i + hi + 1) >> 1;
+        if (s_first[mid] <= q)
+            i = mid;
+        else
+            hi = mid - 1;
+    }
+    int n = s_n[i], j = q - s_first[i];  // j: the item within request i
+    for (int left = qe - q;;) {
+        const int nd = n * a.nch_d;
+        const bool isd = j < nd;
+        const int jj = isd ? j : j - nd, nch = isd ? a.nch_d : a.nch_t;
+        const int k = jj / nch;
+        row_item<TD, TT>(a, i, isd, k, jj - k * nch, s_m, s_s);
+        if (--left == 0)
+            break;
+        __syncthreads();  // s_m / s_s are reused by the next item
+        if (++j == nd + (n + 1) * a.nch_t) {  // past request i's last item
+            ++i;  // items remain: request i exists
+            n = s_n[i];
+            j = 0;
+        }
     }
 }
 
@@ -626,7 +719,20 @@ cudaError_t launch_accept_stochastic(const ddt_ctx *c, const void *draft, const 
     if (nrows > 0x7FFFFFFF)
         return cudaErrorInvalidConfiguration;
     const bool bd = cfg.draft_dtype == DDT_BF16, bt = cfg.target_dtype == DDT_BF16;
-    if (bd && bt)
+    if (n_guess != nullptr) {
+        // only the used rows' items, over a grid of a few waves; R <= R_max
+        // <= 2048 keeps the (2R + 1) ints of shared memory within 16 KB
+        const unsigned grid = (unsigned)std::min<int64_t>(nrows, (int64_t)c->num_sms * 5 * SV_ROW_WAVES);
+        const size_t sm = (size_t)(2 * R + 1) * sizeof(int);
+        if (bd && bt)
+            sv_rows_counted_kernel<uint16_t, uint16_t><<<grid, SV_THREADS, sm, s>>>(ra, R);
+        else if (bd)
+            sv_rows_counted_kernel<uint16_t, float><<<grid, SV_THREADS, sm, s>>>(ra, R);
+        else if (bt)
+            sv_rows_counted_kernel<float, uint16_t><<<grid, SV_THREADS, sm, s>>>(ra, R);
+        else
+            sv_rows_counted_kernel<float, float><<<grid, SV_THREADS, sm, s>>>(ra, R);
+    } else if (bd && bt)
         sv_rows_kernel<uint16_t, uint16_t><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);
     else if (bd)
         sv_rows_kernel<uint16_t, float><<<(unsigned)nrows, SV_THREADS, 0, s>>>(ra);

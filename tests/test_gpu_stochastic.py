@@ -343,3 +343,18 @@ def test_scheduler_output_feeds_verification_on_the_device():
                               n_guess=o_keep)
     compare(g_len, g_tok, o_len, o_tok, d["draft"], d["target"], d["tokens"], d["u"], d["r"],
             o_keep)
+
+
+def test_guess_counts_at_the_most_requests():
+    """2048 requests (the context's limit): the row pass's scan of the
+    counts runs 8 requests per thread."""
+    R, L, V = 2048, 3, 64
+    d = draw(R, L, V, "f32", seed=82)
+    rng = np.random.default_rng(83)
+    ng = rng.integers(0, L + 1, size=R).astype(np.int32)
+    ctx = chain_ctx(R, L, V, False, False)
+    g_len, g_tok, st = run_gpu(ctx, d["draft"], d["target"], d["tokens"], d["u"], d["r"],
+                               n_guess=ng)
+    assert st == 0
+    o_len, o_tok = run_oracle(d["draft"], d["target"], d["tokens"], d["u"], d["r"], n_guess=ng)
+    compare(g_len, g_tok, o_len, o_tok, d["draft"], d["target"], d["tokens"], d["u"], d["r"], ng)
