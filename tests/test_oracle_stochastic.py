@@ -224,16 +224,18 @@ def test_scheduled_prefix_lengths():
     scheduler kept) is the rule on the chain cut to n guesses: the bonus then
     comes from target row n. n = 0 draws the bonus from row 0 at once."""
     rng = np.random.default_rng(9)
-    R, L, V = 6, 5, 30
+    R, L, V = 7, 5, 30
     draft = (rng.standard_normal((R, L, V)) * 2).astype(np.float32)
     target = (rng.standard_normal((R, L + 1, V)) * 2).astype(np.float32)
     target[:, :L] = draft + (0.3 * rng.standard_normal((R, L, V))).astype(np.float32)
     tokens = rng.integers(0, V, size=(R, L)).astype(np.int32)
     u, r = rng.random((R, L)), rng.random(R)
-    n = np.array([0, 1, 2, 3, 5, 9], np.int32)  # 9 is clamped to L
+    n = np.array([0, 1, 2, 3, 5, 9, -1], np.int32)  # 9 is clamped to L, -1 to 0
+    u[5:] = 0.0  # the clamped requests keep every guess they verify
     acc_len, acc_tokens = oracle.accept_stochastic(draft, target, tokens, u, r, n_guess=n)
+    assert acc_len[5] == L + 1 and acc_len[6] == 1
     for i in range(R):
-        m = min(int(n[i]), L)
+        m = min(max(int(n[i]), 0), L)
         cut_len, cut_tok = oracle.accept_stochastic(
             draft[i:i + 1, :m] if m > 0 else np.zeros((1, 0, V), np.float32),
             np.concatenate([target[i:i + 1, :m], target[i:i + 1, m:m + 1]], axis=1),
