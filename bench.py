@@ -190,16 +190,20 @@ def cpu_oracle_round(cfg, inp, reqs):
     return time.perf_counter() - t0
 
 
-def cpu_sample(cfg, inp, n_req):
+def cpu_sample(cfg, inp, n_req, repeats=3):
+    """The oracle, as it stands, on n_req requests of the round: the median of
+    `repeats` passes, scaled to the full batch."""
     import oracle
     rng = np.random.default_rng(12345)
     reqs = np.sort(rng.choice(cfg.R, size=n_req, replace=False))
-    secs = cpu_oracle_round(cfg, inp, reqs)
+    runs = [cpu_oracle_round(cfg, inp, reqs) for _ in range(repeats)]
+    secs = float(np.median(runs))
     per_round = secs * cfg.R / n_req
     return {"value": 1.0 / per_round, "unit": UNIT, "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": "%d of %d requests of the same round (all stages), %.2f s, scaled to the "
-                      "full batch" % (n_req, cfg.R, secs)}
+            "sample": "%d of %d requests of the same round (all stages), median of %d passes "
+                      "(%s s), scaled to the full batch"
+                      % (n_req, cfg.R, repeats, ", ".join("%.2f" % x for x in runs))}
 
 
 # ----------------------------------------------------------------- inputs
@@ -384,7 +388,7 @@ def main():
         out["e2e"] = time_e2e(ctx, cfg, inp, bufs, d, ctx0, stream, dev, world, dist,
                               steps=max(10, min(args.steps, 50)))
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_sample(cfg, inp, n_req=16)
+        out["cpu_baseline"] = cpu_sample(cfg, inp, n_req=min(32, cfg.R))
     if rank == 0:
         print(json.dumps(out))
     if dist:
