@@ -358,3 +358,35 @@ def test_guess_counts_at_the_most_requests():
     assert st == 0
     o_len, o_tok = run_oracle(d["draft"], d["target"], d["tokens"], d["u"], d["r"], n_guess=ng)
     compare(g_len, g_tok, o_len, o_tok, d["draft"], d["target"], d["tokens"], d["u"], d["r"], ng)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_case_with_guess_counts(name):
+    """Every shape and dtype pair of the chain cases, with random counts:
+    each variant of the counted row pass and of the draw."""
+    draft, target, tokens, u, r = case_inputs(name)
+    R, L = tokens.shape
+    ng = np.random.default_rng(85).integers(0, L + 1, size=R).astype(np.int32)
+    ctx = chain_ctx(R, L, draft.shape[-1], draft.dtype == np.uint16, target.dtype == np.uint16)
+    g_len, g_tok, st = run_gpu(ctx, draft, target, tokens, u, r, n_guess=ng)
+    assert st == 0
+    o_len, o_tok = run_oracle(draft, target, tokens, u, r, n_guess=ng)
+    compare(g_len, g_tok, o_len, o_tok, draft, target, tokens, u, r, ng)
+
+
+# ------------------------------------- a vocabulary past the staged decision
+@pytest.mark.parametrize("counts", [False, True])
+def test_wide_vocabulary_decides_per_warp(counts):
+    """V = 600000 at L = 18: the 2L + 1 rows of 37 chunks each hold more
+    pairs than a decision stages in shared memory (1024), so a warp merges
+    each row's pairs from global memory. With counts, only the rows a
+    request verifies."""
+    R, L, V = 2, 18, 600000
+    d = draw(R, L, V, "bf16", seed=85, boost=True)  # request 0 keeps 13 guesses
+    ng = np.array([9, L], np.int32) if counts else None  # request 0's bonus: row 9
+    ctx = chain_ctx(R, L, V, True, True)
+    g_len, g_tok, st = run_gpu(ctx, d["draft"], d["target"], d["tokens"], d["u"], d["r"],
+                               n_guess=ng)
+    assert st == 0
+    o_len, o_tok = run_oracle(d["draft"], d["target"], d["tokens"], d["u"], d["r"], n_guess=ng)
+    compare(g_len, g_tok, o_len, o_tok, d["draft"], d["target"], d["tokens"], d["u"], d["r"], ng)
