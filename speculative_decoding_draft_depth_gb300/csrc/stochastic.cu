@@ -6,16 +6,22 @@
 // guess survives, a bonus token is drawn from p_L. The uniforms are inputs:
 // u[k] decides guess k (kept iff u[k] < min(1, p/q)); r draws by inverse CDF
 // over the vocabulary in index order (the first index whose running sum of
-// weights exceeds r times their total).
+// weights exceeds r times their total). With per-request guess counts (the
+// prefix a scheduler kept), request i verifies only its first n_i guesses;
+// when all of them survive, the bonus comes from p_{n_i}.
 //
 // Design (HBM-bound: every logit is read once, the drawn row once more):
 //  * sv_rows_kernel: one CTA per (request, row, chunk of 32 KB); each
 //    thread keeps 8 vectors of 16 bytes in registers and the CTA reduces
 //    them to the chunk's (max, sum of exp), stores the pair and exits.
+//  * sv_rows_counted_kernel (given guess counts): the same per-chunk work on
+//    a grid of a few waves, each CTA over a contiguous range of only the
+//    used rows' chunks (draft rows k < n_i, target rows k <= n_i).
 //  * sv_draw_kernel (a dependent launch): one CTA per (request, 8192 tokens
 //    of the drawn row). Every CTA of a request first takes the request's
-//    decisions itself -- the log-partitions of its 2L + 1 rows from the
-//    pairs (a warp per row), the guesses' log-probs, the L decisions in one
+//    decisions itself -- the log-partitions of its used rows from the
+//    pairs (staged in shared memory, or a warp per row when they do not
+//    fit), the guesses' log-probs, the n_i decisions in one
 //    warp (a ballot finds the first rejection k*) -- the same loads in the
 //    same order, so all agree; the request's first CTA writes the committed
 //    prefix and the length. Then each sums the draw's weights of its chunk
