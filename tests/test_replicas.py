@@ -40,7 +40,7 @@ def _rank_main(rank, world, port, out):
 
 def test_two_gloo_ranks_reduce_to_the_slowest_and_draw_their_own_inputs():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (threaded) process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, _free_port(), out), nprocs=world, join=True)
         res = dict(out)
