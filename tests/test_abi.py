@@ -38,6 +38,28 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(ddt.EXPORTS) <= set(_declared())
 
 
+def _declarations():
+    """name -> parameter count of every function include/ddt.h declares."""
+    src = open(os.path.join(ROOT, "include", "ddt.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    out = {}
+    for name, params in re.findall(r"\b(ddt_[a-z_]+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+        params = params.strip()
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header(lib):
+    """The ctypes binding passes as many arguments as each declaration takes
+    (a parameter added on one side only fails here, not on a GPU)."""
+    decl = _declarations()
+    assert set(ddt.EXPORTS) <= set(decl)
+    for name in ddt.EXPORTS:
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == decl[name], (name, len(fn.argtypes), decl[name])
+
+
 def _cfg(**kw):
     base = dict(R_max=64, L=15, V=151936, B=32, Hq=32, Hkv=8, d=128, page_size=16,
                 max_pages_per_req=1040, num_pages=40000)
