@@ -214,6 +214,9 @@ class Context:
 
     def ddt_accept_stochastic(self, draft_logits, target_logits, draft_tokens, u, r, R, acc_len,
                               acc_tokens, n_guess=None, stream=None):
+        """Temperature-1 verification of R drafted chains of L guesses.
+        n_guess: None (every guess), or an int32 [R] CUDA tensor of the
+        guesses each request verifies, e.g. ddt_schedule_prefix's n_keep."""
         _check(_lib.ddt_accept_stochastic(self._h, _ptr(draft_logits), _ptr(target_logits),
                                           _ptr(draft_tokens), _ptr(u), _ptr(r), R, _ptr(acc_len),
                                           _ptr(acc_tokens), _ptr(n_guess), _stream(stream)),
@@ -221,6 +224,9 @@ class Context:
 
     def ddt_schedule_prefix(self, conf, R, cost_ms, n_keep, n_total=None, stats=None,
                             stream=None):
+        """The guesses each of R requests verifies: conf [R, L] f32,
+        cost_ms [R*L + 1] f32, n_keep [R] i32 out; n_total [1] i32 and
+        stats [2] f64 (tokens per ms, expected tokens) optional."""
         _check(_lib.ddt_schedule_prefix(self._h, _ptr(conf), R, _ptr(cost_ms), _ptr(n_keep),
                                         _ptr(n_total), _ptr(stats), _stream(stream)),
                "ddt_schedule_prefix")
