@@ -103,6 +103,9 @@ def test_calls_reject_null_context(lib):
     assert lib.ddt_markov_table(None, None, None, None, None, 1, None, None, None) == ddt.EINVAL
     assert lib.ddt_build_tree_markov(None, None, None, 1, None, None, None, None, None,
                                      None) == ddt.EINVAL
+    assert lib.ddt_accept_stochastic(None, None, None, None, None, None, 1, None, None, None,
+                                     None) == ddt.EINVAL
+    assert lib.ddt_schedule_prefix(None, None, 1, None, None, None, None, None) == ddt.EINVAL
     assert lib.ddt_device_status(None, None) == ddt.EINVAL
 
 
