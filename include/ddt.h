@@ -380,10 +380,12 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
  * survivals' sum) / cost_ms[n] -- expected committed tokens per ms; the
  * smallest n wins a tie, and n = 0 when no cost is valid.
  * Outputs (device): n_keep [R] i32, the guesses request r verifies (always
- * a prefix of its block); n_total [1] i32 (may be NULL), the chosen n;
+ * a prefix of its block; it may be passed as ddt_accept_stochastic's n_guess
+ * without leaving the device); n_total [1] i32 (may be NULL), the chosen n;
  * stats [2] f64 (may be NULL): the best tokens per ms and the expected
  * committed tokens. Requires R * L <= DDT_SCHED_MAX_SLOTS (else
- * DDT_EUNSUPPORTED). One CTA is enqueued on `stream`. */
+ * DDT_EUNSUPPORTED). One kernel is enqueued on `stream`: a grid that counts
+ * every slot's rank, whose last CTA to finish picks the budget. */
 #define DDT_SCHED_MAX_SLOTS 8192
 ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const float *cost_ms,
                                int32_t *n_keep, int32_t *n_total, double *stats, void *stream);
