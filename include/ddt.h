@@ -384,8 +384,9 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
  * without leaving the device); n_total [1] i32 (may be NULL), the chosen n;
  * stats [2] f64 (may be NULL): the best tokens per ms and the expected
  * committed tokens. Requires R * L <= DDT_SCHED_MAX_SLOTS (else
- * DDT_EUNSUPPORTED). One kernel is enqueued on `stream`: a grid that counts
- * every slot's rank, whose last CTA to finish picks the budget. */
+ * DDT_EUNSUPPORTED). One kernel is enqueued on `stream`: while (R * L) * R
+ * <= 2^23, a grid that counts every slot's rank, whose last CTA to finish
+ * picks the budget; beyond that, one CTA that sorts the slots. */
 #define DDT_SCHED_MAX_SLOTS 8192
 ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const float *cost_ms,
                                int32_t *n_keep, int32_t *n_total, double *stats, void *stream);
