@@ -20,9 +20,11 @@
  *   ddt_markov_table / ddt_build_tree_markov / ddt_round_markov
  *       SparklingTree's top-C prefilter, Markov table and the heap over it
  *   ddt_accept_stochastic
- *       stochastic verification of drafted chains at temperature 1
+ *       stochastic verification of drafted chains at temperature 1, of
+ *       every guess or of a per-request prefix
  *   ddt_schedule_prefix
- *       the hardware-aware prefix scheduler (guesses to verify per request)
+ *       the hardware-aware prefix scheduler (guesses to verify per request;
+ *       its output is ddt_accept_stochastic's prefix lengths)
  *   ddt_topk_logprobs_noalloc
  *       a1 without a context
  *
