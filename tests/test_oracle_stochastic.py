@@ -108,6 +108,37 @@ def test_output_distribution_is_the_target():
         assert np.abs(dist - p).max() < 3.0 / N, (dist, p)
 
 
+def test_scheduled_prefix_output_follows_the_target():
+    """The rule's guarantee on a cut chain: with L = 3 guesses drafted but a
+    count of n = 1, the committed first token is distributed as target row 0,
+    and after a kept guess the bonus follows target row 1 (row n, not row L).
+    Every (guess, u, r) of a grid is one request; each weighs q_0(x) / N^2."""
+    rng = np.random.default_rng(6)
+    V, N, L = 6, 60, 3
+    p = rng.dirichlet(np.ones(V), size=L + 1)   # target rows 0..L
+    q = rng.dirichlet(np.ones(V), size=L)       # draft rows 0..L-1
+    grid = (np.arange(N) + 0.5) / N
+    x, ui, ri = np.meshgrid(np.arange(V), np.arange(N), np.arange(N), indexing="ij")
+    x, ui, ri = x.ravel(), ui.ravel(), ri.ravel()
+    R = x.size
+    draft = np.broadcast_to(np.log(q), (R, L, V)).astype(np.float64).copy()
+    target = np.broadcast_to(np.log(p), (R, L + 1, V)).astype(np.float64).copy()
+    tokens = np.zeros((R, L), np.int32)
+    tokens[:, 0] = x
+    u = np.zeros((R, L))
+    u[:, 0] = grid[ui]
+    acc_len, acc_tokens = oracle.accept_stochastic(draft, target, tokens, u, grid[ri],
+                                                   n_guess=np.ones(R, np.int32))
+    assert acc_len.max() == 2  # one guess verified, then the bonus
+    w = q[0][x] / (N * N)
+    first = np.bincount(acc_tokens[:, 0], weights=w, minlength=V)
+    assert np.abs(first - p[0]).max() < 3.0 / N, (first, p[0])
+    kept = acc_len == 2
+    bonus = np.bincount(acc_tokens[kept, 1], weights=w[kept], minlength=V) / w[kept].sum()
+    assert np.abs(bonus - p[1]).max() < 3.0 / N, (bonus, p[1])
+    assert np.abs(bonus - p[L]).max() > 6.0 / N  # row L would be told apart
+
+
 def test_toy_lossless_frequencies():
     vocab, big, (keep, spread), rows = _toy()
     V = len(vocab)
