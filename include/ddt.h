@@ -98,7 +98,8 @@ typedef enum ddt_dtype { DDT_BF16 = 0, DDT_F32 = 1 } ddt_dtype;
 typedef struct ddt_config {
     int32_t R_max;             /* most requests a call may carry (1..2048) */
     int32_t L;                 /* draft depths per request (1..18) */
-    int32_t V;                 /* vocabulary size */
+    int32_t V;                 /* vocabulary size (at most 64 chunks of a1: 1048576 bf16,
+                                  524288 fp32 draft logits) */
     int32_t B;                 /* non-root tree nodes (1..127) */
     int32_t K;                 /* per-depth top-K; 0 selects min(B, V) */
     int32_t Hq, Hkv, d;        /* attention heads and head dim (d = 128 or 64) */
@@ -408,25 +409,27 @@ ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);
  *
  * Same operation, layouts and kernel as ddt_topk_logprobs, for `rows`
  * independent rows of V logits (draft_logits [rows, V], draft_dtype BF16 or
- * F32; top_lp, top_ids [rows, K]). Its scratch (per-chunk partial lists,
- * arrival counters, a status word) is one fixed array in the library's
- * device memory, about 8.5 MB, which every GPU that loads libddt.so keeps
- * until the process exits. No call allocates or frees device memory.
+ * F32; top_lp, top_ids [rows, K]). Its scratch (each warp's (max, sum of
+ * exp), each 64-logit group's max, a status word) is one fixed array in the
+ * library's device memory, about 18 MB, which every GPU that loads libddt.so
+ * keeps until the process exits. No call allocates or frees device memory.
  *
  * Limits (DDT_EUNSUPPORTED beyond them, nothing enqueued), with
  * chunks = ceil(V / 16384) for bf16 and ceil(V / 8192) for fp32:
  *   rows <= DDT_NOALLOC_MAX_ROWS, rows * chunks <= DDT_NOALLOC_MAX_ROW_CHUNKS,
- *   rows * chunks * K <= DDT_NOALLOC_MAX_ENTRIES, chunks * K <= 2048,
- *   1 <= K <= min(127, V). Bad pointers or dtype: DDT_EINVAL.
- * Set-up: the first call on each device looks up the array's device address
- * (with that device current); make that first call before any stream
- * capture. Every call clears the counters it needs on `stream` first, but
- * all calls share the one array: calls that can overlap on the GPU (other
- * streams, other threads) race and corrupt each other's results. NaN logits
- * are not reported by this entry point. */
+ *   chunks * K <= 2048, chunks <= 64, 1 <= K <= min(127, V). Bad pointers or
+ *   dtype: DDT_EINVAL.
+ * Set-up: every call looks up the array's device address in the calling
+ * thread's current CUDA context, so any context works (the primary one, one
+ * made with cuCtxCreate, a new one after a device reset). The first call in
+ * a context may load the library's module into it, which is not allowed
+ * while a stream is being captured: make that first call before any
+ * capture. Every call writes the scratch it reads (on `stream`) before
+ * reading it, but all calls share the one array: calls that can overlap on
+ * the GPU (other streams, other threads) race and corrupt each other's
+ * results. NaN logits are not reported by this entry point. */
 #define DDT_NOALLOC_MAX_ROWS 4096
-#define DDT_NOALLOC_MAX_ROW_CHUNKS 65536
-#define DDT_NOALLOC_MAX_ENTRIES 1048576
+#define DDT_NOALLOC_MAX_ROW_CHUNKS 32768
 ddt_status ddt_topk_logprobs_noalloc(const void *draft_logits, int32_t draft_dtype, int32_t rows,
                                      int32_t V, int32_t K, float *top_lp, int32_t *top_ids,
                                      void *stream);

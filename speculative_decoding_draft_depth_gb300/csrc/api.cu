@@ -43,7 +43,7 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
     if (c.Hkv > 255)
         return DDT_EUNSUPPORTED;
     const int nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
-    if ((int64_t)nch * c.K > TOPK_CAND_CAP)
+    if ((int64_t)nch * c.K > TOPK_CAND_CAP || nch > TOPK_MAX_CHUNKS)
         return DDT_EUNSUPPORTED;
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
     if (max_ctx > (int64_t)64 * ATT_CHUNK || c.R_max > 2048)
@@ -65,7 +65,7 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 }
 
 struct Layout {
-    size_t status, tk_val, tk_idx, tk_ms, tk_cnt, am_val, am_idx, att_items, att_meta, att_rg_cnt,
+    size_t status, tk_gkey, tk_wtop, tk_ms, am_val, am_idx, att_items, att_meta, att_rg_cnt,
         att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
         cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
         sv_part_d, sv_part_t, sv_cnt, sv_part_w, ps_rk, ps_rid, ps_arrive, total;
@@ -101,10 +101,10 @@ Layout layout_for(const ddt_config &c)
         return at;
     };
     L.status = take(sizeof(int32_t));
-    L.tk_val = take(rows_d * L.tk_nch * c.K * sizeof(float));
-    L.tk_idx = take(rows_d * L.tk_nch * c.K * sizeof(int32_t));
-    L.tk_ms = take(rows_d * L.tk_nch * sizeof(float2));
-    L.tk_cnt = take(rows_d * sizeof(unsigned));
+    L.tk_gkey = take(rows_d * L.tk_nch * TOPK_THREADS * sizeof(uint16_t));
+    L.tk_wtop = take(rows_d * L.tk_nch * (TOPK_THREADS / 32) * topk_warp_keys(L.tk_nch, c.K) *
+                     sizeof(uint16_t));
+    L.tk_ms = take(rows_d * L.tk_nch * (TOPK_THREADS / 32) * sizeof(float2));
     L.am_val = take(rows_t * L.am_nch * sizeof(float));
     L.am_idx = take(rows_t * L.am_nch * sizeof(int32_t));
     L.att_items = take((size_t)L.max_items * sizeof(int4));
@@ -282,10 +282,9 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     char *w = ctx->ws;
     ctx->status = (int32_t *)(w + L.status);
     ctx->tk_nch = L.tk_nch;
-    ctx->tk_val = (float *)(w + L.tk_val);
-    ctx->tk_idx = (int32_t *)(w + L.tk_idx);
+    ctx->tk_gkey = (uint16_t *)(w + L.tk_gkey);
+    ctx->tk_wtop = (uint16_t *)(w + L.tk_wtop);
     ctx->tk_ms = (float2 *)(w + L.tk_ms);
-    ctx->tk_cnt = (unsigned *)(w + L.tk_cnt);
     ctx->am_nch = L.am_nch;
     ctx->am_val = (float *)(w + L.am_val);
     ctx->am_idx = (int32_t *)(w + L.am_idx);

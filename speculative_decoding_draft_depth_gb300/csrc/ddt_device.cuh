@@ -69,6 +69,13 @@ DDT_DEVINL uint4 ldg_stream(const void *p)
     return v;
 }
 
+// ask the copy engine to bring [p, p + bytes) into L2 (p 16-byte aligned,
+// bytes a multiple of 16); nothing waits for it
+DDT_DEVINL void prefetch_l2(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 DDT_DEVINL void set_status(int32_t *status, int bits)
 {
     atomicOr(status, bits);

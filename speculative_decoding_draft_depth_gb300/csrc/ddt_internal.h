@@ -13,10 +13,13 @@ constexpr int DDT_MAX_K = 127;   // rank + 1 must fit a 7-bit field
 constexpr int DDT_MAX_B = 127;   // frontier of <= B entries in 4 slots per lane
 constexpr int DDT_MAX_P = 128;   // tree positions (B + 1)
 
-// a1: one CTA of TOPK_THREADS reads one chunk of a row
+// a1: one CTA of TOPK_THREADS reads one chunk of TOPK_THREADS *
+// TOPK_VEC_PER_THREAD 16-byte vectors of a row
 constexpr int TOPK_THREADS = 256;
-constexpr int TOPK_VEC_PER_THREAD = 8;   // 16-byte vectors per thread per chunk
-constexpr int TOPK_CAND_CAP = 2048;      // candidate buffer entries
+constexpr int TOPK_VEC_PER_THREAD = 8;   // 16-byte vectors per thread (one group)
+constexpr int TOPK_CTAS_PER_SM = 5;
+constexpr int TOPK_MAX_CHUNKS = 64;      // a row's group keys fit 32 KB of shared memory
+constexpr int TOPK_CAND_CAP = 2048;      // limit on chunks x K per row
 
 // a5: same chunking as a1
 constexpr int AMAX_THREADS = 256;
@@ -46,10 +49,9 @@ struct ddt_ctx {
     int32_t *status;         // device status word
     // a1 partials
     int tk_nch;              // chunks per row
-    float *tk_val;           // [R_max * L, nch, K]
-    int32_t *tk_idx;         // [R_max * L, nch, K]
-    float2 *tk_ms;           // [R_max * L, nch] (max, sum of exp)
-    unsigned *tk_cnt;        // [R_max * L] arrival counters (self-resetting)
+    uint16_t *tk_gkey;       // [R_max * L, nch * TOPK_THREADS] each group's max (ordered key)
+    uint16_t *tk_wtop;       // [R_max * L, nch * TOPK_THREADS / 32, Q] each warp's Q largest keys
+    float2 *tk_ms;           // [R_max * L, nch * TOPK_THREADS / 32] each warp's (max, sum of exp)
     // a5 partials
     int am_nch;
     float *am_val;           // [R_max * P, nch]
@@ -159,9 +161,10 @@ cudaError_t launch_schedule_prefix(const ddt_ctx *c, const float *conf, int R, c
 
 // a1 with caller-supplied scratch (used by the allocation-free entry point)
 cudaError_t launch_topk_scratch(const void *z, int dtype, int rows, int V, int K, int nch,
-                                float *part_val, int32_t *part_idx, float2 *part_ms,
-                                unsigned *cnt, float *top_lp, int32_t *top_ids, int32_t *status,
-                                cudaStream_t s);
+                                int num_sms, uint16_t *gkey, uint16_t *wtop, float2 *part_ms,
+                                float *top_lp, int32_t *top_ids, int32_t *status, cudaStream_t s);
+// keys each warp of a1 keeps for the row threshold (Q)
+int topk_warp_keys(int nch, int K);
 
 // records the CUDA error reported by ddt_last_cuda_error (this thread)
 void ddt_note_cuda_error(int e);

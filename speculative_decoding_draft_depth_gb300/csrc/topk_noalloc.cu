@@ -5,32 +5,35 @@
 // The array below is part of this library's device image: every GPU that
 // loads libddt.so holds it until the process exits. Host code never uses its
 // name as a pointer (on the host it is only a stand-in for the symbol); the
-// device address comes from cudaGetSymbolAddress, looked up once per device
-// with that device current, and is passed to the kernel.
-#include <mutex>
+// device address comes from cudaGetSymbolAddress, looked up on every call in
+// the calling thread's current context, and is passed to the kernel. A
+// lookup per call keeps the address right for whatever context is current
+// (the primary context, one made with cuCtxCreate, or a new context after a
+// device reset); once the library's module is loaded in that context the
+// lookup is a table read.
 #include <stdint.h>
 
 #include "ddt_internal.h"
 
 namespace {
 
-// scratch layout (byte offsets, each 256-aligned)
+// scratch layout (byte offsets, each 256-aligned): the status word, per
+// (row, chunk) each warp's (max, sum of exp), per row group its max as a
+// 16-bit ordered key, and per warp its Q largest keys. With Q as a1 picks it,
+// a row's warps keep at most 32 * chunks + 2K + 16 * chunks keys.
 constexpr size_t NA_STATUS = 0;
-constexpr size_t NA_CNT = 256;
-constexpr size_t NA_MS = NA_CNT + sizeof(unsigned) * DDT_NOALLOC_MAX_ROWS;
-constexpr size_t NA_VAL = NA_MS + sizeof(float2) * DDT_NOALLOC_MAX_ROW_CHUNKS;
-constexpr size_t NA_IDX = NA_VAL + sizeof(float) * DDT_NOALLOC_MAX_ENTRIES;
-constexpr size_t NA_BYTES = NA_IDX + sizeof(int32_t) * DDT_NOALLOC_MAX_ENTRIES;
-static_assert(NA_MS % 256 == 0 && NA_VAL % 256 == 0 && NA_IDX % 256 == 0, "alignment");
-
-constexpr int NA_MAX_DEVICES = 64;
-
-std::mutex g_mu;
-unsigned char *g_base[NA_MAX_DEVICES];  // device address per device, once looked up
+constexpr size_t NA_MS = 256;
+constexpr size_t NA_GKEY =
+    NA_MS + sizeof(float2) * (TOPK_THREADS / 32) * DDT_NOALLOC_MAX_ROW_CHUNKS;
+constexpr size_t NA_WTOP = NA_GKEY + sizeof(uint16_t) * TOPK_THREADS * DDT_NOALLOC_MAX_ROW_CHUNKS;
+constexpr size_t NA_WTOP_KEYS =
+    48 * (size_t)DDT_NOALLOC_MAX_ROW_CHUNKS + 2 * (size_t)DDT_MAX_K * DDT_NOALLOC_MAX_ROWS;
+constexpr size_t NA_BYTES = NA_WTOP + sizeof(uint16_t) * NA_WTOP_KEYS;
+static_assert(NA_MS % 256 == 0 && NA_GKEY % 256 == 0 && NA_WTOP % 256 == 0, "alignment");
 
 }  // namespace
 
-// the scratch itself: file scope, fixed size (about 8.5 MB)
+// the scratch itself: file scope, fixed size (about 22 MB)
 static __device__ __align__(256) unsigned char g_topk_scratch[NA_BYTES];
 
 extern "C" ddt_status ddt_topk_logprobs_noalloc(const void *draft_logits, int32_t draft_dtype,
@@ -50,46 +53,39 @@ extern "C" ddt_status ddt_topk_logprobs_noalloc(const void *draft_logits, int32_
         return DDT_EINVAL;
     const int chunk = topk_chunk_elems(draft_dtype);
     const int64_t nch = ((int64_t)V + chunk - 1) / chunk;
-    if (K > DDT_MAX_K || nch * K > TOPK_CAND_CAP || rows > DDT_NOALLOC_MAX_ROWS ||
-        (int64_t)rows * nch > DDT_NOALLOC_MAX_ROW_CHUNKS ||
-        (int64_t)rows * nch * K > DDT_NOALLOC_MAX_ENTRIES)
+    if (K > DDT_MAX_K || nch * K > TOPK_CAND_CAP || nch > TOPK_MAX_CHUNKS ||
+        rows > DDT_NOALLOC_MAX_ROWS ||
+        (int64_t)rows * nch > DDT_NOALLOC_MAX_ROW_CHUNKS)
         return DDT_EUNSUPPORTED;
 
-    // ---- once per device: the array's device address, with that device current
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
+    // ---- the array's device address in the current context (the first call
+    // in a context may load the library's module there, which stream capture
+    // does not allow: make that call before any capture)
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_topk_scratch);
     if (e != cudaSuccess) {
         ddt_note_cuda_error((int)e);
         return DDT_ECUDA;
     }
-    if (dev < 0 || dev >= NA_MAX_DEVICES)
-        return DDT_EUNSUPPORTED;
-    unsigned char *base;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (g_base[dev] == nullptr) {
-            void *p = nullptr;
-            e = cudaGetSymbolAddress(&p, g_topk_scratch);
-            if (e != cudaSuccess) {
-                ddt_note_cuda_error((int)e);
-                return DDT_ECUDA;
-            }
-            g_base[dev] = (unsigned char *)p;
-        }
-        base = g_base[dev];
+    unsigned char *base = (unsigned char *)p;
+    int dev = 0, num_sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) {
+        ddt_note_cuda_error((int)e);
+        return DDT_ECUDA;
     }
 
-    // ---- the array keeps the previous call's contents: zero the arrival
-    // counters and the status word this call relies on
+    // ---- the array keeps the previous call's contents: every slot this call
+    // reads is written by this call first, except the status word, cleared here
     cudaStream_t s = (cudaStream_t)stream;
-    e = cudaMemsetAsync(base + NA_CNT, 0, sizeof(unsigned) * (size_t)rows, s);
+    e = cudaMemsetAsync(base + NA_STATUS, 0, sizeof(int32_t), s);
     if (e == cudaSuccess)
-        e = cudaMemsetAsync(base + NA_STATUS, 0, sizeof(int32_t), s);
-    if (e == cudaSuccess)
-        e = launch_topk_scratch(draft_logits, draft_dtype, rows, V, K, (int)nch,
-                                (float *)(base + NA_VAL), (int32_t *)(base + NA_IDX),
-                                (float2 *)(base + NA_MS), (unsigned *)(base + NA_CNT), top_lp,
-                                top_ids, (int32_t *)(base + NA_STATUS), s);
+        e = launch_topk_scratch(draft_logits, draft_dtype, rows, V, K, (int)nch, num_sms,
+                                (uint16_t *)(base + NA_GKEY), (uint16_t *)(base + NA_WTOP),
+                                (float2 *)(base + NA_MS), top_lp, top_ids,
+                                (int32_t *)(base + NA_STATUS), s);
     if (e != cudaSuccess) {
         ddt_note_cuda_error((int)e);
         return DDT_ECUDA;

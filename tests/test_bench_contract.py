@@ -28,3 +28,8 @@ def test_reference_arm_prints_the_contract_line(capsys):
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # a step is one whole round: the value is the inverse of the step time
+    assert abs(d["value"] - 1000.0 / d["ms_per_step"]) <= 1e-3 * d["value"] + 1e-4
+    # the same config keys as the GPU arm
+    assert d["config"] == bench.config_dict(synth.config("tiny"), 0) | {"l2": d["config"]["l2"]}
+    assert set(d["config"]) == {"workload", "l2", "parallelism"}

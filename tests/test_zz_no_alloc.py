@@ -2,8 +2,8 @@
 allocate device memory (its scratch is a fixed array inside libddt.so).
 
 It must give the same result as the context-based ddt_topk_logprobs, call
-after call, although every call reuses the same scratch. The file's name
-makes pytest collect it last.
+after call, although every call reuses the same scratch, and the same ids
+and log-probs as the oracle. The file's name makes pytest collect it last.
 """
 import ctypes
 
@@ -11,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from gpu_helpers import dev, host
 from speculative_decoding_draft_depth_gb300 import ddt, synth
 
@@ -67,6 +68,56 @@ def test_noalloc_matches_context_entry_point_on_consecutive_calls(name, override
         assert np.abs(lp - ref_lp).max() <= LP_TOL
 
 
+def test_noalloc_matches_oracle():
+    cfg = synth.config("batch64", R=2, seed=73)
+    inp = synth.draw_round_inputs(cfg)
+    rows = cfg.R * cfg.L
+    lp, ids = _call_noalloc(dev(inp["draft_logits"]), ddt.BF16, rows, cfg.V, cfg.K)
+    o_lp, o_ids, _, _ = oracle.topk_logprobs(inp["draft_logits"], cfg.K)
+    np.testing.assert_array_equal(ids, o_ids.reshape(rows, cfg.K))
+    assert np.abs(lp - o_lp.reshape(rows, cfg.K)).max() <= LP_TOL
+
+
+def test_noalloc_wide_list_merge():
+    # K = 64: more candidates than one warp holds in the row selection
+    cfg = synth.config("wide256", R=2, seed=74)
+    assert cfg.K == 64
+    inp = synth.draw_round_inputs(cfg)
+    z = dev(inp["draft_logits"])
+    rows = cfg.R * cfg.L
+    lp, ids = _call_noalloc(z, ddt.BF16, rows, cfg.V, cfg.K)
+    ref_lp, ref_ids = _call_context(z, ddt.BF16, cfg.R, cfg.L, cfg.V, cfg.K)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert np.abs(lp - ref_lp).max() <= LP_TOL
+
+
+def test_noalloc_smaller_call_after_larger_one():
+    # the second call must ignore the partial lists and counters the first left
+    cfg = synth.config("batch64", R=8, seed=75)
+    inp = synth.draw_round_inputs(cfg)
+    z = dev(inp["draft_logits"])
+    rows = cfg.R * cfg.L
+    _call_noalloc(z, ddt.BF16, rows, cfg.V, cfg.K)
+    small = dev(synth.draw_round_inputs(synth.config("batch64", R=1, seed=76))["draft_logits"])
+    lp, ids = _call_noalloc(small, ddt.BF16, cfg.L, cfg.V, cfg.K)
+    ref_lp, ref_ids = _call_context(small, ddt.BF16, 1, cfg.L, cfg.V, cfg.K)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert np.abs(lp - ref_lp).max() <= LP_TOL
+
+
+def test_noalloc_at_its_scratch_limit():
+    # rows * chunks exactly DDT_NOALLOC_MAX_ROW_CHUNKS: 4096 rows of 131072
+    # bf16 logits (8 chunks) and K = 32; seeded N(0, 3^2) logits
+    rows, V, K = 4096, 131072, 32
+    g = torch.Generator(device="cuda").manual_seed(77)
+    z = (torch.randn((rows, V), generator=g, device="cuda") * 3).to(torch.bfloat16)
+    z16 = z.view(torch.int16)
+    lp, ids = _call_noalloc(z16, ddt.BF16, rows, V, K)
+    ref_lp, ref_ids = _call_context(z16, ddt.BF16, 2048, 2, V, K)
+    np.testing.assert_array_equal(ids, ref_ids)
+    assert np.abs(lp - ref_lp).max() <= LP_TOL
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     z = torch.zeros((16,), dtype=torch.int16, device="cuda")
     out = torch.zeros((16,), dtype=torch.int32, device="cuda")
@@ -74,7 +125,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
     # more rows than the scratch holds
     assert fn(p(z), ddt.BF16, 4097, 8, 4, p(out), p(out), None) == ddt.EUNSUPPORTED
-    # rows * chunks * K above the entry budget: 4096 rows x 10 chunks x 32
+    # rows * chunks above the scratch: 4096 rows x 10 chunks, and 4096 x 9
     assert fn(p(z), ddt.BF16, 4096, 151936, 32, p(out), p(out), None) == ddt.EUNSUPPORTED
+    assert fn(p(z), ddt.BF16, 4096, 131073, 32, p(out), p(out), None) == ddt.EUNSUPPORTED
     assert fn(p(z), ddt.BF16, 1, 8, 9, p(out), p(out), None) == ddt.EINVAL  # K > V
     assert fn(p(z), 5, 1, 8, 4, p(out), p(out), None) == ddt.EINVAL  # unknown dtype
