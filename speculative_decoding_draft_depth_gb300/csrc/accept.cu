@@ -201,7 +201,8 @@ walk_compact_kernel(const int32_t *__restrict__ argmax, const float *__restrict_
                     int do_compact, uint16_t *__restrict__ k_cache, uint16_t *__restrict__ v_cache,
                     const int32_t *__restrict__ block_table, int max_pages, int64_t num_pages,
                     int page, int32_t *__restrict__ ctx_lens, const uint16_t *__restrict__ k_tree,
-                    const uint16_t *__restrict__ v_tree, int rowlen, int32_t *__restrict__ status)
+                    const uint16_t *__restrict__ v_tree, int rowlen, int advance_ctx,
+                    int32_t *__restrict__ status)
 {
     const int r = blockIdx.x, tid = threadIdx.x;
     const int P = B + 1;
@@ -318,8 +319,18 @@ walk_compact_kernel(const int32_t *__restrict__ argmax, const float *__restrict_
         }
     }
     __syncthreads();
-    if (tid == 0)
+    if (tid == 0 && advance_ctx)
         ctx_lens[r] = ctx + nacc + 1;
+}
+
+// the context lengths after compaction: ctx_lens[r] += acc_len[r] (the root
+// and the accepted nodes were copied to slots ctx .. ctx + acc_len - 1)
+__global__ void ctx_advance_kernel(int32_t *__restrict__ ctx_lens,
+                                   const int32_t *__restrict__ acc_len, int R)
+{
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r < R)
+        ctx_lens[r] += acc_len[r];
 }
 
 }  // namespace
@@ -365,13 +376,21 @@ cudaError_t launch_walk_compact(const ddt_ctx *c, const int32_t *argmax, bool ar
                                 int32_t *acc_len, int32_t *acc_nodes, int32_t *acc_tokens,
                                 int32_t *bonus, bool do_walk, bool do_compact, uint16_t *k_cache,
                                 uint16_t *v_cache, const int32_t *block_table, int32_t *ctx_lens,
-                                const uint16_t *k_tree, const uint16_t *v_tree, cudaStream_t s)
+                                const uint16_t *k_tree, const uint16_t *v_tree, bool advance_ctx,
+                                cudaStream_t s)
 {
     const ddt_config &cfg = c->cfg;
     walk_compact_kernel<<<R, 128, 0, s>>>(
         argmax_from_partials ? nullptr : argmax, c->am_val, c->am_idx, c->am_nch, argmax_out,
         tree_tokens, parents, n_nodes, cfg.B, cfg.L, acc_len, acc_nodes, acc_tokens, bonus,
         do_walk ? 1 : 0, do_compact ? 1 : 0, k_cache, v_cache, block_table, cfg.max_pages_per_req,
-        cfg.num_pages, cfg.page_size, ctx_lens, k_tree, v_tree, cfg.Hkv * cfg.d, c->status);
+        cfg.num_pages, cfg.page_size, ctx_lens, k_tree, v_tree, cfg.Hkv * cfg.d,
+        advance_ctx ? 1 : 0, c->status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ctx_advance(int R, int32_t *ctx_lens, const int32_t *acc_len, cudaStream_t s)
+{
+    ctx_advance_kernel<<<(R + 127) / 128, 128, 0, s>>>(ctx_lens, acc_len, R);
     return cudaGetLastError();
 }

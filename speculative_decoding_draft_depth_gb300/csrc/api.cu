@@ -336,7 +336,11 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
         e = cudaEventCreateWithFlags(&ctx->ev_tree, cudaEventDisableTiming);
     if (e == cudaSuccess)
         e = cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming);
+    if (e == cudaSuccess)
+        e = cudaEventCreateWithFlags(&ctx->ev_walk, cudaEventDisableTiming);
     if (e != cudaSuccess) {
+        if (ctx->ev_join)
+            cudaEventDestroy(ctx->ev_join);
         if (ctx->ev_tree)
             cudaEventDestroy(ctx->ev_tree);
         if (ctx->ev_fork)
@@ -362,6 +366,7 @@ void ddt_destroy(ddt_ctx *ctx)
     cudaSetDevice(ctx->device);
     cudaStreamSynchronize(ctx->side);
     cudaStreamSynchronize(ctx->hi);
+    cudaEventDestroy(ctx->ev_walk);
     cudaEventDestroy(ctx->ev_join);
     cudaEventDestroy(ctx->ev_tree);
     cudaEventDestroy(ctx->ev_fork);
@@ -509,7 +514,8 @@ ddt_status ddt_walk(ddt_ctx *ctx, const int32_t *argmax, const int32_t *tree_tok
         return st;
     DDT_TRY(launch_walk_compact(ctx, argmax, false, nullptr, tree_tokens, parents, n_nodes, R,
                                 acc_len, acc_nodes, acc_tokens, bonus, true, false, nullptr,
-                                nullptr, nullptr, nullptr, nullptr, nullptr, (cudaStream_t)stream));
+                                nullptr, nullptr, nullptr, nullptr, nullptr, false,
+                                (cudaStream_t)stream));
     return DDT_OK;
 }
 
@@ -531,7 +537,7 @@ ddt_status ddt_compact(ddt_ctx *ctx, uint16_t *k_cache, uint16_t *v_cache,
     DDT_TRY(launch_walk_compact(ctx, nullptr, false, nullptr, nullptr, nullptr, nullptr, R,
                                 const_cast<int32_t *>(acc_len), const_cast<int32_t *>(acc_nodes),
                                 nullptr, nullptr, false, true, k_cache, v_cache, block_table,
-                                ctx_lens, k_tree, v_tree, (cudaStream_t)stream));
+                                ctx_lens, k_tree, v_tree, true, (cudaStream_t)stream));
     return DDT_OK;
 }
 
@@ -559,7 +565,7 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
     DDT_TRY(launch_argmax_partials(ctx, target_logits, R, s));
     DDT_TRY(launch_walk_compact(ctx, nullptr, true, argmax_out, tree_tokens, parents, n_nodes, R,
                                 acc_len, acc_nodes, acc_tokens, bonus, true, true, k_cache, v_cache,
-                                block_table, ctx_lens, k_tree, v_tree, s));
+                                block_table, ctx_lens, k_tree, v_tree, true, s));
     return DDT_OK;
 }
 
@@ -601,7 +607,10 @@ ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const
     return DDT_OK;
 }
 
-// a4 once the tree (ev_tree) and a5 (ev_join) are done, then a6/a7, on `s`
+// a4 on `s` once the tree (ev_tree) and a5 (ev_join) are done; beside it, on
+// the side stream, a6 and a7's row copies (they need a5 and the tree; the
+// rows they write lie past each request's context, which a4 reads only
+// masked); the context lengths advance on `s` after both, since a4 reads them
 static ddt_status round_verify(ddt_ctx *ctx, const ddt_round_args *a, cudaStream_t s)
 {
     const int32_t R = a->R;
@@ -613,10 +622,14 @@ static ddt_status round_verify(ddt_ctx *ctx, const ddt_round_args *a, cudaStream
                              a->block_table, a->ctx_lens, a->mask, R, a->attn_out, s));
     if (a->att_event_end)
         DDT_TRY(cudaEventRecord((cudaEvent_t)a->att_event_end, s));
+    DDT_TRY(cudaStreamWaitEvent(ctx->side, ctx->ev_tree, 0));
     DDT_TRY(launch_walk_compact(ctx, nullptr, true, a->target_argmax, a->tree_tokens, a->parents,
                                 a->n_nodes, R, a->acc_len, a->acc_nodes, a->acc_tokens, a->bonus,
                                 true, true, a->k_cache, a->v_cache, a->block_table, a->ctx_lens,
-                                a->k_tree, a->v_tree, s));
+                                a->k_tree, a->v_tree, false, ctx->side));
+    DDT_TRY(cudaEventRecord(ctx->ev_walk, ctx->side));
+    DDT_TRY(cudaStreamWaitEvent(s, ctx->ev_walk, 0));
+    DDT_TRY(launch_ctx_advance(R, a->ctx_lens, a->acc_len, s));
     return DDT_OK;
 }
 

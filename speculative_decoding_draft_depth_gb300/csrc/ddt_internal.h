@@ -45,7 +45,7 @@ struct ddt_ctx {
     char *ws;                // one allocation, carved below
     cudaStream_t hi;         // ddt_round: a1..a3 on a highest-priority stream,
     cudaStream_t side;       //   a5 beside them on a lowest-priority one
-    cudaEvent_t ev_fork, ev_tree, ev_join;
+    cudaEvent_t ev_fork, ev_tree, ev_join, ev_walk;
     int32_t *status;         // device status word
     // a1 partials
     int tk_nch;              // chunks per row
@@ -109,7 +109,9 @@ cudaError_t launch_walk_compact(const ddt_ctx *c, const int32_t *argmax, bool ar
                                 int32_t *acc_len, int32_t *acc_nodes, int32_t *acc_tokens,
                                 int32_t *bonus, bool do_walk, bool do_compact, uint16_t *k_cache,
                                 uint16_t *v_cache, const int32_t *block_table, int32_t *ctx_lens,
-                                const uint16_t *k_tree, const uint16_t *v_tree, cudaStream_t s);
+                                const uint16_t *k_tree, const uint16_t *v_tree, bool advance_ctx,
+                                cudaStream_t s);
+cudaError_t launch_ctx_advance(int R, int32_t *ctx_lens, const int32_t *acc_len, cudaStream_t s);
 cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                              const uint16_t *v_tree, const uint16_t *k_cache,
                              const uint16_t *v_cache, const int32_t *block_table,
