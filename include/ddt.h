@@ -102,8 +102,9 @@ typedef struct ddt_config {
                                   524288 fp32 draft logits) */
     int32_t B;                 /* non-root tree nodes (1..127) */
     int32_t K;                 /* per-depth top-K; 0 selects min(B, V) */
-    int32_t Hq, Hkv, d;        /* attention heads and head dim (d = 128 or 64) */
-    int32_t page_size;         /* tokens per KV page (multiple of 16 for a4) */
+    int32_t Hq, Hkv, d;        /* attention heads and head dim (d = 128 or 64); a4 needs
+                                  Hq / Hkv in {1, 2, 4, 8, 16} */
+    int32_t page_size;         /* tokens per KV page: a power of two, at least 16 */
     int32_t max_pages_per_req; /* row length of block_table */
     int64_t num_pages;         /* pages in the KV pool (bounds checks) */
     int32_t draft_dtype;       /* ddt_dtype of draft logits */
@@ -174,7 +175,11 @@ ddt_status ddt_build_mask(ddt_ctx *ctx, const int32_t *parents, const int32_t *n
  *   block_table     [R, max_pages_per_req] i32: page of token t is
  *                   block_table[r][t / page_size], row t % page_size
  *   ctx_lens        [R] i32, mask [R, P, W] u32
- * Page ids out of range set DDT_DEV_BAD_PAGE and are read as zeros. */
+ * Page ids out of range set DDT_DEV_BAD_PAGE and are read as zeros. One
+ * tcgen05 tensor-core kernel serves d = 64 and d = 128. Keys and values are
+ * read in blocks of 16 tokens, so the rows of a request's last page past
+ * ctx_lens are read and masked out: they must hold finite values (zeros, or
+ * earlier rounds' keys and values). */
 ddt_status ddt_tree_attention(ddt_ctx *ctx, const uint16_t *q, const uint16_t *k_tree,
                               const uint16_t *v_tree, const uint16_t *k_cache,
                               const uint16_t *v_cache, const int32_t *block_table,

@@ -40,13 +40,15 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
         return DDT_EUNSUPPORTED;
     if (c.d != 64 && c.d != 128)
         return DDT_EUNSUPPORTED;
+    if (!attention_tc_supported(c))
+        return DDT_EUNSUPPORTED;  // the tcgen05 attention kernel cannot take this shape
     if (c.Hkv > 255)
         return DDT_EUNSUPPORTED;
     const int nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
     if ((int64_t)nch * c.K > TOPK_CAND_CAP || nch > TOPK_MAX_CHUNKS)
         return DDT_EUNSUPPORTED;
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
-    if (max_ctx > (int64_t)64 * ATT_CHUNK || c.R_max > 2048)
+    if (max_ctx > ATT_MAX_CTX || c.R_max > 2048)
         return DDT_EUNSUPPORTED;
     if (c.markov_dim < 0 || c.frontier < 0 || c.prefilter < 0)
         return DDT_EINVAL;
@@ -65,11 +67,10 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
 }
 
 struct Layout {
-    size_t status, tk_gkey, tk_wtop, tk_ms, am_val, am_idx, att_items, att_meta, att_rg_cnt,
-        att_rg_base, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
+    size_t status, tk_gkey, tk_wtop, tk_ms, am_val, am_idx, att_part_o, att_part_ml, cg_part_ms, cg_part_top, cg_fr_tok, cg_fr_cand,
         cg_fr_n, cg_fr_S, cg_c_S, cg_c_meta, cg_thr, cg_seed_lp, cg_seed_ids, mk_cand, mk_tab,
         sv_part_d, sv_part_t, sv_cnt, sv_part_w, ps_rk, ps_rid, ps_arrive, total;
-    int tk_nch, am_nch, rowgroups, max_items, sv_nch_d, sv_nch_t, sv_nch_w;
+    int tk_nch, am_nch, max_items, sv_nch_d, sv_nch_t, sv_nch_w;
 };
 
 Layout layout_for(const ddt_config &c)
@@ -78,22 +79,8 @@ Layout layout_for(const ddt_config &c)
     const int P = c.B + 1, G = c.Hq / c.Hkv;
     L.tk_nch = (c.V + topk_chunk_elems(c.draft_dtype) - 1) / topk_chunk_elems(c.draft_dtype);
     L.am_nch = (c.V + amax_chunk_elems(c.target_dtype) - 1) / amax_chunk_elems(c.target_dtype);
-    L.rowgroups = (P * G + ATT_ROWS - 1) / ATT_ROWS;
-    if (c.d == 128) {  // the tensor-core kernel groups rows by 128 plus a short tail
-        int nm, tail, rg_tc;
-        attention_tc_rows(c, &nm, &tail, &rg_tc);
-        if (rg_tc > L.rowgroups)
-            L.rowgroups = rg_tc;
-    }
-    const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
-    const int ns_max = (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK) > 0
-                           ? (int)((max_ctx + ATT_CHUNK - 1) / ATT_CHUNK)
-                           : 1;
-    L.max_items = c.R_max * c.Hkv * L.rowgroups * ns_max;
-    if (c.d == 128 && L.max_items < 512)  // room for splitting a small batch across the SMs
-        L.max_items = 512;
+    L.max_items = 2 * ATT_MAX_CTAS;
     const size_t rows_d = (size_t)c.R_max * c.L, rows_t = (size_t)c.R_max * P;
-    const size_t rg = (size_t)c.R_max * c.Hkv * L.rowgroups;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t at = off;
@@ -107,10 +94,6 @@ Layout layout_for(const ddt_config &c)
     L.tk_ms = take(rows_d * L.tk_nch * (TOPK_THREADS / 32) * sizeof(float2));
     L.am_val = take(rows_t * L.am_nch * sizeof(float));
     L.am_idx = take(rows_t * L.am_nch * sizeof(int32_t));
-    L.att_items = take((size_t)L.max_items * sizeof(int4));
-    L.att_meta = take(4 * sizeof(int32_t));
-    L.att_rg_cnt = take(rg * sizeof(unsigned));
-    L.att_rg_base = take(rg * sizeof(int32_t));
     L.att_part_o = take((size_t)L.max_items * ATT_ROWS * c.d * sizeof(float));
     L.att_part_ml = take((size_t)L.max_items * ATT_ROWS * sizeof(float2));
     // parent-conditioned tree (sized for up to CG_GRID_MAX CTAs of its GEMM)
@@ -288,12 +271,7 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->am_nch = L.am_nch;
     ctx->am_val = (float *)(w + L.am_val);
     ctx->am_idx = (int32_t *)(w + L.am_idx);
-    ctx->att_rowgroups = L.rowgroups;
     ctx->att_max_items = L.max_items;
-    ctx->att_items = (int4 *)(w + L.att_items);
-    ctx->att_meta = (int32_t *)(w + L.att_meta);
-    ctx->att_rg_cnt = (unsigned *)(w + L.att_rg_cnt);
-    ctx->att_rg_base = (int32_t *)(w + L.att_rg_base);
     ctx->att_part_o = (float *)(w + L.att_part_o);
     ctx->att_part_ml = (float2 *)(w + L.att_part_ml);
     ctx->cg_grid = ctx->num_sms < CG_GRID_MAX ? ctx->num_sms : CG_GRID_MAX;
@@ -320,8 +298,6 @@ ddt_status ddt_create(const ddt_config *cfg, ddt_ctx **out)
     ctx->ps_rk = (uint64_t *)(w + L.ps_rk);
     ctx->ps_rid = (int32_t *)(w + L.ps_rid);
     ctx->ps_arrive = (unsigned *)(w + L.ps_arrive);
-    ctx->att_grid = ctx->num_sms;
-    ctx->att_use_tc = attention_tc_supported(c);
     // ddt_round's streams: a1..a3 at the highest priority, a5 at the lowest, so
     // that a5's CTAs only fill what a1..a3 leave idle
     int prio_least = 0, prio_greatest = 0;

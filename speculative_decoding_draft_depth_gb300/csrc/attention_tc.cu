@@ -1,10 +1,12 @@
 // attention_tc.cu -- a4 on the 5th-generation tensor cores (tcgen05 + TMEM
-// + TMA), for head dim 128.
+// + TMA), for head dims D = 128 and 64 (one kernel, D a template argument:
+// half the K-steps of Q K^T, N = D for P V, one 64-wide box per tile row).
 //
-// Same operation as attention.cu ("SparklingTree ...", Step 4 and the
-// verification discussion; "DDTree Explained ...", sections 5 and 8): every
-// tree query row attends to its request's cached context through the page
-// table plus the tree positions its ancestor mask allows.
+// "SparklingTree ...", Step 4 and the verification discussion; "DDTree
+// Explained ...", sections 5 and 8 (ancestor-only tree mask over a GQA target
+// with a custom attention mask): every tree query row attends to its
+// request's cached context through the page table plus the tree positions its
+// ancestor mask allows.
 //
 // Work split: for one KV head, every (request r, row group) pair is a run of
 // tiles (its ceil(ctx_r / 128) context tiles, then the tree tile); laid end to
@@ -113,7 +115,8 @@ constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16,
 
 constexpr uint32_t IDESC_QK = idesc_bf16(128, 128, false, false);
 constexpr uint32_t IDESC_QKT = idesc_bf16(128, 16, false, false);
-constexpr uint32_t IDESC_PV = idesc_bf16(128, 128, false, true);
+template <int D>
+constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
 constexpr uint32_t IDESC_PVT = idesc_bf16(128, 16, true, false);
 
 struct TcArgs {
@@ -272,19 +275,21 @@ DDT_DEVINL int group_row(const TcArgs &a, const Item &it, int j, int u)
     return it.r * a.P + 16 * u;  // the tree tile: rows of k_tree / v_tree
 }
 
-// whole loader warp: the 16 boxes of one K or V tile into dst, completing on fb;
-// z = group_row(...) of this lane, looked up before the wait for the slot so
-// that the page-table load overlaps it
+// whole loader warp: the 8 * D / 64 boxes of one K or V tile into dst,
+// completing on fb; z = group_row(...) of this lane, looked up before the wait
+// for the slot so that the page-table load overlaps it
+template <int D>
 DDT_DEVINL void load_tile(const Item &it, int j, int lane, int z, uint32_t dst,
                           const void *map_c, const void *map_t, uint32_t fb)
 {
     if (lane == 0)
-        mbar_arrive_expect_tx(fb, 32768u);
+        mbar_arrive_expect_tx(fb, 16384u * (D / 64));
     __syncwarp();
     if (lane < 8) {
         const void *m = (j < it.ntile_ctx) ? map_c : map_t;
         tma_load_3d(dst + lane * 2048, m, 0, it.g, z, fb);
-        tma_load_3d(dst + 16384 + lane * 2048, m, 64, it.g, z, fb);
+        if (D == 128)
+            tma_load_3d(dst + 16384 + lane * 2048, m, 64, it.g, z, fb);
     }
 }
 
@@ -309,7 +314,7 @@ DDT_DEVINL float exps32(const uint32_t *sv, float scale, float m, uint32_t *pw)
     return (r0 + r1) + (r2 + r3);
 }
 
-template <int TQ>
+template <int TQ, int D>
 __global__ void __launch_bounds__(NTHREADS, 1)
 att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qt,
               const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -482,14 +487,16 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 break;
             if (lane == 0) {
                 const uint32_t qb = sb + SM_Q + qs * QSLOT, fb = bar + B_QFULL + 8 * qs;
-                mbar_arrive_expect_tx(fb, 32768u + (it.has_tail ? 4096u : 0u));
+                mbar_arrive_expect_tx(fb, (16384u + (it.has_tail ? 2048u : 0u)) * (D / 64));
                 const int zq = it.r * a.P + it.rg * pos_per_main;
                 tma_load_3d(qb, &tm_q, 0, it.g * a.G, zq, fb);
-                tma_load_3d(qb + 16384, &tm_q, 64, it.g * a.G, zq, fb);
+                if (D == 128)
+                    tma_load_3d(qb + 16384, &tm_q, 64, it.g * a.G, zq, fb);
                 if (it.has_tail) {
                     const int zt = it.r * a.P + a.n_main * pos_per_main;
                     tma_load_3d(qb + 32768, &tm_qt, 0, it.g * a.G, zt, fb);
-                    tma_load_3d(qb + 34816, &tm_qt, 64, it.g * a.G, zt, fb);
+                    if (D == 128)
+                        tma_load_3d(qb + 34816, &tm_qt, 64, it.g * a.G, zt, fb);
                 }
             }
             for (int j = 0; j < it.ntiles; ++j, ++kn) {
@@ -500,7 +507,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                load_tile(it, j, lane, z, sb + SM_K + sl * 32768u, &tm_k, &tm_kt, bar + B_KFULL + 8 * sl);
+                load_tile<D>(it, j, lane, z, sb + SM_K + sl * 32768u, &tm_k, &tm_kt, bar + B_KFULL + 8 * sl);
             }
         }
         // wind down: the last K tiles this warp issued have landed
@@ -527,7 +534,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     ok = false;
                     break;
                 }
-                load_tile(it, j, lane, z, sb + SM_V + sl * 32768u, &tm_v, &tm_vt, bar + B_VFULL + 8 * sl);
+                load_tile<D>(it, j, lane, z, sb + SM_V + sl * 32768u, &tm_v, &tm_vt, bar + B_VFULL + 8 * sl);
             }
         }
         for (int m = vn - NVS; m < vn; ++m)
@@ -598,7 +605,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         const uint64_t dQ = dQ0 + qs * (QSLOT >> 4);
                         const uint32_t s_t = tmem + TM_S + 128u * sl;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
+                        for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
                             mma_bf16(s_t, dQ + off, dK + off, IDESC_QK, kk > 0 ? 1u : 0u);
                         }
@@ -607,7 +614,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             const uint32_t st_t = tmem + TM_ST + 16u * (qt_n & 1);
                             const uint64_t dQT = dQ + (32768u >> 4);
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
+                            for (int kk = 0; kk < D / 16; ++kk) {
                                 const uint32_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
                                 const uint32_t offq = ((kk >> 2) * 2048u + (kk & 3) * 32u) >> 4;
                                 mma_bf16(st_t, dK + off, dQT + offq, IDESC_QKT, kk > 0 ? 1u : 0u);
@@ -639,10 +646,12 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         for (int kt = 0; kt < 8; ++kt) {
                             const uint32_t acc = (pv_j > 0 || kt > 0) ? 1u : 0u;
                             mma_bf16_ts(tmem + TM_O, p_t + 32u * (kt >> 1) + 8u * (kt & 1),
-                                        dV + kt * (2048u >> 4), IDESC_PV, acc);
+                                        dV + kt * (2048u >> 4), IDESC_PV<D>, acc);
                         }
                         mma_commit(bar + B_ODONE);
                         if (pi.has_tail) {
+                            // O_t^T has M = 128 lanes; for D = 64 the upper 64 read the
+                            // stage's unused half (in bounds) and are never read back
                             const uint64_t dPT = dPT0 + (pt_n & 1) * (4096u >> 4);
 #pragma unroll
                             for (int kt = 0; kt < 8; ++kt) {
@@ -682,7 +691,8 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int qw = warp & 3, cq = warp >> 2;  // lane quarter, column quarter
         const int row = qw * 32 + lane;           // TMEM lane = main row
         const uint32_t lane_addr = (uint32_t)(qw * 32) << 16;
-        const uint32_t col0 = 32u * cq;
+        const uint32_t col0 = 32u * cq;       // this warp's S columns (tokens)
+        const uint32_t ocol0 = (D / 4) * cq;  // this warp's O columns (head dim)
         float *xmax = reinterpret_cast<float *>(sgen + SM_BAR + B_XMAX);
         float *xl = reinterpret_cast<float *>(sgen + SM_BAR + B_XL);
         int n = 0;
@@ -777,14 +787,14 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
+                    for (int c = 0; c < D / 64; ++c) {
                         uint32_t ov[16];
-                        tmem_ld16(tmem + lane_addr + TM_O + col0 + 16u * c, ov);
+                        tmem_ld16(tmem + lane_addr + TM_O + ocol0 + 16u * c, ov);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                        tmem_st16(tmem + lane_addr + TM_O + col0 + 16u * c, ov);
+                        tmem_st16(tmem + lane_addr + TM_O + ocol0 + 16u * c, ov);
                     }
                 }
                 // ---- P over this warp's own S columns
@@ -817,13 +827,13 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                                                    blockIdx.x / a.Hkv, gridDim.x / a.Hkv, it.g, a.Hkv);
             const int64_t item_row0 = (int64_t)nat * ATT_ROWS;
             const float inv = (lrow > 0.f) ? 1.f / lrow : 0.f;
-            float *dst = a.out + (((int64_t)it.r * a.P + pos) * a.Hq + it.g * a.G + hl) * 128 + col0;
-            float *pdst = a.part_o + (item_row0 + row) * 128 + col0;
+            float *dst = a.out + (((int64_t)it.r * a.P + pos) * a.Hq + it.g * a.G + hl) * D + ocol0;
+            float *pdst = a.part_o + (item_row0 + row) * D + ocol0;
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t ov[16];
                 if (it.ntiles > 0) {
-                    tmem_ld16(tmem + lane_addr + TM_O + col0 + 16u * c, ov);
+                    tmem_ld16(tmem + lane_addr + TM_O + ocol0 + 16u * c, ov);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -990,17 +1000,17 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
 #pragma unroll
             for (int q = 0; q < TQ; ++q) {
-                if (q >= tail)
+                if (q >= tail || row >= D)  // lanes past D hold no output (D = 64)
                     continue;
                 const float ltot = sb2[q] + sb2[16 + q] + sb2[32 + q] + sb2[48 + q];
                 const int tgr = a.n_main * TILE + q;
                 const int tpos = tgr >> a.g_shift, thl = tgr & (a.G - 1);
                 if (single) {
                     const float inv = (ltot > 0.f) ? 1.f / ltot : 0.f;
-                    a.out[(((int64_t)it.r * a.P + tpos) * a.Hq + it.g * a.G + thl) * 128 + row] =
+                    a.out[(((int64_t)it.r * a.P + tpos) * a.Hq + it.g * a.G + thl) * D + row] =
                         __uint_as_float(ov[q]) * inv;
                 } else {
-                    a.part_o[(item_row0 + TILE + q) * 128 + row] = __uint_as_float(ov[q]);
+                    a.part_o[(item_row0 + TILE + q) * D + row] = __uint_as_float(ov[q]);
                     if (row == 0)
                         a.part_ml[item_row0 + TILE + q] = make_float2(mt[q], ltot);
                 }
@@ -1026,6 +1036,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 constexpr int CB_THREADS = 512;
 constexpr int CB_SEGS = 16;  // segment weights held per combine pass
 
+template <int D>
 __global__ void __launch_bounds__(CB_THREADS)
 att_combine_kernel(const TcArgs a, int NG)
 {
@@ -1127,17 +1138,18 @@ att_combine_kernel(const TcArgs a, int NG)
         }
         __syncthreads();
         // every (row, 4 columns): independent float4 loads, several in flight
-        constexpr int PER = (ATT_ROWS * 32 + CB_THREADS - 1) / CB_THREADS;
+        constexpr int C4 = D / 4;  // float4 per row
+        constexpr int PER = (ATT_ROWS * C4 + CB_THREADS - 1) / CB_THREADS;
         float4 acc[PER];
 #pragma unroll
         for (int u = 0; u < PER; ++u)
             acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < sn; ++s) {
             const float4 *po =
-                reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slots[s0 + s] * ATT_ROWS * 128);
+                reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slots[s0 + s] * ATT_ROWS * D);
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
-                const int e = tid + u * CB_THREADS, rho = e >> 5;
+                const int e = tid + u * CB_THREADS, rho = e / C4;
                 if (rho < nrows) {
                     const float f = s_fac[s * ATT_ROWS + rho];
                     const float4 v = __ldcg(po + e);
@@ -1150,7 +1162,7 @@ att_combine_kernel(const TcArgs a, int NG)
         }
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            const int e = tid + u * CB_THREADS, rho = e >> 5, d4 = (e & 31) * 4;
+            const int e = tid + u * CB_THREADS, rho = e / C4, d4 = (e % C4) * 4;
             if (rho >= nrows)
                 continue;
             const int gr2 = (rho < TILE) ? rg * TILE + rho : a.n_main * TILE + (rho - TILE);
@@ -1158,7 +1170,7 @@ att_combine_kernel(const TcArgs a, int NG)
                 continue;
             const int i2 = gr2 >> a.g_shift, h2 = gr2 & (a.G - 1);
             float4 *dst = reinterpret_cast<float4 *>(
-                a.out + (((int64_t)r * a.P + i2) * a.Hq + g * a.G + h2) * 128 + d4);
+                a.out + (((int64_t)r * a.P + i2) * a.Hq + g * a.G + h2) * D + d4);
             if (s0 == 0) {
                 *dst = acc[u];
             } else {
@@ -1194,14 +1206,14 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D bf16 map: (d = 128, heads, rows) with a (64, bh, brows) box, 128-byte swizzle
-bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int bh, int brows)
+// 3-D bf16 map: (d, heads, rows) with a (64, bh, brows) box, 128-byte swizzle
+bool make_map(CUtensorMap *m, const void *base, int d, int heads, int64_t rows, int bh, int brows)
 {
     EncodeTiledFn f = encode_fn();
     if (f == nullptr)
         return false;
-    const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {256, (cuuint64_t)heads * 256};
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
     const cuuint32_t box[3] = {64, (cuuint32_t)bh, (cuuint32_t)brows};
     const cuuint32_t es[3] = {1, 1, 1};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
@@ -1209,21 +1221,21 @@ bool make_map(CUtensorMap *m, const void *base, int heads, int64_t rows, int bh,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TQ>
+template <int TQ, int D>
 cudaError_t launch_tq(int grid, const CUtensorMap &tq, const CUtensorMap &tqt,
                       const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tkt,
                       const CUtensorMap &tvt, const TcArgs &a, cudaStream_t s)
 {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(att_tc_kernel<TQ>,
+        cudaError_t e = cudaFuncSetAttribute(att_tc_kernel<TQ, D>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)SM_ALLOC);
         if (e != cudaSuccess)
             return e;
         attr_set = true;
     }
-    att_tc_kernel<TQ><<<grid, NTHREADS, SM_ALLOC, s>>>(tq, tqt, tk, tv, tkt, tvt, a);
+    att_tc_kernel<TQ, D><<<grid, NTHREADS, SM_ALLOC, s>>>(tq, tqt, tk, tv, tkt, tvt, a);
     return cudaGetLastError();
 }
 
@@ -1233,8 +1245,10 @@ bool attention_tc_supported(const ddt_config &cfg)
 {
     const int G = cfg.Hq / cfg.Hkv;
     const int pg = cfg.page_size;
-    if (!(cfg.d == 128 && pg >= 16 && (pg & (pg - 1)) == 0 && G >= 1 && G <= 16 && (16 % G) == 0 &&
-          cfg.R_max < 4096 && cfg.Hkv < 256 && encode_fn() != nullptr))
+    // (the tensor-map encoder is looked up at launch; a missing driver entry
+    // point makes the launch fail with a CUDA error)
+    if (!((cfg.d == 128 || cfg.d == 64) && pg >= 16 && (pg & (pg - 1)) == 0 && G >= 1 && G <= 16 &&
+          (16 % G) == 0 && cfg.R_max < 4096 && cfg.Hkv < 256))
         return false;
     int nm, tail, RG;
     attention_tc_rows(cfg, &nm, &tail, &RG);
@@ -1261,7 +1275,7 @@ void attention_tc_rows(const ddt_config &cfg, int *n_main, int *tail_rows, int *
     *rowgroups = nm;
 }
 
-cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
+cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                                 const uint16_t *v_tree, const uint16_t *k_cache,
                                 const uint16_t *v_cache, const int32_t *block_table,
                                 const int32_t *ctx_lens, const uint32_t *mask, int R,
@@ -1273,12 +1287,13 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     attention_tc_rows(cfg, &n_main, &tail, &RG);
     CUtensorMap tq, tqt, tk, tv, tkt, tvt;
     const int64_t rowsq = (int64_t)R * P, rowsc = cfg.num_pages * cfg.page_size;
-    if (!make_map(&tq, q, cfg.Hq, rowsq, G, TILE / G) ||
-        !make_map(&tqt, q, cfg.Hq, rowsq, G, 16 / G) ||
-        !make_map(&tk, k_cache, cfg.Hkv, rowsc, 1, 16) ||
-        !make_map(&tv, v_cache, cfg.Hkv, rowsc, 1, 16) ||
-        !make_map(&tkt, k_tree, cfg.Hkv, rowsq, 1, 16) ||
-        !make_map(&tvt, v_tree, cfg.Hkv, rowsq, 1, 16))
+    const int d = cfg.d;
+    if (!make_map(&tq, q, d, cfg.Hq, rowsq, G, TILE / G) ||
+        !make_map(&tqt, q, d, cfg.Hq, rowsq, G, 16 / G) ||
+        !make_map(&tk, k_cache, d, cfg.Hkv, rowsc, 1, 16) ||
+        !make_map(&tv, v_cache, d, cfg.Hkv, rowsc, 1, 16) ||
+        !make_map(&tkt, k_tree, d, cfg.Hkv, rowsq, 1, 16) ||
+        !make_map(&tvt, v_tree, d, cfg.Hkv, rowsq, 1, 16))
         return cudaErrorInvalidValue;
     TcArgs a;
     a.block_table = block_table;
@@ -1306,7 +1321,7 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     a.n_main = n_main;
     a.tail_rows = tail;
     a.num_pages = cfg.num_pages;
-    a.scale_log2 = 1.4426950408889634f / sqrtf(128.0f);
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
     // groups of Hkv CTAs (one per KV head), two partial slots per CTA
     int groups = c->num_sms / cfg.Hkv;
     if (groups < 1)
@@ -1314,10 +1329,18 @@ cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint1
     while (groups > 1 && groups * cfg.Hkv * 2 > c->att_max_items)
         --groups;
     const int grid = groups * cfg.Hkv;
-    cudaError_t e = (tail <= 4) ? launch_tq<4>(grid, tq, tqt, tk, tv, tkt, tvt, a, s)
-                                : launch_tq<16>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
+    cudaError_t e;
+    if (d == 128)
+        e = (tail <= 4) ? launch_tq<4, 128>(grid, tq, tqt, tk, tv, tkt, tvt, a, s)
+                        : launch_tq<16, 128>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
+    else
+        e = (tail <= 4) ? launch_tq<4, 64>(grid, tq, tqt, tk, tv, tkt, tvt, a, s)
+                        : launch_tq<16, 64>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
     if (e != cudaSuccess || groups == 1)
         return e;
-    att_combine_kernel<<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
+    if (d == 128)
+        att_combine_kernel<128><<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
+    else
+        att_combine_kernel<64><<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
     return cudaGetLastError();
 }

@@ -25,13 +25,11 @@ constexpr int TOPK_CAND_CAP = 2048;      // limit on chunks x K per row
 constexpr int AMAX_THREADS = 256;
 constexpr int AMAX_VEC_PER_THREAD = 8;
 
-// a4: work items of at most ATT_CHUNK cached tokens per (request, KV head)
-constexpr int ATT_CHUNK = 4096;
-constexpr int ATT_BLOCK_N = 64;          // KV tokens per pipeline stage
-constexpr int ATT_MTILES = 9;            // m16 tiles (warps) per row group
-constexpr int ATT_ROWS = ATT_MTILES * 16;  // query rows per row group (144)
-constexpr int ATT_THREADS = ATT_MTILES * 32;
-constexpr int ATT_STAGES = 3;
+// a4: rows of one partial output (128 main rows plus up to 16 tail rows) and
+// the most CTAs of the attention grid (two partial slots each)
+constexpr int ATT_ROWS = 144;
+constexpr int ATT_MAX_CTAS = 256;
+constexpr int ATT_MAX_CTX = 262144;  // tokens of context per request
 
 // parent-conditioned tree: most CTAs of its per-depth GEMM (partials per CTA)
 constexpr int CG_GRID_MAX = 256;
@@ -56,13 +54,8 @@ struct ddt_ctx {
     int am_nch;
     float *am_val;           // [R_max * P, nch]
     int32_t *am_idx;         // [R_max * P, nch]
-    // a4 plan + partials
-    int att_rowgroups;       // ceil(P * G / ATT_ROWS)
-    int att_max_items;
-    int4 *att_items;         // [max_items] (r, g | rowgroup << 16, t0, t1)
-    int32_t *att_meta;       // [0] = item count, [1] = work counter, [2] = done counter
-    unsigned *att_rg_cnt;    // [R_max * Hkv * rowgroups] arrival counters
-    int32_t *att_rg_base;    // [R_max * Hkv * rowgroups] first item of each (r, g, rowgroup)
+    // a4 partials of the runs that share boundaries split (two slots per CTA)
+    int att_max_items;       // 2 * ATT_MAX_CTAS
     float *att_part_o;       // [max_items, ATT_ROWS, d]
     float2 *att_part_ml;     // [max_items, ATT_ROWS]
     // parent-conditioned tree (markov_dim > 0)
@@ -89,8 +82,6 @@ struct ddt_ctx {
     uint64_t *ps_rk;         // [DDT_SCHED_MAX_SLOTS] survival bits in ranking order
     int32_t *ps_rid;         // [DDT_SCHED_MAX_SLOTS] their tie ids
     unsigned *ps_arrive;     // arrival counter (self-resetting)
-    int att_grid;            // persistent CTAs
-    bool att_use_tc;         // tcgen05 kernel (head dim 128, 16-token page multiples)
 };
 
 // launchers (return the cudaGetLastError of the launch)
@@ -118,16 +109,10 @@ cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t
                              const int32_t *ctx_lens, const uint32_t *mask, int R, float *out,
                              cudaStream_t s);
 
-// a4 on tcgen05 (attention_tc.cu) and the shared work-list plan
+// a4 on tcgen05 (attention_tc.cu): the shapes it takes (head dim 64 or 128,
+// G = Hq / Hkv dividing 16, pages of a power-of-two multiple of 16 tokens)
 bool attention_tc_supported(const ddt_config &cfg);
 void attention_tc_rows(const ddt_config &cfg, int *n_main, int *tail_rows, int *rowgroups);
-cudaError_t launch_attention_tc(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
-                                const uint16_t *v_tree, const uint16_t *k_cache,
-                                const uint16_t *v_cache, const int32_t *block_table,
-                                const int32_t *ctx_lens, const uint32_t *mask, int R,
-                                float *out, cudaStream_t s);
-cudaError_t launch_att_plan(const ddt_ctx *c, const int32_t *ctx_lens, int R, int RG, int max_ctx,
-                            cudaStream_t s);
 
 // the parent-conditioned tree (cond_tree.cu)
 bool cond_tree_supported(const ddt_config &cfg);
