@@ -231,9 +231,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true",
                     help="skip the timing of the NEXT rows (parent-conditioned tree)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the single-request and wide workloads' lines")
     ap.add_argument("--stage", default="round",
                     choices=["round", "topk", "tree", "attention", "accept", "cond_tree",
-                             "markov", "stochastic", "scheduler"],
+                             "markov", "stochastic", "scheduler", "single", "wide256"],
                     help="time one stage alone (small profiling cases); cond_tree: the "
                          "parent-conditioned tree's workload alone")
     ap.add_argument("--requests", type=int, default=0,
@@ -257,11 +259,14 @@ def main():
 
     import torch
     torch.cuda.set_device(local_rank)
-    if args.stage in ("cond_tree", "markov", "stochastic", "scheduler"):
+    if args.stage in ("cond_tree", "markov", "stochastic", "scheduler", "single", "wide256"):
         from speculative_decoding_draft_depth_gb300 import ddt
         ddt.load()
         fn = {"cond_tree": time_cond_tree, "markov": time_markov,
-              "stochastic": time_stochastic, "scheduler": time_scheduler}[args.stage]
+              "stochastic": time_stochastic, "scheduler": time_scheduler,
+              "single": time_single,
+              "wide256": lambda dev, reps, cpu: time_wide256(dev, blocks=max(2, reps // 40),
+                                                             cpu=cpu)}[args.stage]
         res = fn(torch.device("cuda", local_rank), reps=max(args.steps, 1),
                  cpu=not args.no_cpu_baseline)
         if rank == 0:
@@ -382,6 +387,9 @@ def main():
            "clocks": clk,
            "acceptance": {"mean_acc_len": float(np.mean(acc_len))}}
 
+    if rank == 0 and not args.no_configs:
+        out["configs"] = {"single": time_single(dev, cpu=not args.no_cpu_baseline),
+                          "wide256": time_wide256(dev, cpu=not args.no_cpu_baseline)}
     if rank == 0 and not args.no_next:
         out["next_rows"] = {"cond_tree": time_cond_tree(dev, cpu=not args.no_cpu_baseline),
                             "markov_table_tree": time_markov(dev, cpu=not args.no_cpu_baseline),
@@ -449,6 +457,233 @@ def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):
     d["ctx_lens"].copy_(ctx0)
     torch.cuda.synchronize()
     return res
+
+
+def _td(a, dev):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).to(dev)
+
+
+def _make_ctx(cfg, block_table, num_pages):
+    from speculative_decoding_draft_depth_gb300 import ddt
+    c = ddt.make_config(R_max=cfg.R, L=cfg.L, V=cfg.V, B=cfg.B, K=cfg.K, Hq=cfg.Hq, Hkv=cfg.Hkv,
+                        d=cfg.d, page_size=cfg.page, max_pages_per_req=block_table.shape[1],
+                        num_pages=num_pages)
+    return ddt.Context(c)
+
+
+def time_single(dev, reps=200, cpu=True):
+    """The single-request workload (R=1, L=15, V=151936, B=32, Qwen3-8B
+    attention at context 4096): a whole round (ddt_round) as device time per
+    call over `reps` calls, the stages alone, the algorithmic bytes, and the
+    oracle's round on the same inputs. The round is latency-bound at batch 1;
+    the pages' DDTree candidate construction (GPU top-K and logsumexp, a copy
+    to the host and a CPU heap) took 0.49 ms per round at batch 1 on an
+    unstated GPU, which the top-K plus tree stages here compare with."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import synth
+    cfg = synth.config("single")
+    inp = synth.draw_round_inputs(cfg)
+    ctx = _make_ctx(cfg, inp["block_table"], inp["k_cache"].shape[0])
+    bufs = ctx.alloc_outputs(cfg.R, device=dev)
+    d = {k: _td(inp[k], dev) for k in ("draft_logits", "q", "k_tree", "v_tree", "k_cache",
+                                       "v_cache", "block_table", "ctx_lens")}
+    ctx0 = d["ctx_lens"].clone()
+    bufs.update(d)
+    bufs["target_logits"] = torch.zeros((cfg.R, cfg.P, cfg.V), dtype=torch.int16, device=dev)
+    ctx.ddt_round(cfg.R, bufs)
+    torch.cuda.synchronize()
+    target = synth.GreedyTarget(cfg, inp["draft"], inp["agree"])
+    tl = target.logits_for_tree(bufs["tree_tokens"].cpu().numpy(), bufs["parents"].cpu().numpy(),
+                                bufs["n_nodes"].cpu().numpy())
+    inp["target_logits"] = tl
+    bufs["target_logits"] = _td(tl, dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        ctx.ddt_round(cfg.R, bufs, stream)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(reps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set in the single-request round")
+    acc_len = bufs["acc_len"].cpu().numpy()
+    stage_ms = time_stages(ctx, cfg, bufs, d, ctx0, stream, reps=max(20, reps // 4))
+    nb = round_bytes(cfg, inp["ctx_lens"], acc_len)
+    peak, _ = _peaks()
+    res = {"workload": _workload_desc(cfg), "ms_per_round": round(ms, 4),
+           "rounds_per_s": round(1e3 / ms, 1),
+           "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+           "construction_ms": round(stage_ms["topk"] + stage_ms["tree"], 4),
+           "construction_context": "the pages' DDTree candidate construction at batch 1: 0.49 ms "
+                                   "per round (GPU top-K + CPU heap, unstated GPU)",
+           "algorithmic_bytes": int(nb["total"]),
+           "GBps": round(nb["total"] / (ms / 1e3) / 1e9, 1),
+           "frac_of_hbm": round(nb["total"] / (ms / 1e3) / 1e9 / peak, 4),
+           "bound": "latency (one request: each stage is a short kernel chain)",
+           "mean_acc_len": float(np.mean(acc_len))}
+    if cpu:
+        secs = [cpu_oracle_round(cfg, inp, np.array([0])) for _ in range(3)]
+        res["cpu_oracle_ms"] = round(float(np.median(secs)) * 1e3, 1)
+        res["cpu_oracle_sample"] = "the whole round (one request), median of 3"
+    ctx.close()
+    return res
+
+
+def gpu_wide_inputs(cfg, dev, seed):
+    """The wide workload's round inputs drawn on the GPU (a seeded torch
+    generator; the numpy generators take minutes at this size): the same
+    recipe as synth.draw_round_inputs (draft rows N(0,1) plus the Zipf boost
+    on 20 distinct tokens, divided by a temperature U[0.3, 1.5] per request
+    and depth; lognormal contexts; a permuted page pool; N(0,1) caches,
+    queries and tree keys/values, all bf16). Contexts and the page table come
+    from numpy (small)."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import synth
+    rng = np.random.default_rng(seed)
+    ctx_lens = synth.draw_ctx_lens(cfg, rng)
+    grow = cfg.rounds * (cfg.L + 1)
+    need = [(int(c) + grow + cfg.page - 1) // cfg.page for c in ctx_lens]
+    num_pages = sum(need) + cfg.spare_pages
+    perm = rng.permutation(num_pages).astype(np.int32)
+    block_table = np.full((cfg.R, max(need)), -1, np.int32)
+    pos = 0
+    for r, n in enumerate(need):
+        block_table[r, :n] = perm[pos:pos + n]
+        pos += n
+    g = torch.Generator(device=dev).manual_seed(int(seed))
+    R, L, V, P = cfg.R, cfg.L, cfg.V, cfg.P
+    z = torch.randn((R * L, V), generator=g, device=dev)
+    toks = torch.multinomial(torch.ones((R * L, V), device=dev), 20, replacement=False,
+                             generator=g)
+    boost = (8.0 * torch.arange(1, 21, device=dev, dtype=torch.float32) ** -1.1).expand(R * L, 20)
+    z.scatter_add_(1, toks, boost.contiguous())
+    lo, hi = cfg.temp_range
+    temp = lo + (hi - lo) * torch.rand((R * L, 1), generator=g, device=dev)
+    z = (z / temp).to(torch.bfloat16).view(R, L, V)
+
+    def nrm(shape):
+        return torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+
+    out = {"draft_logits": z.view(torch.int16), "ctx_lens": ctx_lens, "block_table": block_table,
+           "k_cache": nrm((num_pages, cfg.page, cfg.Hkv, cfg.d)).view(torch.int16),
+           "v_cache": nrm((num_pages, cfg.page, cfg.Hkv, cfg.d)).view(torch.int16),
+           "q": nrm((R, P, cfg.Hq, cfg.d)).view(torch.int16),
+           "k_tree": nrm((R, P, cfg.Hkv, cfg.d)).view(torch.int16),
+           "v_tree": nrm((R, P, cfg.Hkv, cfg.d)).view(torch.int16), "gen": g}
+    return out
+
+
+def time_wide256(dev, blocks=5, cpu=True):
+    """The wide workload (R=256, B=K=64, lognormal contexts up to 32768,
+    Qwen3-4B attention): blocks of 8 consecutive rounds (ddt_round) with
+    compaction in between, the context lengths growing by each round's
+    accepted length; every block restores the first round's contexts. Device
+    time per round over `blocks` blocks after one warm-up block, the
+    algorithmic bytes of the 8 rounds (contexts as they grew), and the
+    oracle's round on two requests scaled to the batch. The 8 rounds of a
+    block reuse one set of logits, queries and tree keys/values (the parity
+    test draws fresh ones per round); the target agrees with the draft's
+    top-1 token at 3 of 4 tree positions, the rest pick a random token."""
+    import torch
+    from speculative_decoding_draft_depth_gb300 import synth
+    cfg = synth.config("wide256")
+    gi = gpu_wide_inputs(cfg, dev, cfg.seed)
+    g = gi.pop("gen")
+    ctx = _make_ctx(cfg, gi["block_table"], gi["k_cache"].shape[0])
+    bufs = ctx.alloc_outputs(cfg.R, device=dev)
+    d = {k: (v if torch.is_tensor(v) else _td(v, dev)) for k, v in gi.items()}
+    ctx0 = d["ctx_lens"].clone()
+    bufs.update(d)
+    R, P, V, L = cfg.R, cfg.P, cfg.V, cfg.L
+    bufs["target_logits"] = torch.zeros((R, P, V), dtype=torch.int16, device=dev)
+    ctx.ddt_round(R, bufs)  # set-up round: the tree the target follows
+    torch.cuda.synchronize()
+    top1 = d["draft_logits"].view(torch.bfloat16).float().argmax(-1)  # [R, L] (construction)
+    depth = bufs["depths"].long().clamp(0, L - 1)
+    want = torch.gather(top1, 1, depth)
+    agree = torch.rand((R, P), generator=g, device=dev) < 0.75
+    tok = torch.where(agree, want, torch.randint(0, V, (R, P), generator=g, device=dev))
+    tl = torch.randn((R, P, V), generator=g, device=dev)
+    tl.scatter_add_(2, tok.unsqueeze(-1), torch.full((R, P, 1), 20.0, device=dev))
+    bufs["target_logits"] = tl.to(torch.bfloat16).view(torch.int16)
+    del tl
+    d["ctx_lens"].copy_(ctx0)
+    stream = torch.cuda.current_stream()
+
+    def block():
+        d["ctx_lens"].copy_(ctx0, non_blocking=True)
+        for _ in range(cfg.rounds):
+            ctx.ddt_round(R, bufs, stream)
+
+    block()
+    torch.cuda.synchronize()
+    acc_len = bufs["acc_len"].cpu().numpy()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(blocks):
+        block()
+    b.record(stream)
+    torch.cuda.synchronize()
+    if ctx.ddt_device_status() != 0:
+        raise RuntimeError("device status flags set in the wide rounds")
+    ms = a.elapsed_time(b) / (blocks * cfg.rounds)
+    c0 = gi["ctx_lens"].astype(np.int64)
+    nbytes = [round_bytes(cfg, c0 + k * acc_len, acc_len)["total"] for k in range(cfg.rounds)]
+    per_round = float(np.mean(nbytes))
+    peak, _ = _peaks()
+    res = {"workload": _workload_desc(cfg) + ", 8 rounds with compaction",
+           "ms_per_round": round(ms, 4), "rounds_per_s": round(1e3 / ms, 1),
+           "rounds_per_block": cfg.rounds, "blocks": blocks,
+           "bytes_per_round": int(per_round),
+           "GBps": round(per_round / (ms / 1e3) / 1e9, 1),
+           "frac_of_hbm": round(per_round / (ms / 1e3) / 1e9 / peak, 4),
+           "mean_acc_len": float(np.mean(acc_len)),
+           "data": "synthetic, drawn on the GPU (seeded torch generator, the synth recipe)"}
+    if cpu:
+        import oracle
+        reqs = np.array([0, 1])
+        sub = _host_requests(cfg, d, bufs, reqs)
+        secs = cpu_oracle_round(replace_R(cfg, len(reqs)), sub, np.arange(len(reqs)))
+        res["cpu_oracle_ms"] = round(secs * R / len(reqs) * 1e3, 1)
+        res["cpu_oracle_sample"] = "2 of 256 requests (all stages), scaled to the batch"
+    ctx.close()
+    return res
+
+
+def replace_R(cfg, R):
+    from dataclasses import replace
+    return replace(cfg, R=R)
+
+
+def _host_requests(cfg, d, bufs, reqs):
+    """Host copies of some requests' round inputs, their pages gathered into a
+    small pool with a renumbered page table (for the oracle)."""
+    import torch
+    bt = d["block_table"].cpu().numpy()[reqs]
+    pages = sorted({int(p) for p in bt.reshape(-1) if p >= 0})
+    remap = {p: i for i, p in enumerate(pages)}
+    nbt = np.where(bt >= 0, np.vectorize(lambda p: remap.get(int(p), -1))(bt), -1).astype(np.int32)
+    pi = torch.tensor(pages, device=d["k_cache"].device, dtype=torch.long)
+    host = lambda t: t.cpu().numpy().view(np.uint16) if t.dtype == torch.int16 else t.cpu().numpy()  # noqa: E731
+    ri = torch.tensor(reqs, device=d["k_cache"].device, dtype=torch.long)
+    return {"draft_logits": host(d["draft_logits"][ri]), "q": host(d["q"][ri]),
+            "k_tree": host(d["k_tree"][ri]), "v_tree": host(d["v_tree"][ri]),
+            "block_table": nbt, "ctx_lens": d["ctx_lens"].cpu().numpy()[reqs],
+            "k_cache": host(d["k_cache"][pi]), "v_cache": host(d["v_cache"][pi]),
+            "target_logits": host(bufs["target_logits"][ri]), "copy_cache": True}
 
 
 def time_cond_tree(dev, reps=20, cpu=True):
