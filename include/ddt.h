@@ -403,6 +403,21 @@ ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const
  * device status word to *host_out (DDT_DEV_* bits) and clear it. */
 ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out);
 
+/* Test-only failure detection for the a4 kernel's bounded waits. The pages
+ * have no counterpart; the call exists so that a test can drive the timeout
+ * path on a GPU without a fault.
+ *
+ * Arms the context's next a4 launch (ddt_tree_attention, or the attention of
+ * one of the round entry points), once: every CTA of that launch starts with
+ * one bounded wait on an on-chip barrier that nothing arrives at, limited to
+ * wait_cycles SM clock cycles. The wait runs out before the CTA has issued
+ * any copy or MMA; the CTA then raises DDT_DEV_TIMEOUT in the device status
+ * word, skips its work (the attention output of that launch is undefined),
+ * frees its tensor memory and returns. The context stays usable and the next
+ * launch is normal. wait_cycles <= 0 disarms. The setting is host state of
+ * the context, read and cleared when the next a4 launch is enqueued. */
+ddt_status ddt_debug_arm_attention_timeout(ddt_ctx *ctx, int64_t wait_cycles);
+
 /* a1 without a context, for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point.
  *

@@ -788,6 +788,14 @@ ddt_status ddt_device_status(ddt_ctx *ctx, int32_t *host_out)
     return DDT_OK;
 }
 
+ddt_status ddt_debug_arm_attention_timeout(ddt_ctx *ctx, int64_t wait_cycles)
+{
+    if (ctx == nullptr)
+        return DDT_EINVAL;
+    ctx->debug_att_wait = wait_cycles > 0 ? wait_cycles : 0;
+    return DDT_OK;
+}
+
 const char *ddt_strerror(ddt_status status)
 {
     switch (status) {

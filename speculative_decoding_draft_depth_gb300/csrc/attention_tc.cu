@@ -108,6 +108,7 @@ constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16,
                    B_TMEM = 400, B_ABORT = 404,
                    B_RING = 416,    // [NRING][4] ints: segments (x = -1: end of the share)
                    B_TOTAL = 480,   // int: T, the batch's total tiles
+                   B_DEBUG = 496,   // a barrier nothing arrives at (the armed test wait)
                    B_RED = 512,     // 2 x [4 warps][16] floats: tail column max
                    B_SUM = 1024,    // 2 x [4 warps][16] floats: tail sums
                    B_XMAX = 1536,   // 2 x [4 column quarters][128 rows] floats: row max
@@ -130,6 +131,7 @@ struct TcArgs {
     int R, P, Hq, Hkv, G, g_shift, W, page_shift, max_pages, RG, n_main, tail_rows, max_ctx;
     int64_t num_pages;
     float scale_log2;
+    long long debug_wait;  // > 0 (tests only): start with a wait that runs out after this many cycles
 };
 
 struct Item {
@@ -174,8 +176,8 @@ DDT_DEVINL int part_slot(long long ps, long long T, int grp, int NG, int g, int 
 }
 
 // bounded mbarrier wait; false (and the abort flag raised) on timeout
-DDT_DEVINL bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                         int32_t *status)
+DDT_DEVINL bool wait_bar_for(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                             int32_t *status, long long limit)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -183,13 +185,18 @@ DDT_DEVINL bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag)
             return false;
-        if (clock64() - t0 > WAIT_LIMIT) {
+        if (clock64() - t0 > limit) {
             *abort_flag = 1;
             atomicOr(status, DDT_DEV_TIMEOUT);
             return false;
         }
     }
     return true;
+}
+
+DDT_DEVINL bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *status)
+{
+    return wait_bar_for(bar, parity, abort_flag, status, WAIT_LIMIT);
 }
 
 // wind-down wait for work this thread itself started (ignores the abort flag)
@@ -362,6 +369,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(bar + B_ODONE, 1);
         mbar_init(bar + B_OTDONE, 1);
         mbar_init(bar + B_FINAL, 1);
+        mbar_init(bar + B_DEBUG, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -379,8 +387,18 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(sgen + SM_BAR + B_TMEM);
     const int PG = a.P * a.G;
     const int pos_per_main = TILE >> a.g_shift;
+    if (a.debug_wait > 0) {
+        // armed by a test: a bounded wait on a barrier nothing arrives at, before
+        // any copy or MMA is issued; it runs out, and every role is skipped
+        if (tid == 0)
+            wait_bar_for(bar + B_DEBUG, 0, abort_flag, a.status, a.debug_wait);
+        __syncthreads();
+    }
+    const bool run = (*abort_flag == 0);
 
-    if (warp == W_KPROD) {
+    if (!run) {
+        // nothing issued: straight to the wind-down
+    } else if (warp == W_KPROD) {
         // ============================================================ share walk, Q and K loads
         if (lane == 0) {
             prefetch_tmap(&tm_q);
@@ -1275,7 +1293,7 @@ void attention_tc_rows(const ddt_config &cfg, int *n_main, int *tail_rows, int *
     *rowgroups = nm;
 }
 
-cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
+cudaError_t launch_attention(ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                                 const uint16_t *v_tree, const uint16_t *k_cache,
                                 const uint16_t *v_cache, const int32_t *block_table,
                                 const int32_t *ctx_lens, const uint32_t *mask, int R,
@@ -1322,6 +1340,8 @@ cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t
     a.tail_rows = tail;
     a.num_pages = cfg.num_pages;
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+    a.debug_wait = c->debug_att_wait;  // one-shot test setting
+    c->debug_att_wait = 0;
     // groups of Hkv CTAs (one per KV head), two partial slots per CTA
     int groups = c->num_sms / cfg.Hkv;
     if (groups < 1)

@@ -45,6 +45,7 @@ struct ddt_ctx {
     cudaStream_t side;       //   a5 beside them on a lowest-priority one
     cudaEvent_t ev_fork, ev_tree, ev_join, ev_walk;
     int32_t *status;         // device status word
+    int64_t debug_att_wait;  // > 0: the next attention launch starts with a wait that runs out (test only)
     // a1 partials
     int tk_nch;              // chunks per row
     uint16_t *tk_gkey;       // [R_max * L, nch * TOPK_THREADS] each group's max (ordered key)
@@ -103,7 +104,7 @@ cudaError_t launch_walk_compact(const ddt_ctx *c, const int32_t *argmax, bool ar
                                 const uint16_t *k_tree, const uint16_t *v_tree, bool advance_ctx,
                                 cudaStream_t s);
 cudaError_t launch_ctx_advance(int R, int32_t *ctx_lens, const int32_t *acc_len, cudaStream_t s);
-cudaError_t launch_attention(const ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
+cudaError_t launch_attention(ddt_ctx *c, const uint16_t *q, const uint16_t *k_tree,
                              const uint16_t *v_tree, const uint16_t *k_cache,
                              const uint16_t *v_cache, const int32_t *block_table,
                              const int32_t *ctx_lens, const uint32_t *mask, int R, float *out,

@@ -16,14 +16,14 @@ LIB_PATH = os.path.join(_HERE, "_build", "libddt.so")
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOMEM = 0, 1, 2, 3, 4
 BF16, F32 = 0, 1
-DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE = 0x1, 0x2, 0x4
+DEV_NAN_LOGITS, DEV_BAD_PAGE, DEV_BAD_TREE, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 EXPORTS = ("ddt_create", "ddt_destroy", "ddt_workspace_bytes", "ddt_topk_logprobs",
            "ddt_build_tree", "ddt_build_tree_conditioned", "ddt_build_mask", "ddt_tree_attention", "ddt_target_argmax",
            "ddt_walk", "ddt_compact", "ddt_accept", "ddt_round", "ddt_round_conditioned",
            "ddt_markov_table", "ddt_build_tree_markov", "ddt_round_markov",
            "ddt_accept_stochastic", "ddt_schedule_prefix", "ddt_device_status", "ddt_strerror",
-           "ddt_last_cuda_error")
+           "ddt_last_cuda_error", "ddt_debug_arm_attention_timeout")
 
 
 class DdtError(RuntimeError):
@@ -92,6 +92,7 @@ def load(path=LIB_PATH):
         "ddt_accept_stochastic": ([_P, _P, _P, _P, _P, _P, i32, _P, _P, _P, _P], i32),
         "ddt_schedule_prefix": ([_P, _P, i32, _P, _P, _P, _P, _P], i32),
         "ddt_device_status": ([_P, ctypes.POINTER(i32)], i32),
+        "ddt_debug_arm_attention_timeout": ([_P, i64], i32),
         "ddt_strerror": ([i32], ctypes.c_char_p),
         "ddt_last_cuda_error": ([], i32),
     }
@@ -298,6 +299,12 @@ class Context:
         out = ctypes.c_int32(0)
         _check(_lib.ddt_device_status(self._h, ctypes.byref(out)), "ddt_device_status")
         return out.value
+
+    def ddt_debug_arm_attention_timeout(self, wait_cycles):
+        """Test only: the next a4 launch starts with a bounded wait that runs
+        out after wait_cycles SM cycles (see include/ddt.h)."""
+        _check(_lib.ddt_debug_arm_attention_timeout(self._h, int(wait_cycles)),
+               "ddt_debug_arm_attention_timeout")
 
     # -- allocation helper (plumbing) ----------------------------------------
     def alloc_outputs(self, R, device="cuda"):
