@@ -5,9 +5,12 @@ CPU-baseline / reference leg of ``bench.py`` may import this package. The
 product path (the CUDA library and its binding) never imports it, and the two
 share no code; only the seeded input generators feed both.
 
-The arithmetic lives in ``oracle.c`` (plain C, IEEE double). This module only
-marshals numpy arrays into it. bf16 tensors travel as their raw 16-bit
-patterns (``numpy.uint16``) and are widened exactly inside the C code.
+The arithmetic lives in ``oracle.c`` (plain C, IEEE double). This module
+marshals numpy arrays into it; bf16 tensors travel as their raw 16-bit
+patterns (``numpy.uint16``) and are widened exactly inside the C code. One
+small helper is plain Python: ``prefixes_at_least`` enumerates the prefixes
+near a score cut (the tie band of the tree tests), a handful per request,
+with fp64 sums.
 
 Pages cited (by title and section):
   "SparklingTree: 30-40% faster speculative decoding over DSpark",
@@ -153,6 +156,35 @@ def build_tree(lp, ids, B):
     if rc:
         raise ValueError("bad arguments to build_tree")
     return t
+
+
+def prefixes_at_least(lp, ids, smin):
+    """Every prefix of one request's token space whose score is at least smin.
+
+    The DDTree prefix space ("DDTree Explained ...", section 4 and Algorithm
+    1): a prefix is a path of tokens, one per depth, depth d's token drawn
+    from the K candidates of that depth; its score is the fp64 sum of the
+    chosen candidates' log-probs. lp/ids [L, K] with each depth's lp in
+    descending order (the top-K order). Returns [(token path, score)].
+    A depth-first walk visits a node's children in rank order and stops at
+    the first one below smin: lp <= 0, so a prefix scores no more than its
+    parent, and a later rank scores no more than an earlier one."""
+    lp = np.ascontiguousarray(lp, dtype=np.float64)
+    L, K = lp.shape
+    out = []
+    stack = [((), 0.0, 0)]
+    while stack:
+        path, S, d = stack.pop()
+        if d == L:
+            continue
+        for j in range(K):
+            s = S + lp[d, j]
+            if s < smin:
+                break
+            p = path + (int(ids[d, j]),)
+            out.append((p, s))
+            stack.append((p, s, d + 1))
+    return out
 
 
 def build_tree_bruteforce(lp, ids, B, max_prefixes=5_000_000):

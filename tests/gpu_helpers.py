@@ -101,8 +101,11 @@ def tree_paths(tokens, parents, n):
 def check_tie_band(B, o_lp, o_ids, otree, g_tokens, g_parents, g_depths, g_n_nodes, rows):
     """End-to-end node set of the GPU tree (built from fp32 log-probs) against
     the oracle's (fp64): prefix scores within TIE_EPS nats of the B-th count as
-    tied; every prefix above the band must be present, none below it, and the
-    band must hold as many nodes on both sides."""
+    tied. Every prefix above the band must be present and none below it; the
+    band is compared as a set: the GPU's tied nodes must all belong to the
+    oracle's full band (every prefix within TIE_EPS of the B-th score, the ones
+    the heap selected and the ones it left behind), and both trees take the
+    same number of them."""
     for r in rows:
         n = int(otree.n_nodes[r])
         assert int(g_n_nodes[r]) == n
@@ -119,4 +122,7 @@ def check_tie_band(B, o_lp, o_ids, otree, g_tokens, g_parents, g_depths, g_n_nod
         assert all(s >= SB - TIE_EPS for s in Sg)
         band_o = {p for p, s in zip(paths_o, So) if abs(s - SB) <= TIE_EPS}
         band_g = {p for p, s in zip(paths_g, Sg) if abs(s - SB) <= TIE_EPS}
+        band_all = {p for p, s in oracle.prefixes_at_least(o_lp[r], o_ids[r], SB - TIE_EPS)
+                    if s <= SB + TIE_EPS}
+        assert band_o <= band_all and band_g <= band_all
         assert len(band_o) == len(band_g)

@@ -198,3 +198,45 @@ def test_tree_structure_invariants_at_full_vocab(orc):
         key = (int(t.parents[0, node]), int(t.tokens[0, node - 1]))
         assert key not in sib
         sib[key] = node
+
+
+@pytest.mark.parametrize("L,K,quant,seed", [(3, 3, False, 1), (4, 3, True, 2), (2, 5, True, 3)])
+def test_prefixes_at_least_matches_full_enumeration(orc, L, K, quant, seed):
+    """The pruned walk returns exactly the prefixes a full enumeration of the
+    K + K^2 + ... + K^L prefixes scores at or above the cut, with the same
+    fp64 scores (quantised log-probs make many exact ties at the cut)."""
+    rng = np.random.default_rng(seed)
+    lp = -np.sort(rng.exponential(1.0, (L, K)), axis=1)
+    if quant:
+        lp = np.round(lp * 2) / 2
+    lp = -np.sort(-lp, axis=1)  # descending per depth
+    ids = np.stack([rng.permutation(50)[:K] for _ in range(L)]).astype(np.int32)
+    full = {}
+    for depth in range(1, L + 1):
+        for ranks in itertools.product(range(K), repeat=depth):
+            path = tuple(int(ids[d, j]) for d, j in enumerate(ranks))
+            full[path] = float(sum(lp[d, j] for d, j in enumerate(ranks)))
+    for smin in sorted(set(full.values()))[::max(1, len(full) // 7)] + [-1e9, 0.0]:
+        want = {p: s for p, s in full.items() if s >= smin}
+        got = dict(orc.prefixes_at_least(lp, ids, smin))
+        assert set(got) == set(want)
+        for p in want:
+            assert got[p] == pytest.approx(want[p], abs=1e-12)
+
+
+def test_tree_nodes_lie_in_the_prefix_set_of_its_last_score(orc):
+    """The heap's B nodes all score at least the B-th score, and every prefix
+    strictly above it is one of them."""
+    rng = np.random.default_rng(5)
+    L, K, B = 5, 4, 24
+    lp = -np.sort(np.round(rng.exponential(1.0, (1, L, K)) * 2) / 2, axis=2)
+    ids = np.stack([rng.permutation(100)[:K] for _ in range(L)])[None].astype(np.int32)
+    t = orc.build_tree(lp, ids, B)
+    n = int(t.n_nodes[0])
+    SB = t.S[0, 1:n + 1].min()
+    above = {p for p, s in orc.prefixes_at_least(lp[0], ids[0], SB) if s > SB}
+    paths = {}
+    for node in range(1, n + 1):
+        paths[node] = paths.get(int(t.parents[0, node]), ()) + (int(t.tokens[0, node - 1]),)
+    assert above <= set(paths.values())
+    assert set(paths.values()) <= {p for p, _ in orc.prefixes_at_least(lp[0], ids[0], SB)}
