@@ -366,7 +366,7 @@ def main():
     traffic = _traffic_for("attention_tc.cu", "att_kernel")
     roofline = {"bound": "hbm", "achieved": round(att_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(att_gbs / peak, 4), "traffic": traffic,
-                "kernel": "ddt_tree_attention (paged GQA tree attention)",
+                "kernel": "att_tc_kernel (a4, ddt_tree_attention: paged GQA tree attention on tcgen05)",
                 "launch_ms": round(att_ms_live, 4),
                 "peak_kind": peak_kind}
     round_gbs = nb["total"] * value / world / 1e9
@@ -751,17 +751,28 @@ def time_cond_tree(dev, reps=20, cpu=True):
     ms_round = timed(round_)
     if ctx.ddt_device_status() != 0:
         raise RuntimeError("device status flags set in the conditioned round")
-    nbytes = cfg.L * (cfg.V * cfg.markov_dim * 2 + R * cfg.V * 2) + R * (cfg.L * cfg.frontier *
-                                                                        cfg.markov_dim * 2)
+    # W is read at every depth but stays in L2 after the first (evict-last
+    # TMA loads): DRAM bytes count it once, L2 bytes once per depth
+    w_bytes = cfg.V * cfg.markov_dim * 2
+    rows = cfg.L * R * cfg.V * 2 + R * cfg.L * cfg.frontier * cfg.markov_dim * 2
+    nbytes = w_bytes + rows
+    l2_bytes = cfg.L * w_bytes + rows
     rb = round_bytes(cfg, inp["ctx_lens"], bufs["acc_len"].cpu().numpy())
     nbytes_round = nbytes + rb["attention"] + rb["accept"]
     peak, _ = _peaks()
     res = {"workload": "treespark: R=8, 7 depths, V=151936, H=256, k=4, F=4, N=32, "
                        "Hq=32, Hkv=8, d=128, ctx 2048, bf16",
-           "ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+           "ms": round(ms, 4),
+           "bound": "latency: %d dependent depth steps (a GEMM over the L2-resident W, then "
+                    "the merge), chained by programmatic dependent launch" % cfg.L,
+           "us_per_depth": round(ms * 1e3 / cfg.L, 2),
+           "algorithmic_bytes": int(nbytes),
+           "dram_bytes_note": "W (%.1f MB) once, the backbone rows and the frontier's E rows "
+                              "at every depth" % (w_bytes / 1e6),
            "GBps": round(nbytes / (ms / 1e3) / 1e9, 1),
            "frac_of_hbm": round(nbytes / (ms / 1e3) / 1e9 / peak, 4),
-           "note": "W (78 MB) is read once per depth and fits in L2",
+           "l2_bytes": int(l2_bytes),
+           "l2_GBps": round(l2_bytes / (ms / 1e3) / 1e9, 1),
            "round": {"ms": round(ms_round, 4), "rounds_per_s": round(1e3 / ms_round, 1),
                      "algorithmic_bytes": int(nbytes_round),
                      "GBps": round(nbytes_round / (ms_round / 1e3) / 1e9, 1),
@@ -858,7 +869,11 @@ def time_markov(dev, reps=20, cpu=True):
 
     res = {"workload": "sparkling: R=64, L=15, V=151936, C=128, B=64, H=256, Hq=32, Hkv=8, "
                        "d=128, ctx~U[512,16384], bf16",
-           "table": rate(b_table, ms_table), "tree": rate(b_tree, ms_tree),
+           "table": dict(rate(b_table, ms_table),
+                         bound="HBM: the logits once, then gathered W/E rows and the table"),
+           "tree": dict(rate(b_tree, ms_tree),
+                        bound="latency: %d dependent heap pops per request (one CTA each)" % B,
+                        us_per_pop=round(ms_tree * 1e3 / B, 3)),
            "round": dict(rate(b_round, ms_round), rounds_per_s=round(1e3 / ms_round, 1))}
     if cpu:
         import oracle
