@@ -409,10 +409,12 @@ def main():
 
 
 def launches_per_round(cfg):
-    """Kernels ddt_round launches: top-K chunks (+ row merge when a row spans
-    several chunks), tree, attention plan + attention, argmax chunks, walk."""
-    chunk = 256 * 8 * (8 if cfg.logit_dtype == "bf16" else 4)
-    return 6 + (1 if cfg.V > chunk else 0)
+    """Kernels of this library one ddt_round launches (the ncu launch list in
+    profiles/launches_round_batch64.md shows the same set): a1 streaming +
+    a1 selection, the a2/a3 tree, a5 argmax, a4 attention and its split
+    combine (launched whenever the grid has more than one CTA group, i.e.
+    Hkv < SMs / 2), a6/a7 walk + compaction, and the context-length update."""
+    return 8
 
 
 def time_stages(ctx, cfg, bufs, d, ctx0, stream, reps, only=None):

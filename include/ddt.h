@@ -430,9 +430,10 @@ ddt_status ddt_debug_arm_attention_timeout(ddt_ctx *ctx, int64_t wait_cycles);
  * Same operation, layouts and kernel as ddt_topk_logprobs, for `rows`
  * independent rows of V logits (draft_logits [rows, V], draft_dtype BF16 or
  * F32; top_lp, top_ids [rows, K]). Its scratch (each warp's (max, sum of
- * exp), each 64-logit group's max, a status word) is one fixed array in the
- * library's device memory, about 18 MB, which every GPU that loads libddt.so
- * keeps until the process exits. No call allocates or frees device memory.
+ * exp), each 64-logit group's max, each warp's best group keys, a status
+ * word) is one fixed array in the library's device memory, about 24 MB, which
+ * every GPU that loads libddt.so keeps until the process exits. No call
+ * allocates or frees device memory.
  *
  * Limits (DDT_EUNSUPPORTED beyond them, nothing enqueued), with
  * chunks = ceil(V / 16384) for bf16 and ceil(V / 8192) for fp32:
