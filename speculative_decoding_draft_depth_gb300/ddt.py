@@ -237,15 +237,7 @@ class Context:
         att_events: optional (begin, end) torch.cuda.Event pair, recorded by
         the library around the attention launch (each already created, e.g.
         by one earlier record())."""
-        a = RoundArgs()
-        a.R = R
-        for name, _ in RoundArgs._fields_[1:]:
-            if name.startswith("att_event"):
-                continue
-            setattr(a, name, _ptr(bufs.get(name)))
-        if att_events is not None:
-            a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
-            a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
+        a = self._round_args(R, bufs, att_events)
         _check(_lib.ddt_round(self._h, ctypes.byref(a), _stream(stream)), "ddt_round")
 
     def ddt_markov_table(self, draft_logits, W, E, anchors, R, cand_ids, tab_lp, stream=None):
@@ -268,6 +260,8 @@ class Context:
                                      _stream(stream)), "ddt_round_markov")
 
     def _round_args(self, R, bufs, att_events):
+        """ddt_round_args from a dict of tensors named like its fields (absent
+        ones are NULL) and the optional attention event pair."""
         a = RoundArgs()
         a.R = R
         for name, _ in RoundArgs._fields_[1:]:
@@ -283,15 +277,7 @@ class Context:
         """The parent-conditioned round: bufs as for ddt_round (draft_logits are
         the backbone's per-depth logits; top_lp / top_ids unused), W, E [V, H]
         bf16 and anchors [R] int32."""
-        a = RoundArgs()
-        a.R = R
-        for name, _ in RoundArgs._fields_[1:]:
-            if name.startswith("att_event"):
-                continue
-            setattr(a, name, _ptr(bufs.get(name)))
-        if att_events is not None:
-            a.att_event_begin = ctypes.c_void_p(att_events[0].cuda_event)
-            a.att_event_end = ctypes.c_void_p(att_events[1].cuda_event)
+        a = self._round_args(R, bufs, att_events)
         _check(_lib.ddt_round_conditioned(self._h, ctypes.byref(a), _ptr(W), _ptr(E), _ptr(anchors),
                                           _stream(stream)), "ddt_round_conditioned")
 
