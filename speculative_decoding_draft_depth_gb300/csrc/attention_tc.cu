@@ -1049,8 +1049,10 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 // ---------------------------------------------------------------- split combine
 // After the main kernel: one CTA per (share boundary, KV head). A boundary
 // that falls inside a (request, row group) run of tiles split that run; the
-// CTA of the first such boundary combines the run's partials (one per share
-// that holds a segment of it) into the output rows.
+// CTAs of the boundaries that cut a run combine its partials (one per share
+// that holds a segment of it) into the output rows, each taking an equal
+// block of the rows (a short run cut once: one CTA; a long run over many
+// shares, as with one request: many CTAs).
 constexpr int CB_THREADS = 512;
 constexpr int CB_SEGS = 16;  // segment weights held per combine pass
 
@@ -1061,7 +1063,7 @@ att_combine_kernel(const TcArgs a, int NG)
     __shared__ float s_fac[CB_SEGS * ATT_ROWS];
     __shared__ int s_slots[512];
     __shared__ long long s_ps, s_T;
-    __shared__ int s_r, s_rg, s_go, s_ns;
+    __shared__ int s_r, s_rg, s_go, s_ns, s_j, s_nb;
     const int tid = threadIdx.x, lane = tid & 31;
     const int bnd = blockIdx.x / a.Hkv + 1, g = blockIdx.x % a.Hkv;
     if (tid < 32) {
@@ -1097,8 +1099,11 @@ att_combine_kernel(const TcArgs a, int NG)
                     s_rg = rg;
                     s_ps = ps;
                     s_T = T;
-                    // cut inside the run, and the first boundary that cuts it
-                    s_go = (t > ps && bnd == share_of(ps, T, NG) + 1) ? 1 : 0;
+                    // cut inside the run: boundary j of the nb that cut it
+                    const int c0 = share_of(ps, T, NG);
+                    s_go = (t > ps) ? 1 : 0;
+                    s_j = bnd - c0 - 1;
+                    s_nb = share_of(ps + tp - 1, T, NG) - c0;
                     break;
                 }
                 acc += span;
@@ -1122,15 +1127,19 @@ att_combine_kernel(const TcArgs a, int NG)
     const int ns = s_ns;
     const int PG = a.P * a.G;
     const int nrows = TILE + ((rg == 0 && a.tail_rows > 0) ? a.tail_rows : 0);
+    // this CTA's block of the run's rows
+    const int rlo = (int)((long long)s_j * nrows / s_nb), rhi = (int)((long long)(s_j + 1) * nrows / s_nb);
+    const int nlr = rhi - rlo;
     for (int s0 = 0; s0 < ns; s0 += CB_SEGS) {
         const int sn = min(CB_SEGS, ns - s0);
         // per row: every segment's weight exp2(m_s - M) / L (the pairs of up to
         // CB_SEGS segments loaded at once)
-        if (tid < nrows) {
+        if (tid < nlr) {
+            const int row = rlo + tid;
             float2 ml[CB_SEGS];
 #pragma unroll
             for (int s = 0; s < CB_SEGS; ++s)
-                ml[s] = (s0 + s < ns) ? __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + tid])
+                ml[s] = (s0 + s < ns) ? __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + row])
                                       : make_float2(DDT_NEG_INF, 0.f);
             float M = DDT_NEG_INF, Ls = 0.f;
             if (ns <= CB_SEGS) {
@@ -1142,9 +1151,9 @@ att_combine_kernel(const TcArgs a, int NG)
                     Ls += (ml[s].x == DDT_NEG_INF) ? 0.f : ml[s].y * ex2(ml[s].x - M);
             } else {
                 for (int s = 0; s < ns; ++s)
-                    M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]).x);
+                    M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + row]).x);
                 for (int s = 0; s < ns; ++s) {
-                    const float2 v = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + tid]);
+                    const float2 v = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + row]);
                     Ls += (v.x == DDT_NEG_INF) ? 0.f : v.y * ex2(v.x - M);
                 }
             }
@@ -1167,10 +1176,10 @@ att_combine_kernel(const TcArgs a, int NG)
                 reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slots[s0 + s] * ATT_ROWS * D);
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
-                const int e = tid + u * CB_THREADS, rho = e / C4;
-                if (rho < nrows) {
-                    const float f = s_fac[s * ATT_ROWS + rho];
-                    const float4 v = __ldcg(po + e);
+                const int e = tid + u * CB_THREADS, lr = e / C4;
+                if (lr < nlr) {
+                    const float f = s_fac[s * ATT_ROWS + lr];
+                    const float4 v = __ldcg(po + (rlo + lr) * C4 + e % C4);
                     acc[u].x += v.x * f;
                     acc[u].y += v.y * f;
                     acc[u].z += v.z * f;
@@ -1180,9 +1189,10 @@ att_combine_kernel(const TcArgs a, int NG)
         }
 #pragma unroll
         for (int u = 0; u < PER; ++u) {
-            const int e = tid + u * CB_THREADS, rho = e / C4, d4 = (e % C4) * 4;
-            if (rho >= nrows)
+            const int e = tid + u * CB_THREADS, lr = e / C4, d4 = (e % C4) * 4;
+            if (lr >= nlr)
                 continue;
+            const int rho = rlo + lr;
             const int gr2 = (rho < TILE) ? rg * TILE + rho : a.n_main * TILE + (rho - TILE);
             if (gr2 >= PG)
                 continue;
