@@ -1061,6 +1061,7 @@ __global__ void __launch_bounds__(CB_THREADS)
 att_combine_kernel(const TcArgs a, int NG)
 {
     __shared__ float s_fac[CB_SEGS * ATT_ROWS];
+    __shared__ float s_M[ATT_ROWS], s_inv[ATT_ROWS];
     __shared__ int s_slots[512];
     __shared__ long long s_ps, s_T;
     __shared__ int s_r, s_rg, s_go, s_ns, s_j, s_nb;
@@ -1118,9 +1119,17 @@ att_combine_kernel(const TcArgs a, int NG)
     if (tid == 0) {
         const int c0 = share_of(ps, T, NG), c1 = share_of(pe - 1, T, NG);
         int ns = 0;
-        for (int c = c0; c <= c1; ++c)
-            if (share_start(T, c, NG) < share_start(T, c + 1, NG))
-                s_slots[ns++] = part_slot(ps, T, c, NG, g, a.Hkv);
+        if (T >= NG) {
+            // every share holds tiles: the first segment of every share after
+            // c0, and of c0 only when the run starts its share
+            const bool first = (ps == share_start(T, c0, NG));
+            for (int c = c0; c <= c1; ++c)
+                s_slots[ns++] = 2 * (c * a.Hkv + g) + ((c == c0 && !first) ? 1 : 0);
+        } else {
+            for (int c = c0; c <= c1; ++c)
+                if (share_start(T, c, NG) < share_start(T, c + 1, NG))
+                    s_slots[ns++] = part_slot(ps, T, c, NG, g, a.Hkv);
+        }
         s_ns = ns;
     }
     __syncthreads();
@@ -1130,34 +1139,43 @@ att_combine_kernel(const TcArgs a, int NG)
     // this CTA's block of the run's rows
     const int rlo = (int)((long long)s_j * nrows / s_nb), rhi = (int)((long long)(s_j + 1) * nrows / s_nb);
     const int nlr = rhi - rlo;
-    for (int s0 = 0; s0 < ns; s0 += CB_SEGS) {
-        const int sn = min(CB_SEGS, ns - s0);
-        // per row: every segment's weight exp2(m_s - M) / L (the pairs of up to
-        // CB_SEGS segments loaded at once)
-        if (tid < nlr) {
-            const int row = rlo + tid;
+    // per row: the largest m and the total weight over every segment, CB_SEGS
+    // segments' (m, l) loaded at once and merged into a running pair
+    if (tid < nlr) {
+        const int row = rlo + tid;
+        float M = DDT_NEG_INF, Ls = 0.f;
+        for (int b0 = 0; b0 < ns; b0 += CB_SEGS) {
             float2 ml[CB_SEGS];
 #pragma unroll
             for (int s = 0; s < CB_SEGS; ++s)
-                ml[s] = (s0 + s < ns) ? __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + row])
+                ml[s] = (b0 + s < ns) ? __ldcg(&a.part_ml[(int64_t)s_slots[b0 + s] * ATT_ROWS + row])
                                       : make_float2(DDT_NEG_INF, 0.f);
-            float M = DDT_NEG_INF, Ls = 0.f;
-            if (ns <= CB_SEGS) {
+            float Mn = M;
 #pragma unroll
-                for (int s = 0; s < CB_SEGS; ++s)
-                    M = fmaxf(M, ml[s].x);
+            for (int s = 0; s < CB_SEGS; ++s)
+                Mn = fmaxf(Mn, ml[s].x);
+            float Lb = 0.f;
 #pragma unroll
-                for (int s = 0; s < CB_SEGS; ++s)
-                    Ls += (ml[s].x == DDT_NEG_INF) ? 0.f : ml[s].y * ex2(ml[s].x - M);
-            } else {
-                for (int s = 0; s < ns; ++s)
-                    M = fmaxf(M, __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + row]).x);
-                for (int s = 0; s < ns; ++s) {
-                    const float2 v = __ldcg(&a.part_ml[(int64_t)s_slots[s] * ATT_ROWS + row]);
-                    Ls += (v.x == DDT_NEG_INF) ? 0.f : v.y * ex2(v.x - M);
-                }
-            }
-            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+            for (int s = 0; s < CB_SEGS; ++s)
+                Lb += (ml[s].x == DDT_NEG_INF) ? 0.f : ml[s].y * ex2(ml[s].x - Mn);
+            Ls = ((M == DDT_NEG_INF) ? 0.f : Ls * ex2(M - Mn)) + Lb;
+            M = Mn;
+        }
+        s_M[tid] = M;
+        s_inv[tid] = (Ls > 0.f) ? 1.f / Ls : 0.f;
+    }
+    __syncthreads();
+    for (int s0 = 0; s0 < ns; s0 += CB_SEGS) {
+        const int sn = min(CB_SEGS, ns - s0);
+        // per row: every segment's weight exp2(m_s - M) / L
+        if (tid < nlr) {
+            const int row = rlo + tid;
+            const float M = s_M[tid], inv = s_inv[tid];
+            float2 ml[CB_SEGS];
+#pragma unroll
+            for (int s = 0; s < CB_SEGS; ++s)
+                ml[s] = (s < sn) ? __ldcg(&a.part_ml[(int64_t)s_slots[s0 + s] * ATT_ROWS + row])
+                                 : make_float2(DDT_NEG_INF, 0.f);
 #pragma unroll
             for (int s = 0; s < CB_SEGS; ++s)
                 if (s < sn)
@@ -1171,19 +1189,30 @@ att_combine_kernel(const TcArgs a, int NG)
 #pragma unroll
         for (int u = 0; u < PER; ++u)
             acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s = 0; s < sn; ++s) {
-            const float4 *po =
-                reinterpret_cast<const float4 *>(a.part_o + (int64_t)s_slots[s0 + s] * ATT_ROWS * D);
+        // four segments at a time: their loads are independent and in flight together
+        for (int s = 0; s < sn; s += 4) {
+            const float4 *po[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                po[q] = reinterpret_cast<const float4 *>(
+                    a.part_o + (int64_t)s_slots[s0 + min(s + q, sn - 1)] * ATT_ROWS * D);
 #pragma unroll
             for (int u = 0; u < PER; ++u) {
                 const int e = tid + u * CB_THREADS, lr = e / C4;
                 if (lr < nlr) {
-                    const float f = s_fac[s * ATT_ROWS + lr];
-                    const float4 v = __ldcg(po + (rlo + lr) * C4 + e % C4);
-                    acc[u].x += v.x * f;
-                    acc[u].y += v.y * f;
-                    acc[u].z += v.z * f;
-                    acc[u].w += v.w * f;
+                    const int off = (rlo + lr) * C4 + e % C4;
+                    float4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        v[q] = __ldcg(po[q] + off);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float f = (s + q < sn) ? s_fac[(s + q) * ATT_ROWS + lr] : 0.f;
+                        acc[u].x += v[q].x * f;
+                        acc[u].y += v[q].y * f;
+                        acc[u].z += v[q].z * f;
+                        acc[u].w += v[q].w * f;
+                    }
                 }
             }
         }
