@@ -535,7 +535,8 @@ DDT_DEVINL uint64_t warp_best_below(const uint64_t *k, uint64_t bound, int lane,
     return (who != 0u) ? w : 0ull;
 }
 
-constexpr int SLOTS = 4;  // frontier slots per lane: 128 >= B entries
+// frontier slots per lane: a template parameter, ceil(B / 32) (each pop adds
+// at most one entry, so B entries fit)
 
 DDT_DEVINL void prefetch_l1(const void *p)
 {
@@ -550,6 +551,7 @@ struct TreeArgs {
     uint32_t *mask;
 };
 
+template <int SLOTS>
 __global__ void __launch_bounds__(32)
 mk_tree_kernel(const TreeArgs a)
 {
@@ -848,13 +850,19 @@ cudaError_t launch_markov_tree(const ddt_ctx *c, const int32_t *cand, const floa
 {
     const ddt_config &cfg = c->cfg;
     const size_t smem = tree_smem(cfg.L, cfg.prefilter, cfg.B);
-    static size_t attr = 0;
+    static bool attr = false;
     cudaError_t e;
-    if (attr < 200 * 1024) {
-        if ((e = cudaFuncSetAttribute(mk_tree_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!attr) {
+        if ((e = cudaFuncSetAttribute(mk_tree_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      200 * 1024)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(mk_tree_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      200 * 1024)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(mk_tree_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      200 * 1024)) != cudaSuccess ||
+            (e = cudaFuncSetAttribute(mk_tree_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       200 * 1024)) != cudaSuccess)
             return e;
-        attr = 200 * 1024;
+        attr = true;
     }
     TreeArgs a;
     a.cand = cand;
@@ -867,6 +875,14 @@ cudaError_t launch_markov_tree(const ddt_ctx *c, const int32_t *cand, const floa
     a.depths = depths;
     a.n_nodes = n_nodes;
     a.mask = mask;
-    mk_tree_kernel<<<R, 32, smem, s>>>(a);
+    const int slots = (cfg.B + 31) / 32;  // 1..4 (B <= 127)
+    if (slots <= 1)
+        mk_tree_kernel<1><<<R, 32, smem, s>>>(a);
+    else if (slots == 2)
+        mk_tree_kernel<2><<<R, 32, smem, s>>>(a);
+    else if (slots == 3)
+        mk_tree_kernel<3><<<R, 32, smem, s>>>(a);
+    else
+        mk_tree_kernel<4><<<R, 32, smem, s>>>(a);
     return cudaGetLastError();
 }

@@ -23,7 +23,10 @@
 
 namespace {
 
-constexpr int SLOTS = 4;  // frontier slots per lane: 128 >= B entries
+// Frontier slots per lane (a template parameter of the kernel): each pop
+// frees its entry's slot or reuses it for the sibling and adds at most one
+// child, so before the i-th pop at most i entries are live and B entries in
+// total fit 32 * ceil(B / 32) slots.
 
 DDT_DEVINL void field_or(uint64_t &hi, uint64_t &lo, int i, uint64_t val)
 {
@@ -71,6 +74,7 @@ DDT_DEVINL unsigned keep_max(unsigned cand, uint32_t v, int lane)
     return cand & __ballot_sync(0xFFFFFFFFu, v == m);
 }
 
+template <int SLOTS>
 __global__ void __launch_bounds__(32)
 build_tree_kernel(const float *__restrict__ top_lp, const int32_t *__restrict__ top_ids, int L,
                   int K, int B, int32_t *__restrict__ tree_tokens, int32_t *__restrict__ parents,
@@ -276,8 +280,19 @@ cudaError_t launch_build_tree(const ddt_ctx *c, const float *top_lp, const int32
                               int32_t *n_nodes, uint32_t *mask, cudaStream_t s)
 {
     const ddt_config &cfg = c->cfg;
-    build_tree_kernel<<<R, 32, 0, s>>>(top_lp, top_ids, cfg.L, cfg.K, cfg.B, tree_tokens, parents,
-                                       depths, n_nodes, mask);
+    const int slots = (cfg.B + 31) / 32;  // 1..4 (B <= 127)
+    if (slots <= 1)
+        build_tree_kernel<1><<<R, 32, 0, s>>>(top_lp, top_ids, cfg.L, cfg.K, cfg.B, tree_tokens, parents,
+                                              depths, n_nodes, mask);
+    else if (slots == 2)
+        build_tree_kernel<2><<<R, 32, 0, s>>>(top_lp, top_ids, cfg.L, cfg.K, cfg.B, tree_tokens, parents,
+                                              depths, n_nodes, mask);
+    else if (slots == 3)
+        build_tree_kernel<3><<<R, 32, 0, s>>>(top_lp, top_ids, cfg.L, cfg.K, cfg.B, tree_tokens, parents,
+                                              depths, n_nodes, mask);
+    else
+        build_tree_kernel<4><<<R, 32, 0, s>>>(top_lp, top_ids, cfg.L, cfg.K, cfg.B, tree_tokens, parents,
+                                              depths, n_nodes, mask);
     return cudaGetLastError();
 }
 
