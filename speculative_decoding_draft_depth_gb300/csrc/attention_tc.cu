@@ -1114,6 +1114,9 @@ att_combine_kernel(const TcArgs a, int NG)
     __syncthreads();
     if (!s_go)
         return;
+    // launched as a programmatic dependent of the main kernel: its partials are
+    // read only after it has completed (the lookup above reads inputs only)
+    pdl_wait();
     const long long T = s_T, ps = s_ps, pe = ps + pair_tiles(a, s_r);
     const int r = s_r, rg = s_rg;
     if (tid == 0) {
@@ -1397,9 +1400,19 @@ cudaError_t launch_attention(ddt_ctx *c, const uint16_t *q, const uint16_t *k_tr
                         : launch_tq<16, 64>(grid, tq, tqt, tk, tv, tkt, tvt, a, s);
     if (e != cudaSuccess || groups == 1)
         return e;
+    // the merge of split runs, a programmatic dependent of the main kernel (its
+    // launch is staged while the main kernel's last CTAs finish)
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((groups - 1) * cfg.Hkv);
+    lc.blockDim = dim3(CB_THREADS);
+    lc.dynamicSmemBytes = 0;
+    lc.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = at;
+    lc.numAttrs = 1;
     if (d == 128)
-        att_combine_kernel<128><<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
-    else
-        att_combine_kernel<64><<<(groups - 1) * cfg.Hkv, CB_THREADS, 0, s>>>(a, groups);
-    return cudaGetLastError();
+        return cudaLaunchKernelEx(&lc, att_combine_kernel<128>, a, groups);
+    return cudaLaunchKernelEx(&lc, att_combine_kernel<64>, a, groups);
 }
