@@ -35,8 +35,11 @@
 //  * warps 0-15: main-row softmax and epilogue, four warps per TMEM lane
 //    quarter, each on 32 of the 128 columns; warps 16-19: tail-row softmax;
 //    warp 20: walks the CTA's share and loads Q and K; warp 21: V loads; warp 22: TMEM
-//    owner and MMA issuer, which polls its barriers and issues whichever of
-//    the next Q K^T and the next P V is ready.
+//    owner and MMA issuer of the main rows, which polls its barriers and issues
+//    whichever of the next Q K^T and the next P V is ready; warp 23: the same
+//    for the tail rows' products (a second issuing thread on another scheduler:
+//    the issue of the main and the tail MMAs overlaps, and a K / V / Q slot
+//    frees once both issuers have released it).
 //  * softmax in the base-2 domain with a lazily updated reference max: O and
 //    l are rescaled only when a row's max grows by more than 2^8. A tile's
 //    exponentials are computed against the current reference before the four
@@ -59,10 +62,10 @@ namespace {
 constexpr int TILE = 128;
 constexpr int NMAIN = 512;                // main-row softmax threads (warps 0-15)
 constexpr int NTAILT = 128;               // tail-row softmax threads (warps 16-19)
-constexpr int W_TAIL0 = 16, W_KPROD = 20, W_VPROD = 21, W_MMA = 22;
-constexpr int NTHREADS = 23 * 32;
+constexpr int W_TAIL0 = 16, W_KPROD = 20, W_VPROD = 21, W_MMA = 22, W_MMAT = 23;
+constexpr int NTHREADS = 24 * 32;
 constexpr int NRING = 4;                  // ring of segments handed from the walker to the other roles
-constexpr int RING_CONSUMERS = 1 + 1 + 16 + 4;  // V loader, MMA, main warps, tail warps
+constexpr int RING_CONSUMERS = 1 + 2 + 16 + 4;  // V loader, two MMA issuers, main warps, tail warps
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TM_S = 0;     // two S buffers (P overwrites their first columns)
 constexpr uint32_t TM_O = 256;   // O main: 128 columns
@@ -108,6 +111,7 @@ constexpr uint32_t B_QFULL = 0, B_QEMPTY = 16,
                    B_TMEM = 400, B_ABORT = 404,
                    B_RING = 416,    // [NRING][4] ints: segments (x = -1: end of the share)
                    B_TOTAL = 480,   // int: T, the batch's total tiles
+                   B_FINALT = 488,  // the tail issuer's wind-down
                    B_DEBUG = 496,   // a barrier nothing arrives at (the armed test wait)
                    B_RED = 512,     // 2 x [4 warps][16] floats: tail column max
                    B_SUM = 1024,    // 2 x [4 warps][16] floats: tail sums
@@ -340,7 +344,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar + B_QFULL + 8 * i, 1);
-            mbar_init(bar + B_QEMPTY + 8 * i, 1);
+            mbar_init(bar + B_QEMPTY + 8 * i, 2);  // both issuers
 
 
             mbar_init(bar + B_SFULL + 8 * i, 1);
@@ -351,11 +355,11 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         for (int i = 0; i < NKS; ++i) {
             mbar_init(bar + B_KFULL + 8 * i, 1);
-            mbar_init(bar + B_KEMPTY + 8 * i, 1);
+            mbar_init(bar + B_KEMPTY + 8 * i, 2);  // both issuers
         }
         for (int i = 0; i < NVS; ++i) {
             mbar_init(bar + B_VFULL + 8 * i, 1);
-            mbar_init(bar + B_VEMPTY + 8 * i, 1);
+            mbar_init(bar + B_VEMPTY + 8 * i, 2);  // both issuers
         }
         for (int i = 0; i < NRING; ++i) {
             mbar_init(bar + B_RFULL + 8 * i, 1);
@@ -369,6 +373,7 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(bar + B_ODONE, 1);
         mbar_init(bar + B_OTDONE, 1);
         mbar_init(bar + B_FINAL, 1);
+        mbar_init(bar + B_FINALT, 1);
         mbar_init(bar + B_DEBUG, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -558,9 +563,14 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int m = vn - NVS; m < vn; ++m)
             if (m >= 0)
                 drain_bar(bar + B_VFULL + 8 * (m % NVS), (m / NVS) & 1);
-    } else if (warp == W_MMA) {
-        // ============================================================ MMA issuer
+    } else if (warp == W_MMA || warp == W_MMAT) {
+        // ============================================================ MMA issuers
+        // (warp W_MMA: the main rows' products; warp W_MMAT: the tail rows'.
+        // Both walk every tile of the share; the tail issuer releases the
+        // slots of tiles without tail rows by a plain arrival, after the slot's
+        // fill it waited for, so its arrivals never run a phase ahead.)
         if (lane == 0) {
+            const bool tailw = (warp == W_MMAT);
             const uint64_t dK0 = sdesc_sw128(sb + SM_K, 16, 1024);
             const uint64_t dV0 = sdesc_sw128(sb + SM_V, 16384, 1024);
             const uint64_t dQ0 = sdesc_sw128(sb + SM_Q, 16, 1024);
@@ -622,13 +632,14 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         const uint64_t dK = dK0 + ks * (32768u >> 4);
                         const uint64_t dQ = dQ0 + qs * (QSLOT >> 4);
                         const uint32_t s_t = tmem + TM_S + 128u * sl;
+                        if (!tailw) {
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
-                            mma_bf16(s_t, dQ + off, dK + off, IDESC_QK, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar + B_SFULL + 8 * sl);
-                        if (qi.has_tail) {
+                            for (int kk = 0; kk < D / 16; ++kk) {
+                                const uint32_t off = ((kk >> 2) * 16384u + (kk & 3) * 32u) >> 4;
+                                mma_bf16(s_t, dQ + off, dK + off, IDESC_QK, kk > 0 ? 1u : 0u);
+                            }
+                            mma_commit(bar + B_SFULL + 8 * sl);
+                        } else if (qi.has_tail) {
                             const uint32_t st_t = tmem + TM_ST + 16u * (qt_n & 1);
                             const uint64_t dQT = dQ + (32768u >> 4);
 #pragma unroll
@@ -640,10 +651,20 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             mma_commit(bar + B_STFULL + 8 * (qt_n & 1));
                             ++qt_n;
                         }
-                        mma_commit(bar + B_KEMPTY + 8 * ks);
+                        // the K slot (and at the item's end the Q slot) is free once
+                        // these MMAs completed; the tail issuer with nothing to do
+                        // here releases it at once
+                        const bool issued = !tailw || qi.has_tail;
+                        if (issued)
+                            mma_commit(bar + B_KEMPTY + 8 * ks);
+                        else
+                            mbar_arrive(bar + B_KEMPTY + 8 * ks);
                         ++qk_n;
                         if (++qk_j == qi.ntiles) {
-                            mma_commit(bar + B_QEMPTY + 8 * qs);
+                            if (issued)
+                                mma_commit(bar + B_QEMPTY + 8 * qs);
+                            else
+                                mbar_arrive(bar + B_QEMPTY + 8 * qs);
                             ++qk_k;
                             qk_state = 0;
                         }
@@ -653,21 +674,25 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 // ---- P V of tile pv_n: its P (and tail P) and V are ready
                 if (pv_state == 1 && pv_n < qk_n) {
                     const int sl = pv_n & 1, vs = pv_n % NVS;
-                    if (mbar_test_wait(bar + B_PFULL + 8 * sl, (pv_n >> 1) & 1) &&
-                        mbar_test_wait(bar + B_VFULL + 8 * vs, (pv_n / NVS) & 1) &&
-                        (!pi.has_tail ||
-                         mbar_test_wait(bar + B_PTFULL + 8 * (pt_n & 1), (pt_n >> 1) & 1))) {
+                    const bool ready =
+                        tailw ? (mbar_test_wait(bar + B_VFULL + 8 * vs, (pv_n / NVS) & 1) &&
+                                 (!pi.has_tail ||
+                                  mbar_test_wait(bar + B_PTFULL + 8 * (pt_n & 1), (pt_n >> 1) & 1)))
+                              : (mbar_test_wait(bar + B_PFULL + 8 * sl, (pv_n >> 1) & 1) &&
+                                 mbar_test_wait(bar + B_VFULL + 8 * vs, (pv_n / NVS) & 1));
+                    if (ready) {
                         tc_fence_after();
                         const uint64_t dV = dV0 + vs * (32768u >> 4);
                         const uint32_t p_t = tmem + TM_S + 128u * sl;
+                        if (!tailw) {
 #pragma unroll
-                        for (int kt = 0; kt < 8; ++kt) {
-                            const uint32_t acc = (pv_j > 0 || kt > 0) ? 1u : 0u;
-                            mma_bf16_ts(tmem + TM_O, p_t + 32u * (kt >> 1) + 8u * (kt & 1),
-                                        dV + kt * (2048u >> 4), IDESC_PV<D>, acc);
-                        }
-                        mma_commit(bar + B_ODONE);
-                        if (pi.has_tail) {
+                            for (int kt = 0; kt < 8; ++kt) {
+                                const uint32_t acc = (pv_j > 0 || kt > 0) ? 1u : 0u;
+                                mma_bf16_ts(tmem + TM_O, p_t + 32u * (kt >> 1) + 8u * (kt & 1),
+                                            dV + kt * (2048u >> 4), IDESC_PV<D>, acc);
+                            }
+                            mma_commit(bar + B_ODONE);
+                        } else if (pi.has_tail) {
                             // O_t^T has M = 128 lanes; for D = 64 the upper 64 read the
                             // stage's unused half (in bounds) and are never read back
                             const uint64_t dPT = dPT0 + (pt_n & 1) * (4096u >> 4);
@@ -680,7 +705,10 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                             mma_commit(bar + B_OTDONE);
                             ++pt_n;
                         }
-                        mma_commit(bar + B_VEMPTY + 8 * vs);
+                        if (!tailw || pi.has_tail)
+                            mma_commit(bar + B_VEMPTY + 8 * vs);
+                        else
+                            mbar_arrive(bar + B_VEMPTY + 8 * vs);
                         ++pv_n;
                         if (++pv_j == pi.ntiles) {
                             ++pv_k;
@@ -700,8 +728,9 @@ att_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             }
             (void)failed;
             // wind down: every MMA issued here has completed
-            mma_commit(bar + B_FINAL);
-            drain_bar(bar + B_FINAL, 0);
+            const uint32_t fin = bar + (tailw ? B_FINALT : B_FINAL);
+            mma_commit(fin);
+            drain_bar(fin, 0);
         }
         __syncwarp();
     } else if (warp < W_TAIL0) {
