@@ -29,7 +29,7 @@ CASES = {
     "single_ctx128": dict(name="single", V=4096, ctx_args=(128,), seed=52),
     "mid": dict(name="batch64", R=5, ctx_args=(1, 9000), seed=41),
     "wide_small": dict(name="wide256", R=6, rounds=1, ctx_args=(3000, 1.0, 9000), seed=43),
-    # two row groups per KV head at head dim 64 (the row-group CTAs share K / V loads)
+    # two row groups per KV head at head dim 64 (one run of tiles per row group)
     "wide_d64": dict(name="wide256", R=4, V=4096, d=64, rounds=1, ctx_args=(2000, 1.0, 6000),
                      seed=44),
     # three row groups (P * G = 388 rows): each row-group CTA loads its own K / V
