@@ -52,7 +52,9 @@
  *     config says; their pointers are const void*.
  *   - All tensors are dense row-major with the shapes given below; no
  *     strides are accepted. Vectorised paths need 16-byte-aligned base
- *     pointers; unaligned ones are rejected with DDT_EINVAL.
+ *     pointers; every other pointer needs its element's alignment (4 bytes
+ *     for i32 and f32, 8 for f64). Unaligned ones are rejected with
+ *     DDT_EINVAL.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Every
  *     call only enqueues work on it and returns; none synchronises the host
  *     except ddt_device_status. One context must not be used by two streams

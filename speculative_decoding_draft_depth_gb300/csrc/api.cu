@@ -138,6 +138,7 @@ Layout layout_for(const ddt_config &c)
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool aligned4(const void *p) { return ((uintptr_t)p & 3u) == 0; }
+bool aligned8(const void *p) { return ((uintptr_t)p & 7u) == 0; }
 
 ddt_status check_R(const ddt_ctx *ctx, int32_t R)
 {
@@ -203,6 +204,8 @@ ddt_status chk_walk(const int32_t *tok, const int32_t *par, const int32_t *nn, c
                     const int32_t *an, const int32_t *at, const int32_t *bo)
 {
     DDT_CHECK(tok && par && nn && al && an && at && bo);
+    DDT_CHECK(aligned4(tok) && aligned4(par) && aligned4(nn) && aligned4(al) && aligned4(an) &&
+              aligned4(at) && aligned4(bo));
     return DDT_OK;
 }
 
@@ -210,7 +213,8 @@ ddt_status chk_compact(const uint16_t *kc, const uint16_t *vc, const int32_t *bt
                        const int32_t *cl, const uint16_t *kt, const uint16_t *vt)
 {
     DDT_CHECK(kc && vc && bt && cl && kt && vt);
-    DDT_CHECK(aligned16(kc) && aligned16(vc) && aligned16(kt) && aligned16(vt));
+    DDT_CHECK(aligned16(kc) && aligned16(vc) && aligned16(kt) && aligned16(vt) && aligned4(bt) &&
+              aligned4(cl));
     return DDT_OK;
 }
 
@@ -483,8 +487,9 @@ ddt_status ddt_walk(ddt_ctx *ctx, const int32_t *argmax, const int32_t *tree_tok
         return st;
     if (R == 0)
         return DDT_OK;
-    if (!argmax || (st = chk_walk(tree_tokens, parents, n_nodes, acc_len, acc_nodes, acc_tokens,
-                                  bonus)) != DDT_OK)
+    if (!argmax || !aligned4(argmax) ||
+        (st = chk_walk(tree_tokens, parents, n_nodes, acc_len, acc_nodes, acc_tokens, bonus)) !=
+            DDT_OK)
         return DDT_EINVAL;
     if ((st = set_device(ctx)) != DDT_OK)
         return st;
@@ -505,7 +510,7 @@ ddt_status ddt_compact(ddt_ctx *ctx, uint16_t *k_cache, uint16_t *v_cache,
         return st;
     if (R == 0)
         return DDT_OK;
-    if (!acc_nodes || !acc_len ||
+    if (!acc_nodes || !acc_len || !aligned4(acc_nodes) || !aligned4(acc_len) ||
         (st = chk_compact(k_cache, v_cache, block_table, ctx_lens, k_tree, v_tree)) != DDT_OK)
         return DDT_EINVAL;
     if ((st = set_device(ctx)) != DDT_OK)
@@ -529,7 +534,7 @@ ddt_status ddt_accept(ddt_ctx *ctx, const void *target_logits, const int32_t *tr
         return st;
     if (R == 0)
         return DDT_OK;
-    if (!target_logits || !aligned16(target_logits))
+    if (!target_logits || !aligned16(target_logits) || (argmax_out && !aligned4(argmax_out)))
         return DDT_EINVAL;
     if ((st = chk_walk(tree_tokens, parents, n_nodes, acc_len, acc_nodes, acc_tokens, bonus)) !=
             DDT_OK ||
@@ -557,6 +562,8 @@ ddt_status ddt_accept_stochastic(ddt_ctx *ctx, const void *draft_logits,
         return DDT_OK;
     if (!draft_logits || !target_logits || !draft_tokens || !u || !r || !acc_len || !acc_tokens)
         return DDT_EINVAL;
+    DDT_CHECK(aligned4(draft_tokens) && aligned4(u) && aligned4(r) && aligned4(acc_len) &&
+              aligned4(acc_tokens) && (!n_guess || aligned4(n_guess)));
     if ((st = set_device(ctx)) != DDT_OK)
         return st;
     DDT_TRY(launch_accept_stochastic(ctx, draft_logits, target_logits, draft_tokens, u, r, R,
@@ -574,6 +581,8 @@ ddt_status ddt_schedule_prefix(ddt_ctx *ctx, const float *conf, int32_t R, const
         return DDT_OK;
     if (!conf || !cost_ms || !n_keep)
         return DDT_EINVAL;
+    DDT_CHECK(aligned4(conf) && aligned4(cost_ms) && aligned4(n_keep) &&
+              (!n_total || aligned4(n_total)) && (!stats || aligned8(stats)));
     if ((int64_t)R * ctx->cfg.L > DDT_SCHED_MAX_SLOTS)
         return DDT_EUNSUPPORTED;
     if ((st = set_device(ctx)) != DDT_OK)
@@ -627,7 +636,8 @@ ddt_status ddt_round(ddt_ctx *ctx, const ddt_round_args *a, void *stream)
         (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
                        a->acc_tokens, a->bonus)) != DDT_OK)
         return st;
-    if (!a->target_logits || !aligned16(a->target_logits))
+    if (!a->target_logits || !aligned16(a->target_logits) ||
+        (a->target_argmax && !aligned4(a->target_argmax)))
         return DDT_EINVAL;
     if ((st = set_device(ctx)) != DDT_OK)
         return st;
@@ -668,7 +678,8 @@ ddt_status ddt_round_conditioned(ddt_ctx *ctx, const ddt_round_args *a, const ui
         (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
                        a->acc_tokens, a->bonus)) != DDT_OK)
         return st;
-    if (!a->target_logits || !aligned16(a->target_logits))
+    if (!a->target_logits || !aligned16(a->target_logits) ||
+        (a->target_argmax && !aligned4(a->target_argmax)))
         return DDT_EINVAL;
     if (R * ctx->cfg.frontier > CG_NP_MAX)
         return DDT_EUNSUPPORTED;
@@ -754,7 +765,8 @@ ddt_status ddt_round_markov(ddt_ctx *ctx, const ddt_round_args *a, const uint16_
         (st = chk_walk(a->tree_tokens, a->parents, a->n_nodes, a->acc_len, a->acc_nodes,
                        a->acc_tokens, a->bonus)) != DDT_OK)
         return st;
-    if (!a->target_logits || !aligned16(a->target_logits))
+    if (!a->target_logits || !aligned16(a->target_logits) ||
+        (a->target_argmax && !aligned4(a->target_argmax)))
         return DDT_EINVAL;
     if ((st = set_device(ctx)) != DDT_OK)
         return st;

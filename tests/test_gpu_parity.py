@@ -8,6 +8,8 @@ stage-wise (the oracle's heap fed the GPU's fp32 log-probs, must match
 bit-for-bit including order) and end to end (oracle fp64 log-probs: prefix
 scores within 1e-6 nats count as tied and the tie band must agree).
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -280,6 +282,33 @@ def test_invalid_arguments_are_rejected_before_launch():
     with pytest.raises(ddt.DdtError):
         ctx.ddt_topk_logprobs(raw[1:], 1, lp, ids)  # misaligned logits pointer
     ctx.ddt_topk_logprobs(z, 0, lp, ids)  # R = 0 is a no-op
+
+
+def test_misaligned_element_pointers_are_rejected_before_launch():
+    """An i32, f32 or f64 array off its element alignment is rejected with
+    DDT_EINVAL before anything is enqueued. Every pointer lies inside one
+    buffer owned by the test, far from its ends."""
+    cfg = synth.config("tiny")  # R = 1, L = 4, V = 32
+    inp = synth.draw_round_inputs(cfg)
+    ctx = make_ctx(cfg, inp)
+    lib = ddt.load()
+    buf = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+
+    def at(off):
+        return ctypes.c_void_p(buf.data_ptr() + (1 << 16) + off)
+
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # scheduler: conf two bytes off; then f64 stats four bytes off
+    assert lib.ddt_schedule_prefix(ctx._h, at(2), 1, at(4096), at(8192), None, None, s) == ddt.EINVAL
+    assert lib.ddt_schedule_prefix(ctx._h, at(0), 1, at(4096), at(8192), at(12288), at(16388),
+                                   s) == ddt.EINVAL
+    # stochastic verification: the guesses two bytes off
+    assert lib.ddt_accept_stochastic(ctx._h, at(0), at(4096), at(8194), at(12288), at(16384), 1,
+                                     at(20480), at(24576), None, s) == ddt.EINVAL
+    # greedy walk: acc_len one byte off
+    assert lib.ddt_walk(ctx._h, at(0), at(4096), at(8192), at(12288), 1, at(16385), at(20480),
+                        at(24576), at(28672), s) == ddt.EINVAL
+    assert ctx.ddt_device_status() == 0
 
 
 def test_chain_tree_attention_is_causal_decode():
