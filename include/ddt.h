@@ -108,7 +108,9 @@ typedef struct ddt_config {
                                   Hq / Hkv in {1, 2, 4, 8, 16} */
     int32_t page_size;         /* tokens per KV page: a power of two, at least 16 */
     int32_t max_pages_per_req; /* row length of block_table */
-    int64_t num_pages;         /* pages in the KV pool (bounds checks) */
+    int64_t num_pages;         /* pages in the KV pool (bounds checks); at most
+                                  (2^31 - 1) / page_size, since a4 addresses the
+                                  pool's token rows with 32-bit coordinates */
     int32_t draft_dtype;       /* ddt_dtype of draft logits */
     int32_t target_dtype;      /* ddt_dtype of target logits */
     /* parent-conditioned tree (ddt_build_tree_conditioned); 0 = not used */

@@ -50,6 +50,9 @@ ddt_status check_config(const ddt_config *in, ddt_config *out)
     const int64_t max_ctx = (int64_t)c.max_pages_per_req * c.page_size;
     if (max_ctx > ATT_MAX_CTX || c.R_max > 2048)
         return DDT_EUNSUPPORTED;
+    // the pool's token rows are TMA row coordinates (signed 32-bit) in a4
+    if (c.num_pages > (int64_t)0x7FFFFFFF / c.page_size)
+        return DDT_EUNSUPPORTED;
     if (c.markov_dim < 0 || c.frontier < 0 || c.prefilter < 0)
         return DDT_EINVAL;
     if ((c.frontier > 0 || c.prefilter > 0) && c.markov_dim == 0)

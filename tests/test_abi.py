@@ -75,7 +75,9 @@ def test_workspace_bytes_and_validation(lib):
     for bad in (dict(R_max=0), dict(L=0), dict(B=0), dict(K=200, V=100), dict(Hq=30, Hkv=8),
                 dict(page_size=0), dict(num_pages=0), dict(draft_dtype=7)):
         assert ddt.workspace_bytes(_cfg(**bad)) == 0, bad
-    for unsupported in (dict(L=19), dict(B=128), dict(d=96)):
+    # a pool of 2^31 token rows or more: a4's row coordinates are 32-bit
+    assert ddt.workspace_bytes(_cfg(num_pages=(2**31 - 1) // 16)) > 0
+    for unsupported in (dict(L=19), dict(B=128), dict(d=96), dict(num_pages=2**27)):
         assert ddt.workspace_bytes(_cfg(**unsupported)) == 0, unsupported
     # the Markov-head trees: the head's width is required, and the table's
     # workspace grows with the prefilter width
