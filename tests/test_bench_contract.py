@@ -33,3 +33,37 @@ def test_reference_arm_prints_the_contract_line(capsys):
     # the same config keys as the GPU arm
     assert d["config"] == bench.config_dict(synth.config("tiny"), 0) | {"l2": d["config"]["l2"]}
     assert set(d["config"]) == {"workload", "l2", "parallelism"}
+
+
+def _batch64_contexts():
+    import numpy as np
+    from speculative_decoding_draft_depth_gb300 import synth
+    cfg = synth.config("batch64")
+    rng = np.random.default_rng(cfg.seed)
+    synth.draw_draft_logits(cfg, rng)  # the recipe draws the contexts after the logits
+    return cfg, synth.draw_ctx_lens(cfg, rng)
+
+
+def test_round_bytes_of_the_batch64_workload():
+    """The algorithmic bytes behind the roofline fractions: 2314.24 MB for
+    a4 and 3248.83 MB for the round on the seeded batch64 contexts."""
+    import bench
+    cfg, ctx = _batch64_contexts()
+    b = bench.round_bytes(cfg, ctx)
+    assert abs(b["attention"] / 1e6 - 2314.24) < 0.01
+    assert abs(b["total"] / 1e6 - 3248.83) < 0.01
+    assert b["total"] == sum(v for k, v in b.items() if k != "total")
+
+
+def test_round_bytes_context_term():
+    """One more context token costs a4 one K row and one V row of every KV
+    head (bf16) and changes no other stage."""
+    import bench
+    cfg, ctx = _batch64_contexts()
+    b0 = bench.round_bytes(cfg, ctx)
+    ctx2 = ctx.copy()
+    ctx2[5] += 1
+    b1 = bench.round_bytes(cfg, ctx2)
+    assert b1["attention"] - b0["attention"] == 2 * cfg.Hkv * cfg.d * 2
+    for k in ("topk", "tree", "accept"):
+        assert b1[k] == b0[k]
